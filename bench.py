@@ -1,0 +1,510 @@
+#!/usr/bin/env python3
+"""Benchmark of the ZeRO partitioned mixed-precision Adam step on GB300.
+
+One step = every row of the hot path for one batch of synthetic gradients:
+for each simulated partition, the N-way bucketed reduce + unscale + overflow +
+sum of squares, the global-norm/skip/loss-scale decision, the fused AdamW +
+cast into the parameter layout, and (stage 3) the forward and backward
+per-unit gathers of the N parameter shards.  All of it runs in libzero's
+kernels through the C ABI; PyTorch only allocates memory and owns the stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl gb300|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload (the baseline arm).
+"""
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "13b-zero2"
+METRIC = "partition elements/s per ZeRO step (with achieved HBM GB/s)"
+UNIT = "elements/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------- byte model
+
+def bytes_per_element(n_ranks: int):
+    """Algorithmic HBM bytes per partition element of one step.
+    reduce: N lp reads (2N) + f32 grad write (4); Adam: grad, master, m, v
+    reads (16) + master, m, v writes (12) + lp param write (2)."""
+    return {"reduce": 2 * n_ranks + 4, "adam": 30, "step": 2 * n_ranks + 34,
+            "floor": 2 * n_ranks + 26}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "zero_partitioned_mixed_flat_gb300", "csrc", "kernels.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, only while the
+    kernel source is unchanged since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[workload][kernel]
+        if e.get("kernels_cu_sha256_16") != kernel_source_hash():
+            return None
+        return e.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, enabled=True):
+        self.proc = None
+        self.enabled = enabled
+
+    def start(self):
+        if not self.enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        want = vis.split(",")[0].strip() if vis and vis.split(",")[0].strip().isdigit() else None
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        if want is not None:
+            rows = [r for r in rows if r[0].strip() == want] or rows
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower() in ("active", "1")})
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- the step
+
+class Run:
+    """Buffers and calls of one workload on this GPU."""
+
+    def __init__(self, w, part_ranks, dev):
+        import torch
+        import zero_partitioned_mixed_flat_gb300 as Z
+        from zero_partitioned_mixed_flat_gb300 import synth
+        self.torch, self.Z, self.synth = torch, Z, synth
+        self.w = w
+        self.dev = dev
+        self.ranks = part_ranks
+        self.plan = Z.ZeroPlan(-1, w.n_ranks, w.sizes, w.align, w.stage, w.unit_of_tensor, w.lp,
+                               growth_interval=w.growth_interval)
+        P = self.P = self.plan.part_len
+        self.S = w.loss_scale
+        lpd = synth.LP_DTYPES[w.lp]
+        self.slices, self.g, self.master, self.m, self.v, self.shard = {}, {}, {}, {}, {}, {}
+        scale = self.S if w.grads_times_scale else 1.0
+        for r in self.ranks:
+            keep = self.plan.keep_ranges(r)
+            sl = torch.empty((w.n_ranks, P), dtype=lpd, device=dev)
+            for j in range(w.n_ranks):
+                synth.normal_(sl[j], w.grad_std * scale, 0, 1, j, r, synth.KINDS["grad"])
+                synth.zero_outside(sl[j], keep)
+            self.slices[r] = sl
+            self.g[r] = torch.empty(P, dtype=torch.float32, device=dev)
+            self.master[r] = synth.master_init(P, w.master_std, 0, r, dev, keep)
+            self.m[r] = torch.zeros(P, dtype=torch.float32, device=dev)
+            self.v[r] = torch.zeros(P, dtype=torch.float32, device=dev)
+            if w.stage == 3:
+                self.shard[r] = torch.zeros(P, dtype=lpd, device=dev)
+        self.param = None if w.stage == 3 else torch.zeros(self.plan.psi_padded, dtype=lpd,
+                                                           device=dev)
+        self.gather_shards = None
+        if w.stage == 3 and w.gather:
+            r0 = self.ranks[0]
+            others = [synth.lp_shard(P, w.lp, w.master_std, 0, j, dev)
+                      for j in range(w.n_ranks) if j != r0]
+            self.gather_shards = others[:r0] + [self.shard[r0]] + others[r0:]
+            biggest = max(self.plan.shard_len(u) for u in range(self.plan.n_units)) * w.n_ranks
+            self.gather_out = torch.empty(biggest, dtype=lpd, device=dev)
+        self.slice_lists = {r: [self.slices[r][j] for j in range(w.n_ranks)] for r in self.ranks}
+        bucket = w.bucket_elems
+        tile = 32768
+        if bucket:
+            bucket = -(-bucket // tile) * tile
+            self.buckets = -(-P // bucket) if P else 0
+        else:
+            self.buckets = 1 if P else 0
+
+    def launches_per_step(self):
+        n = len(self.ranks)
+        gathers = 2 * self.plan.n_units if self.gather_shards is not None else 0
+        return n * self.buckets + 1 + n + gathers
+
+    def gathers(self, stream, events=None):
+        if self.gather_shards is None:
+            return
+        units = list(range(self.plan.n_units))
+        for u in units + units[::-1]:        # forward, then backward
+            self.plan.gather(u, self.gather_shards, self.gather_out, stream)
+
+    def reduce(self, stream):
+        for r in self.ranks:
+            self.plan.reduce(r, self.slice_lists[r], self.g[r], self.S, self.w.bucket_elems, stream)
+
+    def adam(self, stream):
+        w = self.w
+        for r in self.ranks:
+            out = self.shard[r] if w.stage == 3 else self.param
+            self.plan.adam(r, self.g[r], self.master[r], self.m[r], self.v[r], out, w.lr, w.beta1,
+                           w.beta2, w.eps, w.wd, int(w.adamw), self.S, w.clip, 0.0, 0, stream)
+
+    def bytes_per_step(self):
+        b = bytes_per_element(self.w.n_ranks)
+        step = b["step"] * self.P * len(self.ranks)
+        if self.gather_shards is not None:
+            step += 2 * 4 * int(sum(self.plan.unit_padded))
+        return step
+
+
+def dist_setup(n_gpus):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        return ws, rank, local, dist
+    torch.cuda.set_device(0)
+    return 1, 0, 0, None
+
+
+def cpu_baseline(run, seconds):
+    """The oracle as it stands, single-threaded, on a bounded sample of the
+    same workload: the first M elements of the first simulated partition."""
+    import numpy as np
+    import oracle
+    from zero_partitioned_mixed_flat_gb300 import synth
+    w = run.w
+    r = run.ranks[0]
+    M = min(run.P, 1 << 21)
+    if M == 0:
+        return None
+    sl = [synth.to_numpy_codes(run.slices[r][j, :M]) for j in range(w.n_ranks)]
+    master0 = run.master[r][:M].cpu().numpy().copy()
+    m = np.zeros(M, np.float32)
+    v = np.zeros(M, np.float32)
+    master = master0.copy()
+    reps, t0 = 0, time.perf_counter()
+    step, good = 0, 0
+    while True:
+        g, ss, of = oracle.reduce(sl, w.lp, run.S)
+        d = oracle.decide(ss, of, w.clip, run.S, step, good, w.growth_interval, w.beta1, w.beta2)
+        oracle.adam(g, master, m, v, w.lp, d["coef"], d["skip"], w.lr, w.beta1, w.beta2, w.eps,
+                    w.wd, int(w.adamw), d["bc1"], d["bc2"])
+        step, good = d["step"], d["good_steps"]
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or el >= 30.0:
+            break
+    return {"value": M * reps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "first %d elements of partition %d (all %d slices): reduce + decide + "
+                      "Adam, %d repetitions, %.1f s, single thread" % (M, r, w.n_ranks, reps, el)}
+
+
+def run_reference(args):
+    """Baseline arm: the CPU oracle, as it stands, timed per step on a bounded
+    sample of the workload (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from zero_partitioned_mixed_flat_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    lay = oracle.layout(w.sizes, w.n_ranks, w.align, w.stage, w.unit_of_tensor)
+    P = lay["part_len"]
+    M = min(P, 1 << 20)
+    rng = np.random.default_rng(0)
+    scale = w.loss_scale if w.grads_times_scale else 1.0
+    vals = (rng.standard_normal((w.n_ranks, M)) * w.grad_std * scale).astype(np.float32)
+    if w.lp == 0:
+        sl = list(vals.astype(np.float16).view(np.uint16))
+    else:
+        sl = list(oracle.float_to_lp(vals, 1).reshape(w.n_ranks, M))
+    master = (rng.standard_normal(M) * w.master_std).astype(np.float32)
+    m = np.zeros(M, np.float32)
+    v = np.zeros(M, np.float32)
+    step = good = 0
+
+    def one():
+        nonlocal step, good
+        g, ss, of = oracle.reduce(sl, w.lp, w.loss_scale)
+        d = oracle.decide(ss, of, w.clip, w.loss_scale, step, good, w.growth_interval,
+                          w.beta1, w.beta2)
+        oracle.adam(g, master, m, v, w.lp, d["coef"], d["skip"], w.lr, w.beta1, w.beta2, w.eps,
+                    w.wd, int(w.adamw), d["bc1"], d["bc2"])
+        step, good = d["step"], d["good_steps"]
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    value = M * args.steps / el
+    sample = ("%d of the %d elements of one partition, all %d slices, per step "
+              "(reduce + decide + Adam), single thread" % (M, P, w.n_ranks))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "sample_elements": M, "part_len": P,
+                       "n_ranks": w.n_ranks, "stage": w.stage},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import zero_partitioned_mixed_flat_gb300 as Z
+    from zero_partitioned_mixed_flat_gb300.workloads import WORKLOADS
+    Z.load()
+    ws, rank, local, dist = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    # weak scaling: every GPU owns its own partition(s) of the simulated job
+    part_ranks = [(r + rank) % w.n_ranks for r in w.ranks]
+    t_setup = time.perf_counter()
+    run = Run(w, part_ranks, dev)
+    torch.cuda.synchronize()
+    log("setup %.1f s: workload %s, P=%d, N=%d, partitions %s" %
+        (time.perf_counter() - t_setup, w.name, run.P, w.n_ranks, part_ranks))
+    stream = torch.cuda.current_stream()
+    sh = int(stream.cuda_stream)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        run.gathers(sh)
+        if evs is not None:
+            evs[1].record(stream)
+        run.reduce(sh)
+        if evs is not None:
+            evs[2].record(stream)
+        run.adam(sh)
+        if evs is not None:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(enabled=not args.no_clocks)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3 if not args.no_clocks else 0.0)
+    start.record(stream)
+    for k in range(K):
+        step(evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    res = run.plan.result()
+    if res["skipped"]:
+        log("warning: a timed step was skipped (overflow)")
+    gather_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    reduce_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    adam_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    ms_per_step = total_ms / K
+    elems = run.P * len(run.ranks)
+    value = elems * ws / (ms_per_step / 1e3)
+    peak, peak_kind = load_peaks()
+    b = bytes_per_element(w.n_ranks)
+    n_part = len(run.ranks)
+    per_call_ms = {"reduce": statistics.mean(reduce_ms) / n_part,
+                   "adam": statistics.mean(adam_ms) / n_part}
+    kernel_bytes = {"reduce": b["reduce"] * run.P, "adam": b["adam"] * run.P}
+    if run.gather_shards is not None:
+        n_gathers = 2 * run.plan.n_units
+        per_call_ms["gather"] = statistics.mean(gather_ms) / n_gathers
+        kernel_bytes["gather"] = 4 * int(sum(run.plan.unit_padded)) // run.plan.n_units
+    # dominant kernel = the one with the largest share of the step
+    share = {"reduce": statistics.mean(reduce_ms), "adam": statistics.mean(adam_ms)}
+    if run.gather_shards is not None:
+        share["gather"] = statistics.mean(gather_ms)
+    dom = max(share, key=share.get)
+    kname = {"reduce": "reduce_unscale_stats", "adam": "adam_fused_cast",
+             "gather": "gather_layer_tma"}[dom]
+    achieved = kernel_bytes[dom] / (per_call_ms[dom] / 1e3) / 1e9
+    step_gbs = run.bytes_per_step() / (ms_per_step / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                "traffic": traffic_for(kname, w.name),
+                "algorithmic_bytes_per_launch": kernel_bytes[dom],
+                "avg_launch_ms": per_call_ms[dom]}
+    kernels = {k: {"avg_ms": per_call_ms[k], "GBps": kernel_bytes[k] / (per_call_ms[k] / 1e3) / 1e9,
+                   "frac_of_peak": kernel_bytes[k] / (per_call_ms[k] / 1e3) / 1e9 / peak}
+               for k in per_call_ms}
+
+    # ---- end to end through the ABI, host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(run, args.e2e_steps, stream, sh, ws, dist, dev)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(run, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": w.name, "psi": int(sum(w.sizes)),
+                           "n_ranks": w.n_ranks, "stage": w.stage,
+                           "lp": ["fp16", "bf16"][w.lp], "part_len": run.P,
+                           "partitions_per_gpu": len(run.ranks),
+                           "bucket_elems": w.bucket_elems,
+                           "l2": "inputs larger than L2 (%.1f GB touched per step vs 129 MB L2)"
+                                 % (run.bytes_per_step() / 1e9),
+                           "parallelism": "dp%d simulated on each GPU (ranks as device buffers)"
+                                          % w.n_ranks},
+                "step_hbm_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
+                "step_frac_of_nominal_8tbs": step_gbs / 8000.0,
+                "bytes_per_element": b, "roofline": roofline, "kernels": kernels,
+                "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+                "gpu_launches": run.launches_per_step() * K,
+                "decision": res}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    run.plan.close()
+    return 0
+
+
+def measure_e2e(run, steps, stream, sh, ws, dist, dev):
+    """Same metric through the public API with host (pinned) gradient slices:
+    each step copies the slices host->device, reduces, updates, and reads the
+    step result back (a synchronising device->host copy)."""
+    import torch
+    torch.cuda.synchronize()
+    host = {}
+    try:
+        for r in run.ranks:
+            host[r] = torch.empty(run.slices[r].shape, dtype=run.slices[r].dtype, pin_memory=True)
+            host[r].copy_(run.slices[r])
+        pinned = True
+    except RuntimeError:
+        host = {r: run.slices[r].cpu() for r in run.ranks}
+        pinned = False
+    h2d = sum(int(t.numel()) * t.element_size() for t in host.values())
+
+    def one():
+        for r in run.ranks:
+            run.slices[r].copy_(host[r], non_blocking=True)
+        run.gathers(sh)
+        run.reduce(sh)
+        run.adam(sh)
+        return run.plan.result()          # synchronises and reads the record
+
+    one()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    el = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([el], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el = float(t.item())
+    value = run.P * len(run.ranks) * ws * steps / el
+    del host
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 64,
+            "pinned": pinned, "steps": steps, "ms_per_step": el / steps * 1e3}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

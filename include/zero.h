@@ -1,0 +1,239 @@
+/*
+ * zero.h -- C ABI of libzero: the ZeRO partitioned mixed-precision Adam step
+ * over a flat, padded parameter buffer, on one NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (the sources are web pages on ZeRO):
+ *  - "10.6 ZeRO 与 FSDP" §10.6.2–§10.6.4: per step, each of N data-parallel
+ *    ranks reduce-scatters the gradients so it holds the reduced 1/N slice
+ *    of its partition (Step 2), updates its 1/N of the fp32 optimizer state
+ *    and parameters locally (Step 3) and all-gathers the new parameters into
+ *    the full layout (Step 4, stages 1/2); stage 3 instead all-gathers each
+ *    layer's parameter shards when the layer is needed (§10.6.4).
+ *  - Table 10-2 of the same page: per-GPU bytes 16Ψ, 4Ψ+12Ψ/N, 2Ψ+14Ψ/N,
+ *    16Ψ/N and communication 2Ψ, 2Ψ, 2Ψ, 3Ψ.
+ *  - "从'年糕切片'理解ZeRO" §4.2–§4.3: gradient clipping 1.0 and fp16 loss
+ *    scaling.
+ *  - "第13篇 · ZeRO" §2.1 item 3: gradients live in one flat buffer.
+ * On one GPU, the N ranks' gradient slices and parameter shards are N
+ * separate device buffers supplied by the caller.
+ *
+ * Conventions for every call:
+ *  - Device pointers are caller-owned CUDA device memory on the current
+ *    device and must be 16-byte aligned; lengths are element counts.
+ *    The library never frees or retains caller memory after a call returns
+ *    (kernels launched by the call may still be reading/writing it on
+ *    `stream`).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *    device work of a call is enqueued on it; calls return without waiting,
+ *    except the ones documented as synchronising.
+ *  - Errors are returned as zero_status codes; nothing is thrown.
+ *    zero_last_error() gives a message for the last failure on the calling
+ *    thread.  On an error, no device work has been enqueued by that call.
+ *  - Low-precision ("lp") values are IEEE binary16 (ZERO_FP16) or bfloat16
+ *    (ZERO_BF16), chosen per plan.
+ */
+#ifndef ZERO_H
+#define ZERO_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct zero_plan zero_plan; /* opaque, owned by the library */
+
+typedef enum {
+    ZERO_OK = 0,
+    ZERO_EINVAL = 1,   /* bad argument: NULL, negative size, rank >= N ... */
+    ZERO_EALIGN = 2,   /* a device pointer is not 16-byte aligned           */
+    ZERO_ENOMEM = 3,   /* host or device allocation of plan scratch failed */
+    ZERO_ECUDA = 4,    /* a CUDA runtime call failed (see zero_last_error) */
+    ZERO_ETIMEOUT = 5, /* a bounded device wait ran out (gather pipeline)  */
+    ZERO_ESTATE = 6    /* call out of order (e.g. Adam before any reduce)  */
+} zero_status;
+
+typedef enum { ZERO_FP16 = 0, ZERO_BF16 = 1 } zero_lp;
+
+#define ZERO_MAX_RANKS 1024
+
+/* ----------------------------------------------------------------------
+ * Plan: the flat-buffer partitioner.
+ *
+ * The flat buffer holds the tensors back to back in list order with no
+ * per-tensor padding ("第13篇 · ZeRO" §2.1 item 3), then zero padding up to
+ * a multiple of n_ranks * align so that N equal partitions of length
+ * P = Ψ_p / N exist ("10.6 ZeRO 与 FSDP" §10.6.2).  Rank r owns
+ * [r*P, (r+1)*P).  Padding elements are not parameters: their gradients
+ * must be zero, and then their master/m/v/param stay exactly zero.
+ *
+ * stage 0 = DDP (no partitioning: one replica, rank must be 0, P = Ψ_p),
+ * stage 1/2 = ZeRO-1/2 (same arithmetic on the rank's partition; the stages
+ * differ only in what the caller keeps, see zero_memory_report),
+ * stage 3 = ZeRO-3: tensors are grouped into units (unit_of_tensor:
+ * non-decreasing, starting at 0, no gaps; NULL = one unit).  Each unit is
+ * padded on its own to a multiple of N*align and sharded N ways ("10.6" §10.6.7
+ * FSDP units); rank r's partition is the concatenation, in unit order, of
+ * its shard of every unit.
+ *
+ * psi: total parameter count; with tensor_sizes == NULL the buffer is one
+ * tensor of psi elements; with a tensor list, psi must equal the sum of the
+ * sizes, or be -1 to take the sum.  align: elements, a positive multiple of
+ * 8 (so every partition starts on a 16-byte boundary).  n_ranks in
+ * [1, ZERO_MAX_RANKS].
+ * Allocates no device memory (scratch is allocated on the first device call).
+ */
+zero_status zero_plan_create(int64_t psi, int32_t n_ranks,
+                             const int64_t *tensor_sizes, int32_t n_tensors,
+                             int32_t align, int32_t stage,
+                             const int32_t *unit_of_tensor, zero_lp lp,
+                             zero_plan **out);
+
+/* Padded length Ψ_p, partition length P, and (nullable, n_tensors entries)
+ * the flat offset of each tensor.  Host only. */
+zero_status zero_plan_query(const zero_plan *plan, int64_t *psi_padded,
+                            int64_t *part_len, int64_t *tensor_offsets);
+
+/* Stage-3 unit table (one unit in stages 0-2): n_units, unit_offsets
+ * (n_units + 1 entries: flat start of each padded unit, then Ψ_p) and
+ * unit_padded (U_p per unit).  Either array may be NULL.  Host only. */
+zero_status zero_plan_units(const zero_plan *plan, int32_t *n_units,
+                            int64_t *unit_offsets, int64_t *unit_padded);
+
+/* Fragments of rank r's partition: maximal runs of partition elements lying
+ * in one tensor, in partition order, 4 int64 each: (tensor id, offset in the
+ * tensor, offset in the partition, length).  Writes min(count, max_frag)
+ * fragments into frag (nullable when max_frag == 0); *count gets the total.
+ * Partition positions covered by no fragment are padding.  Host only. */
+zero_status zero_plan_fragments(const zero_plan *plan, int32_t rank,
+                                int64_t max_frag, int64_t *frag,
+                                int64_t *count);
+
+/* Dynamic loss-scale rule ("从'年糕切片'理解ZeRO" §4.3): on overflow the step
+ * is skipped and S halves (floor 1); after growth_interval consecutive good
+ * steps S doubles.  growth_interval <= 0 keeps S static (overflowing steps
+ * are still skipped).  Default 1000.  Host only. */
+zero_status zero_plan_set_loss_scaler(zero_plan *plan, int32_t growth_interval);
+
+/* Resume: set the device step counter t and the good-step count (e.g. from a
+ * checkpoint).  Synchronises the device. */
+zero_status zero_plan_set_state(zero_plan *plan, int64_t step,
+                                int32_t good_steps);
+
+/* Bound on the polls of each device-side wait in zero_gather_layer; 0 makes
+ * every wait give up at once (used to test the timeout path).  A wait that
+ * gives up sets the plan's error word; the next synchronising call
+ * (zero_step_result or zero_plan_check) returns ZERO_ETIMEOUT.  Host only. */
+zero_status zero_plan_set_spin_limit(zero_plan *plan, int64_t polls);
+
+/* ----------------------------------------------------------------------
+ * Reduce ("10.6 ZeRO 与 FSDP" §10.6.1 Reduce-Scatter, §10.6.2 Step 2; average
+ * over ranks per "ZeRO-1/2/3 vs DDP" ZeRO-2; unscale per "年糕切片" §4.3).
+ *
+ * grad_slices: N device pointers; grad_slices[j] holds P lp elements, rank
+ * j's gradient over rank `rank`'s partition.  For every i < P:
+ *   s = g_0[i] + g_1[i] + ... + g_{N-1}[i]   (float, in rank order)
+ *   grad_out[i] = s * float(1 / (loss_scale * N))
+ * and, over the partition, the overflow flag (any s not finite) and the
+ * partial sums of grad_out^2 that feed the global norm.
+ * grad_out: P floats (device).  bucket_elems: reduce in buckets of this many
+ * elements (rounded up to a whole number of 32768-element norm tiles, so
+ * results are bit-identical for every bucket size); 0 = one bucket.
+ * The first reduce after a step's Adam call starts a new step; every
+ * partition reduced before the next zero_adam_step joins that step's norm
+ * and overflow decision.  Stage 0: rank must be 0, slices hold Ψ_p elements.
+ */
+zero_status zero_reduce_partition(zero_plan *plan, int32_t rank,
+                                  const void *const *grad_slices,
+                                  float *grad_out, float loss_scale,
+                                  int64_t bucket_elems, void *stream);
+
+/* Local result of the reduces of the current step: sum of squares (fp64)
+ * and overflow flag, for exchanging with other real ranks (pass the others'
+ * totals as remote_* to zero_adam_step).  Synchronises `stream`. */
+zero_status zero_partition_stats(zero_plan *plan, double *sumsq,
+                                 int32_t *overflow, void *stream);
+
+/* ----------------------------------------------------------------------
+ * Decision + fused Adam/AdamW + cast ("10.6 ZeRO 与 FSDP" §10.6.2 Steps 3-4;
+ * "年糕切片" §4.2 clipping, §4.3 loss scaling).
+ *
+ * The first zero_adam_step of a step decides, on the device:
+ *   norm = sqrt(sum of squares of every reduced partition + remote_sumsq)
+ *   coef = clip / (norm + 1e-6) if clip > 0 and that is < 1, else 1
+ *   skip = overflow of any reduced partition or remote_overflow != 0
+ *   skip:  S' = max(S/2, 1) (dynamic) or S (static); t unchanged
+ *   else:  t = t + 1; after growth_interval good steps S' = 2S
+ * Later zero_adam_step calls of the same step (other ranks) reuse that
+ * decision (their loss_scale, clip and remote_* arguments are ignored).
+ * Then, unless skip, for each i < P of rank `rank`'s partition, each float
+ * op rounded to nearest on its own (no fused multiply-add):
+ *   g' = grad[i] * coef;  adamw == 0: g' = g' + wd * master[i]   (L2 Adam)
+ *   m  = b1*m + (1-b1)*g';   v = b2*v + (1-b2)*(g'*g')
+ *   upd = (lr * (m / (1-b1^t))) / (sqrt(v / (1-b2^t)) + eps)
+ *   adamw != 0: master = master * float(1 - lr*wd)   (decoupled decay)
+ *   master = master - upd;  param = round-to-nearest-even lp(master)
+ * grad, master, m, v: P floats (device).  param_out: lp, device; stages 0-2:
+ * the full Ψ_p-element layout (the all-gather destination; this rank writes
+ * [rank*P, (rank+1)*P)); stage 3: rank's own P-element shard buffer (there
+ * is no step-end all-gather, "10.6" §10.6.4).  param_out may be NULL (no
+ * cast).  loss_scale: the S used by this step's reduces.
+ */
+zero_status zero_adam_step(zero_plan *plan, int32_t rank, const float *grad,
+                           float *master, float *m, float *v, void *param_out,
+                           float lr, float beta1, float beta2, float eps,
+                           float wd, int32_t adamw, float loss_scale,
+                           float clip, double remote_sumsq,
+                           int32_t remote_overflow, void *stream);
+
+/* Decision of the last decided step: global norm, skipped flag, loss scale
+ * for the next step, and the step counter t.  Any pointer may be NULL.
+ * Synchronises the device.  Returns ZERO_ETIMEOUT (and clears it) if a
+ * bounded device wait gave up since the last check. */
+zero_status zero_step_result(zero_plan *plan, double *norm, int32_t *skipped,
+                             float *new_loss_scale, int64_t *step);
+
+/* Synchronises the device and reports (then clears) the plan's device error
+ * word: ZERO_OK or ZERO_ETIMEOUT. */
+zero_status zero_plan_check(zero_plan *plan);
+
+/* ----------------------------------------------------------------------
+ * Stage-3 layer gather ("10.6 ZeRO 与 FSDP" §10.6.4 forward/backward step 1:
+ * All-Gather of one layer's parameters; §10.6.7 FSDP unit).
+ * shards: N device pointers, shards[j] = rank j's P-element lp shard buffer
+ * (the buffer zero_adam_step writes in stage 3).  out: U_p lp elements
+ * (device) receiving unit `unit` in full layout:
+ *   out[j * (U_p/N) + k] = shards[j][unit_shard_offset + k],  k < U_p/N.
+ * Copies with TMA bulk transfers staged through shared memory; every device
+ * wait is bounded (zero_plan_set_spin_limit).  Stage 3 plans only.
+ */
+zero_status zero_gather_layer(zero_plan *plan, int32_t unit,
+                              const void *const *shards, void *out,
+                              void *stream);
+
+/* ----------------------------------------------------------------------
+ * Accounting ("10.6 ZeRO 与 FSDP" Table 10-2; "第13篇 · ZeRO" §3.2, §3.4).
+ * formula_bytes: per-GPU model-state bytes from the closed forms
+ *   [0] DDP 16Ψ, [1] stage 1 4Ψ+12Ψ/N, [2] stage 2 2Ψ+14Ψ/N, [3] stage 3 16Ψ/N
+ *   (exact rational values rounded once to double).
+ * actual_bytes: the same for the padded layout (Ψ_p = Ψ rounded up to a
+ *   multiple of N*align, P = Ψ_p/N): 16Ψ, 4Ψ_p+12P, 2Ψ_p+14P, 16P.
+ * comm_elems: elements moved per step: DDP 2Ψ, stage 1 2Ψ, stage 2 2Ψ,
+ *   stage 3 3Ψ.
+ * Pure host arithmetic; align >= 1.  Any output array may be NULL.
+ */
+zero_status zero_memory_report(int64_t psi, int32_t n_ranks, int32_t align,
+                               double formula_bytes[4], int64_t actual_bytes[4],
+                               int64_t comm_elems[4]);
+
+/* Frees the plan and its device scratch (synchronises the device first if
+ * scratch was allocated).  NULL is allowed. */
+void zero_plan_destroy(zero_plan *plan);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char *zero_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZERO_H */

@@ -15,7 +15,7 @@ LIB = os.path.join(HERE, "liboracle_zero.so")
 CFLAGS = [
     "-O2", "-std=c11", "-fPIC", "-shared",
     "-ffp-contract=off", "-fno-fast-math", "-fexcess-precision=standard",
-    "-fno-strict-aliasing", "-Wall",
+    "-fno-strict-aliasing", "-fno-semantic-interposition", "-Wall",
 ]
 
 

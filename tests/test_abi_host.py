@@ -1,0 +1,162 @@
+"""Host-side checks of libzero (CPU only: no kernel is launched).
+
+The library loads on a machine without a GPU (CUDA runtime linked
+statically), exports every entry point include/zero.h declares, and its
+partitioner and accounting agree with the independent oracle bit for bit.
+Argument validation happens before any device call, so it is tested here.
+"""
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import zero_partitioned_mixed_flat_gb300 as Z
+from zero_partitioned_mixed_flat_gb300.workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from zero_partitioned_mixed_flat_gb300 import build
+    build.build()
+    return Z.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "zero.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(zero_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 16
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(Z.SIGNATURES) == names   # the binding covers exactly the ABI
+
+
+def _cmp_layout(orc, sizes, n, align, stage, units):
+    plan = Z.zero_plan_create(-1 if sizes else 0, n, sizes or None, align, stage, units, 0)
+    try:
+        lay = orc.layout(sizes or [0], n, align, stage, units)
+        psi_p, part, offs = Z.zero_plan_query(plan, len(sizes))
+        assert psi_p == lay["psi_padded"] and part == lay["part_len"]
+        assert list(offs) == list(lay["tensor_offsets"])[:len(sizes)]
+        nu, uoff, upad = Z.zero_plan_units(plan)
+        assert nu == lay["n_units"]
+        assert list(uoff) == list(lay["unit_offsets"]) and list(upad) == list(lay["unit_padded"])
+        for r in range(n):
+            got = Z.zero_plan_fragments(plan, r)
+            exp = orc.fragments(sizes or [0], n, align, stage, r, units)
+            assert np.array_equal(got, exp), (sizes, n, align, stage, r)
+    finally:
+        Z.zero_plan_destroy(plan)
+
+
+def test_plan_matches_oracle_random(lib, orc):
+    rng = random.Random(23)
+    for _ in range(300):
+        nt = rng.randrange(1, 9)
+        sizes = [rng.choice([0, 1, 7, 8, 100, 1000, 4097, 65536]) for _ in range(nt)]
+        n = rng.choice([1, 2, 3, 4, 8, 64])
+        align = rng.choice([8, 16, 128])
+        stage = rng.choice([0, 1, 2, 3])
+        units = None
+        if stage == 3 and rng.random() < 0.8:
+            units, u = [], 0
+            for t in range(nt):
+                if t and rng.random() < 0.5:
+                    u += 1
+                units.append(u)
+        _cmp_layout(orc, sizes, n, align, stage, units)
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_plan_matches_oracle_workloads(lib, orc, name):
+    w = WORKLOADS[name]
+    plan = Z.ZeroPlan(-1, w.n_ranks, w.sizes, w.align, w.stage, w.unit_of_tensor, w.lp)
+    lay = orc.layout(w.sizes, w.n_ranks, w.align, w.stage, w.unit_of_tensor)
+    assert plan.psi_padded == lay["psi_padded"] and plan.part_len == lay["part_len"]
+    assert list(plan.tensor_offsets) == list(lay["tensor_offsets"])
+    for r in sorted({0, w.n_ranks - 1}):
+        assert np.array_equal(plan.fragments(r),
+                              orc.fragments(w.sizes, w.n_ranks, w.align, w.stage, r,
+                                            w.unit_of_tensor))
+    plan.close()
+
+
+def test_memory_report_matches_oracle(lib, orc):
+    rng = random.Random(5)
+    cases = [(7_500_000_000, 64, 1), (30_000_000_000, 64, 1), (1_000_000_000_000, 1024, 1),
+             (13_000_000_000, 16, 128), (0, 1, 1)]
+    cases += [(rng.randrange(0, 10 ** 13), rng.choice([1, 3, 8, 64, 1024]),
+               rng.choice([1, 8, 128])) for _ in range(500)]
+    for psi, n, al in cases:
+        f1, a1, c1 = Z.zero_memory_report(psi, n, al)
+        f2, a2, c2 = orc.memory(psi, n, al)
+        assert np.array_equal(f1, f2) and np.array_equal(a1, a2) and np.array_equal(c1, c2)
+
+
+@pytest.mark.parametrize("args", [
+    dict(n_ranks=0), dict(n_ranks=1025), dict(align=4), dict(align=12), dict(stage=4),
+    dict(stage=3, sizes=[4, 4], units=[0, 2]), dict(stage=3, sizes=[4, 4], units=[1, 1]),
+    dict(sizes=[4, -1]), dict(psi=9, sizes=[4, 4]), dict(lp=2), dict(psi=-5, sizes=None),
+])
+def test_plan_create_rejects(lib, args):
+    a = dict(psi=-1, n_ranks=2, sizes=[16, 16], align=8, stage=1, units=None, lp=0)
+    a.update(args)
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_plan_create(a["psi"], a["n_ranks"], a["sizes"], a["align"], a["stage"],
+                           a["units"], a["lp"])
+    assert e.value.code == Z.ZERO_EINVAL
+
+
+def test_step_calls_validate_before_touching_the_device(lib):
+    plan = Z.zero_plan_create(1024, 2, None, 8, 1, None, 0)
+    try:
+        buf = 1 << 20  # a fake, 16-byte aligned address: never dereferenced
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_reduce_partition(plan, 2, [buf, buf], buf, 1.0, 0, stream=0)
+        assert e.value.code == Z.ZERO_EINVAL                     # rank >= N
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_reduce_partition(plan, 0, [buf, buf + 2], buf, 1.0, 0, stream=0)
+        assert e.value.code == Z.ZERO_EALIGN                     # misaligned slice
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_reduce_partition(plan, 0, [buf, buf], buf + 4, 1.0, 0, stream=0)
+        assert e.value.code == Z.ZERO_EALIGN                     # misaligned output
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_reduce_partition(plan, 0, [buf, buf], buf, 0.0, 0, stream=0)
+        assert e.value.code == Z.ZERO_EINVAL                     # loss scale <= 0
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_reduce_partition(plan, 0, [buf, None], buf, 1.0, 0, stream=0)
+        assert e.value.code == Z.ZERO_EINVAL                     # NULL slice
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_adam_step(plan, 0, buf, buf, buf, buf, buf, 1e-3, .9, .999, 1e-8, 0., 1,
+                             1.0, 1.0, stream=0)
+        assert e.value.code == Z.ZERO_ESTATE                     # Adam before any reduce
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_adam_step(plan, 0, buf, buf + 8, buf, buf, buf, 1e-3, .9, .999, 1e-8, 0.,
+                             1, 1.0, 1.0, stream=0)
+        assert e.value.code == Z.ZERO_EALIGN
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_gather_layer(plan, 0, [buf, buf], buf, stream=0)
+        assert e.value.code == Z.ZERO_EINVAL                     # not a stage-3 plan
+        with pytest.raises(Z.ZeroError):
+            Z.zero_plan_fragments(plan, 5)
+        assert "rank" in Z.zero_last_error()
+    finally:
+        Z.zero_plan_destroy(plan)
+    p3 = Z.zero_plan_create(-1, 2, [64, 64], 8, 3, [0, 1], 0)
+    try:
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_gather_layer(p3, 2, [1 << 20, 1 << 20], 1 << 20, stream=0)
+        assert e.value.code == Z.ZERO_EINVAL                     # unit out of range
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_gather_layer(p3, 0, [1 << 20, (1 << 20) + 8], 1 << 20, stream=0)
+        assert e.value.code == Z.ZERO_EALIGN
+    finally:
+        Z.zero_plan_destroy(p3)

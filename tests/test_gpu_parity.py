@@ -1,0 +1,257 @@
+"""GPU parity of libzero against the CPU oracle (small and odd sizes).
+
+Every case runs through the C ABI on seeded synthetic inputs and compares
+with the oracle element by element: the reduced gradient, flags and the
+skip/scale decision bit for bit, master/m/v within 1e-6 relative (bit-exact
+when the clip coefficients agree), the norm within 1e-5, the fp16/bf16
+parameters within 1 ulp, and gathers bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zero_partitioned_mixed_flat_gb300 as Z
+from zero_partitioned_mixed_flat_gb300 import synth
+from zero_partitioned_mixed_flat_gb300.workloads import WORKLOADS, Workload
+
+from .zstep import Harness, same_floats
+
+pytestmark = pytest.mark.gpu
+TILE = 32768
+
+
+def _plan(psi, n, lp, stage=1, align=8, sizes=None, units=None):
+    return Z.ZeroPlan(psi if sizes is None else -1, n, sizes, align, stage, units, lp)
+
+
+def _reduce_case(zlib, n, part, lp, scale, bucket=0, rank=0, seed=0):
+    psi = n * part
+    plan = _plan(psi, n, lp)
+    assert plan.part_len == part
+    dev = torch.device("cuda")
+    slices = [synth.grad_slice(part, lp, 1.0, scale, seed, 1, j, rank, dev) for j in range(n)]
+    g = torch.empty(part, dtype=torch.float32, device=dev)
+    plan.reduce(rank, slices, g, scale, bucket)
+    ss, of = plan.stats()
+    host = [synth.to_numpy_codes(t) for t in slices]
+    og, oss, oof = oracle.reduce(host, lp, scale)
+    assert same_floats(g.cpu().numpy(), og)
+    assert of == oof
+    assert abs(ss - oss) <= 1e-6 * oss
+    plan.close()
+    return g, ss
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 16, 17, 64, 65, 130])
+@pytest.mark.parametrize("lp", [0, 1])
+def test_reduce_ragged_and_wide(zlib, n, lp):
+    # 3 whole norm tiles plus a ragged tail of 136 elements
+    _reduce_case(zlib, n, 3 * TILE + 136, lp, 1024.0 if lp == 0 else 1.0)
+
+
+@pytest.mark.parametrize("part", [8, 64, 4096, TILE - 8, TILE, TILE + 8, 7 * TILE + 4000])
+def test_reduce_sizes(zlib, part):
+    _reduce_case(zlib, 4, part, 0, 4.0)
+
+
+def test_bucket_size_never_changes_a_bit(zlib):
+    n, part, lp = 8, 5 * TILE + 1000, 1
+    ref = None
+    for bucket in [0, 1, TILE, 2 * TILE + 3, 10 ** 9]:
+        g, ss = _reduce_case(zlib, n, part, lp, 1.0, bucket=bucket)
+        cur = (g.cpu().numpy(), ss)
+        if ref is None:
+            ref = cur
+        else:
+            assert same_floats(cur[0], ref[0]) and cur[1] == ref[1]
+
+
+def test_empty_partition(zlib):
+    plan = _plan(0, 4, 0)
+    assert plan.part_len == 0
+    dev = torch.device("cuda")
+    e = torch.empty(0, dtype=torch.float16, device=dev)
+    f = torch.empty(0, dtype=torch.float32, device=dev)
+    plan.reduce(0, [e] * 4, f, 1.0)
+    plan.adam(0, f, f, f, f, None, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0, 1.0)
+    r = plan.result()
+    assert r["norm"] == 0.0 and r["skipped"] == 0 and r["step"] == 1
+    plan.close()
+
+
+def _tiny(**kw):
+    w = WORKLOADS["tiny-zero1"]
+    d = dict(w.__dict__)
+    d.update(kw)
+    return Workload(**d)
+
+
+def test_tiny_zero1_all_partitions(zlib):
+    h = Harness(WORKLOADS["tiny-zero1"])
+    for _ in range(3):
+        info = h.step()
+        assert info["coef_equal"]
+    h.close()
+
+
+def test_ddp_replica_equals_sharded_step(zlib):
+    # "ZeRO does not change the math": the stage-0 replica over the whole
+    # buffer and the four stage-1 partitions give the same bits.
+    w = WORKLOADS["tiny-zero1"]
+    a = Harness(w)
+    b = Harness(w, ranks=[0], stage=0)
+    b.st[0].master.copy_(torch.cat([a.st[r].master for r in a.ranks]))
+    # feed stage 0 the concatenation of the four partitions' slices
+    for _ in range(3):
+        a.step_no += 1
+        for r in a.ranks:
+            a.make_slices(r)
+        ra = a.gpu_step()
+        b.st[0].slices = [torch.cat([a.st[r].slices[j] for r in a.ranks]) for j in range(w.n_ranks)]
+        rb = b.gpu_step()
+        assert (ra["skipped"], ra["step"], ra["loss_scale"]) == (rb["skipped"], rb["step"], rb["loss_scale"])
+        assert abs(ra["norm"] - rb["norm"]) <= 1e-12 * ra["norm"]
+        full = lambda t: torch.cat([getattr(a.st[r], t) for r in a.ranks]).cpu().numpy()
+        for t in ("master", "m", "v", "g"):
+            assert same_floats(full(t), getattr(b.st[0], t).cpu().numpy()), t
+        assert torch.equal(a.param, b.param)
+    a.close()
+    b.close()
+
+
+@pytest.mark.parametrize("kw", [
+    dict(adamw=False),                                     # L2 Adam
+    dict(lp=1, loss_scale=1.0, grads_times_scale=False),   # bf16
+    dict(clip=0.0),                                        # no clipping
+    dict(clip=0.05),                                       # clipping active
+    dict(n_ranks=3, ranks=[0, 1, 2], sizes=[100_000, 7, 33_333]),  # odd N, ragged
+    dict(n_ranks=1, ranks=[0]),                            # N = 1: plain mixed-precision Adam
+    dict(bucket_elems=40_000),                             # several buckets
+])
+def test_tiny_variants(zlib, kw):
+    h = Harness(_tiny(**kw))
+    for _ in range(2):
+        h.step()
+    h.close()
+
+
+def test_overflow_skips_and_halves_scale(zlib):
+    w = _tiny(growth_interval=1000, inject_inf_step=2, loss_scale=65536.0, steps=3)
+    h = Harness(w)
+    seen = []
+    for _ in range(3):
+        info = h.step()
+        seen.append((info["gpu"]["skipped"], info["gpu"]["loss_scale"], info["gpu"]["step"]))
+    assert seen == [(0, 65536.0, 1), (1, 32768.0, 1), (0, 32768.0, 2)]
+    h.close()
+
+
+def test_nan_and_remote_terms(zlib):
+    dev = torch.device("cuda")
+    n, part = 2, 4096
+    plan = _plan(n * part, n, 0)
+    sl = [synth.grad_slice(part, 0, 1e-2, 1.0, 0, 1, j, 0, dev) for j in range(n)]
+    g = torch.empty(part, device=dev)
+    w = torch.zeros(part, device=dev); m = torch.zeros(part, device=dev); v = torch.zeros(part, device=dev)
+    # remote overflow forces a skip even when this partition is finite
+    plan.reduce(0, sl, g, 1.0)
+    plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0, 0.0, 1)
+    r = plan.result()
+    assert r["skipped"] == 1 and r["step"] == 0 and not w.any().item()
+    # remote sum of squares joins the global norm
+    plan.reduce(0, sl, g, 1.0)
+    ss, _ = plan.stats()
+    plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0, 3.0 * ss, 0)
+    r = plan.result()
+    assert abs(r["norm"] - np.sqrt(4.0 * ss)) <= 1e-6 * r["norm"] and r["step"] == 1
+    # a NaN gradient is an overflow
+    sl[1][17] = float("nan")
+    plan.reduce(0, sl, g, 1.0)
+    before = w.clone()
+    plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0)
+    r = plan.result()
+    assert r["skipped"] == 1 and torch.equal(before, w)
+    plan.close()
+
+
+def test_resume_is_bit_identical(zlib):
+    w = WORKLOADS["tiny-zero1"]
+    a = Harness(w)
+    for _ in range(3):
+        a.step()
+    # replay: two steps, checkpoint (state + step counter), fresh plan, step 3
+    b = Harness(w)
+    b.step()
+    b.step()
+    ck = {r: (b.st[r].master.clone(), b.st[r].m.clone(), b.st[r].v.clone()) for r in b.ranks}
+    step, S = b.o_step, b.S
+    b.close()
+    c = Harness(w)
+    c.plan.set_state(step, 0)
+    for r in c.ranks:
+        c.st[r].master.copy_(ck[r][0]); c.st[r].m.copy_(ck[r][1]); c.st[r].v.copy_(ck[r][2])
+    c.step_no, c.S = 3, S
+    for r in c.ranks:
+        c.make_slices(r)
+    res = c.gpu_step()
+    assert res["step"] == 3
+    for r in c.ranks:
+        for t in ("master", "m", "v"):
+            assert torch.equal(getattr(c.st[r], t), getattr(a.st[r], t))
+    a.close()
+    c.close()
+
+
+# ------------------------------------------------------------------ gather
+
+def _gather_case(n, sizes, units, lp=0, align=8, spin=None):
+    dev = torch.device("cuda")
+    plan = _plan(-1, n, lp, stage=3, align=align, sizes=sizes, units=units)
+    shards = [synth.lp_shard(plan.part_len, lp, 1.0, 3, j, dev) for j in range(n)]
+    host = [synth.to_numpy_codes(s) for s in shards]
+    if spin is not None:
+        plan.set_spin_limit(spin)
+    outs = []
+    for u in range(plan.n_units):
+        sl = plan.shard_len(u)
+        off = plan.unit_shard_offset(u)
+        out = torch.full((sl * n,), 7, dtype=synth.LP_DTYPES[lp], device=dev)
+        plan.gather(u, shards, out)
+        outs.append((u, out, [h[off:off + sl] for h in host]))
+    return plan, outs
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 64, 65])
+def test_gather_units(zlib, n):
+    sizes = [1000, 24, 4096 * 9 + 8, 5, 16384 * 3, 100_000]
+    units = [0, 0, 1, 2, 2, 3]
+    plan, outs = _gather_case(n, sizes, units)
+    plan.check()
+    for u, out, host in outs:
+        assert np.array_equal(synth.to_numpy_codes(out), oracle.gather(host)), u
+    plan.close()
+
+
+def test_gather_large_unit_many_chunks(zlib):
+    plan, outs = _gather_case(8, [3_000_000, 1_000_008], [0, 1], lp=1, align=128)
+    plan.check()
+    for u, out, host in outs:
+        assert np.array_equal(synth.to_numpy_codes(out), oracle.gather(host)), u
+    plan.close()
+
+
+def test_gather_wait_timeout_is_reported_and_recoverable(zlib):
+    # spin limit 0: every bounded wait gives up at once; the kernel drains its
+    # copies, sets the error word and returns; the context stays usable
+    plan, outs = _gather_case(4, [200_000], None, spin=0)
+    with pytest.raises(Z.ZeroError) as e:
+        plan.check()
+    assert e.value.code == Z.ZERO_ETIMEOUT
+    plan.check()   # the error word was cleared
+    plan.close()
+    plan2, outs2 = _gather_case(4, [200_000], None)
+    plan2.check()
+    u, out, host = outs2[0]
+    assert np.array_equal(synth.to_numpy_codes(out), oracle.gather(host))
+    plan2.close()

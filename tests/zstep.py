@@ -1,0 +1,272 @@
+"""Test harness: run a workload's steps through libzero on the GPU and through
+the CPU oracle on the same seeded inputs, and compare.
+
+Used by the GPU parity tests.  The oracle never sees a value computed by the
+CUDA path: it gets the synthetic inputs (gradient slices, initial master
+weights, other ranks' parameter shards) and evolves its own state.
+
+Comparison bars (from the task's parity statement):
+  layout, padding, overflow flag, skip, loss scale, step: bit-exact;
+  reduced fp32 gradient: bit-exact (fixed rank order on both sides);
+  master / m / v: max relative error 1e-6 (denominator floored at 1e-30), and
+      bit-exact whenever both sides took the same clip coefficient;
+  global norm: 1e-5 relative;
+  fp16/bf16 parameters: within 1 ulp (bit-exact when the coefficients agree).
+"""
+import math
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional
+
+import numpy as np
+import torch
+
+import oracle
+import zero_partitioned_mixed_flat_gb300 as Z
+from zero_partitioned_mixed_flat_gb300 import synth
+from zero_partitioned_mixed_flat_gb300.workloads import Workload
+
+SEED = 0
+REL_TOL = 1e-6
+NORM_TOL = 1e-5
+
+
+def bits(a: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(a).view(np.uint32)
+
+
+def same_floats(a: np.ndarray, b: np.ndarray) -> bool:
+    """Bitwise equal, treating any two NaNs as equal."""
+    eq = bits(a) == bits(b)
+    return bool(np.all(eq | (np.isnan(a) & np.isnan(b))))
+
+
+def max_rel_err(a: np.ndarray, b: np.ndarray) -> float:
+    a64, b64 = a.astype(np.float64), b.astype(np.float64)
+    den = np.maximum(np.abs(b64), 1e-30)
+    if a64.size == 0:
+        return 0.0
+    return float(np.max(np.abs(a64 - b64) / den))
+
+
+def lp_ulp_dist(a: np.ndarray, b: np.ndarray) -> int:
+    """Largest distance in units in the last place between two lp code arrays."""
+    def key(c):
+        c = c.astype(np.int32)
+        return np.where(c & 0x8000, -(c & 0x7FFF), c)
+    if a.size == 0:
+        return 0
+    return int(np.max(np.abs(key(a) - key(b))))
+
+
+def coef_from_norm(norm: float, clip: float) -> float:
+    if clip > 0:
+        c = clip / (norm + 1e-6)
+        if c < 1.0:
+            return float(np.float32(c))
+    return 1.0
+
+
+@dataclass
+class RankState:
+    slices: List[torch.Tensor] = field(default_factory=list)
+    g: Optional[torch.Tensor] = None
+    master: Optional[torch.Tensor] = None
+    m: Optional[torch.Tensor] = None
+    v: Optional[torch.Tensor] = None
+    shard: Optional[torch.Tensor] = None       # stage 3: this rank's lp shard
+    idx: Optional[np.ndarray] = None           # compared positions
+    idx_dev: Optional[torch.Tensor] = None
+    o_master: Optional[np.ndarray] = None      # oracle state at idx
+    o_m: Optional[np.ndarray] = None
+    o_v: Optional[np.ndarray] = None
+    keep: list = field(default_factory=list)
+    pad_idx: Optional[torch.Tensor] = None
+
+
+class Harness:
+    """Runs `w` on the GPU through libzero and on the oracle; compares each step."""
+
+    def __init__(self, w: Workload, ranks=None, full: bool = True, n_sample: int = 1 << 20,
+                 threads: int = 8, chunk: int = 1 << 22, device="cuda", bucket=None,
+                 stage=None):
+        self.w = w
+        self.dev = torch.device(device)
+        self.full = full
+        self.threads = threads
+        self.chunk = chunk
+        self.stage = w.stage if stage is None else stage
+        self.bucket = w.bucket_elems if bucket is None else bucket
+        self.plan = Z.ZeroPlan(-1, w.n_ranks, w.sizes, w.align, self.stage, w.unit_of_tensor,
+                               w.lp, growth_interval=w.growth_interval)
+        self.lay = oracle.layout(w.sizes, w.n_ranks, w.align, self.stage, w.unit_of_tensor)
+        assert self.plan.psi_padded == self.lay["psi_padded"]
+        assert self.plan.part_len == self.lay["part_len"]
+        self.P = self.plan.part_len
+        self.ranks = list(w.ranks if ranks is None else ranks)
+        self.S = w.loss_scale
+        self.o_step = 0
+        self.o_good = 0
+        self.step_no = 0
+        self.log: List[Dict] = []
+        gen = np.random.default_rng(1234)
+        if self.stage == 3:
+            self.param = None
+        else:
+            self.param = torch.zeros(self.plan.psi_padded, dtype=synth.LP_DTYPES[w.lp],
+                                     device=self.dev)
+        self.st: Dict[int, RankState] = {}
+        self.o_param: Dict[int, np.ndarray] = {}
+        for r in self.ranks:
+            s = RankState()
+            s.keep = self.plan.keep_ranges(r)
+            s.master = synth.master_init(self.P, w.master_std, SEED, r, self.dev, s.keep)
+            s.m = torch.zeros(self.P, dtype=torch.float32, device=self.dev)
+            s.v = torch.zeros(self.P, dtype=torch.float32, device=self.dev)
+            s.g = torch.full((self.P,), float("nan"), dtype=torch.float32, device=self.dev)
+            if self.stage == 3:
+                s.shard = torch.zeros(self.P, dtype=synth.LP_DTYPES[w.lp], device=self.dev)
+            if full or self.P <= n_sample:
+                s.idx = np.arange(self.P, dtype=np.int64)
+            else:
+                edges = [np.arange(0, min(4096, self.P)), np.arange(max(0, self.P - 4096), self.P)]
+                tiles = np.arange(0, self.P, 32768)
+                edges += [t + np.arange(-8, 8) for t in tiles[1:]]
+                rnd = gen.integers(0, self.P, n_sample)
+                s.idx = np.unique(np.clip(np.concatenate(edges + [rnd]), 0, self.P - 1))
+            s.idx_dev = torch.from_numpy(s.idx).to(self.dev)
+            s.o_master = s.master[s.idx_dev].cpu().numpy().copy()
+            s.o_m = np.zeros(s.idx.size, np.float32)
+            s.o_v = np.zeros(s.idx.size, np.float32)
+            # padding positions inside the partition
+            mask = torch.ones(self.P, dtype=torch.bool, device=self.dev)
+            for a, n in s.keep:
+                mask[a:a + n] = False
+            s.pad_idx = torch.nonzero(mask).flatten()
+            self.st[r] = s
+
+    # ------------------------------------------------------------ inputs
+    def make_slices(self, r: int):
+        w = self.w
+        scale = self.S if w.grads_times_scale else 1.0
+        s = self.st[r]
+        s.slices = [synth.grad_slice(self.P, w.lp, w.grad_std, scale, SEED, self.step_no, j, r,
+                                     self.dev, s.keep) for j in range(w.n_ranks)]
+        if w.inject_inf_step and self.step_no == w.inject_inf_step and r == self.ranks[0]:
+            j, i = synth.inject_position(SEED, self.step_no, r, w.n_ranks, s.keep)
+            s.slices[j][i] = float("inf")
+
+    # ------------------------------------------------------------- GPU
+    def gpu_step(self):
+        w = self.w
+        for r in self.ranks:
+            s = self.st[r]
+            self.plan.reduce(r, s.slices, s.g, self.S, self.bucket)
+        for r in self.ranks:
+            s = self.st[r]
+            out = s.shard if self.stage == 3 else self.param
+            self.plan.adam(r, s.g, s.master, s.m, s.v, out, w.lr, w.beta1, w.beta2, w.eps, w.wd,
+                           int(w.adamw), self.S, w.clip)
+        return self.plan.result()
+
+    # ---------------------------------------------------------- oracle
+    def _oracle_reduce(self, r: int):
+        """Chunked oracle reduce of rank r; compares the GPU gradient bit for bit.
+        Returns (sumsq, overflow, g at idx)."""
+        w, s = self.w, self.st[r]
+        chunks = [(c, min(self.P, c + self.chunk)) for c in range(0, self.P, self.chunk)]
+        idx = s.idx
+
+        def work(c0, c1, host_slices, host_g):
+            g, ss, of = oracle.reduce(host_slices, w.lp, self.S)
+            ok = same_floats(g, host_g)
+            lo, hi = np.searchsorted(idx, [c0, c1])
+            return ss, of, ok, g[idx[lo:hi] - c0]
+
+        results = []
+        with ThreadPoolExecutor(self.threads) as ex:
+            pending = []
+            for c0, c1 in chunks:
+                hs = [synth.to_numpy_codes(t[c0:c1]) for t in s.slices]
+                hg = s.g[c0:c1].cpu().numpy()
+                pending.append(ex.submit(work, c0, c1, hs, hg))
+                if len(pending) >= 2 * self.threads:
+                    results.append(pending.pop(0).result())
+            results += [f.result() for f in pending]
+        ss = 0.0
+        of = 0
+        for r_ss, r_of, ok, _ in results:
+            ss += r_ss
+            of |= r_of
+            assert ok, "reduced gradient differs from the oracle (rank %d)" % r
+        g_idx = np.concatenate([x[3] for x in results]) if results else np.zeros(0, np.float32)
+        return ss, of, g_idx
+
+    def oracle_step(self):
+        w = self.w
+        tot, of, g_at = 0.0, 0, {}
+        for r in self.ranks:
+            ss, o, g_at[r] = self._oracle_reduce(r)
+            tot += ss
+            of |= o
+        d = oracle.decide(tot, of, w.clip, self.S, self.o_step, self.o_good, w.growth_interval,
+                          w.beta1, w.beta2)
+        params = {}
+        for r in self.ranks:
+            s = self.st[r]
+            params[r] = oracle.adam(g_at[r], s.o_master, s.o_m, s.o_v, w.lp, d["coef"], d["skip"],
+                                    w.lr, w.beta1, w.beta2, w.eps, w.wd, int(w.adamw), d["bc1"],
+                                    d["bc2"])
+        return d, params
+
+    # --------------------------------------------------------- compare
+    def step(self):
+        self.step_no += 1
+        for r in self.ranks:
+            self.make_slices(r)
+        res = self.gpu_step()
+        d, params = self.oracle_step()
+        info = {"step": self.step_no, "gpu": res, "oracle": {k: d[k] for k in
+                ("norm", "coef", "skip", "new_scale", "step")}}
+        assert res["skipped"] == d["skip"], info
+        assert res["step"] == d["step"], info
+        assert res["loss_scale"] == d["new_scale"], info
+        if d["skip"]:
+            assert not math.isfinite(res["norm"]) or not math.isfinite(d["norm"]) or \
+                abs(res["norm"] - d["norm"]) <= NORM_TOL * d["norm"], info
+        else:
+            assert abs(res["norm"] - d["norm"]) <= NORM_TOL * d["norm"], info
+        gpu_coef = coef_from_norm(res["norm"], self.w.clip)
+        exact = (gpu_coef == d["coef"]) or d["skip"]
+        info["coef_equal"] = exact
+        for r in self.ranks:
+            s = self.st[r]
+            gm = s.master[s.idx_dev].cpu().numpy()
+            gmm = s.m[s.idx_dev].cpu().numpy()
+            gv = s.v[s.idx_dev].cpu().numpy()
+            if self.stage == 3:
+                gp = synth.to_numpy_codes(s.shard[s.idx_dev])
+            else:
+                gp = synth.to_numpy_codes(self.param[r * self.P + s.idx_dev])
+            errs = (max_rel_err(gm, s.o_master), max_rel_err(gmm, s.o_m), max_rel_err(gv, s.o_v))
+            info.setdefault("rel_err", {})[r] = errs
+            assert max(errs) <= REL_TOL, info
+            if exact:
+                assert same_floats(gm, s.o_master) and same_floats(gmm, s.o_m) \
+                    and same_floats(gv, s.o_v), info
+            if not d["skip"]:
+                self.o_param[r] = params[r]
+            if r in self.o_param:
+                # the param buffer holds the cast of the latest master
+                assert lp_ulp_dist(gp, self.o_param[r]) <= (0 if exact else 1), info
+            # padding stays exactly zero
+            if s.pad_idx.numel():
+                for t in (s.master, s.m, s.v):
+                    assert not t[s.pad_idx].any().item(), "padding became non-zero"
+        self.S = d["new_scale"]
+        self.o_step, self.o_good = d["step"], d["good_steps"]
+        self.log.append(info)
+        return info
+
+    def close(self):
+        self.plan.close()

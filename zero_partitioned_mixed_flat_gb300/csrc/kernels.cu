@@ -1,0 +1,606 @@
+// kernels.cu -- the device side of libzero (sm_103a).
+//
+// K1 reduce_unscale_stats  N-way reduce of lp gradient slices into one fp32
+//                          partition, unscale, overflow flag, per-tile sum of
+//                          squares ("10.6 ZeRO 与 FSDP" §10.6.1 Reduce-Scatter,
+//                          §10.6.2 Step 2).
+// K2 norm_finalize_decide  global norm, clip coefficient, skip and loss-scale
+//                          decision, step counter ("年糕切片" §4.2-§4.3).
+// K3 adam_fused_cast       Adam/AdamW on fp32 master/m/v + lp cast into the
+//                          all-gather destination (§10.6.2 Steps 3-4).
+// K4 gather_layer_tma      stage-3 per-layer all-gather of N shards
+//                          (§10.6.4 step 1), TMA bulk copies through shared
+//                          memory with bounded mbarrier waits.
+//
+// Everything here is bandwidth-bound streaming: no tensor cores.  All float
+// arithmetic of the step uses explicit round-to-nearest intrinsics so that no
+// multiply-add is fused and the op order is the one the ABI documents.
+#include "zero_internal.h"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+namespace zk {
+namespace {
+
+constexpr int kReduceThreads = 256;
+constexpr int kVec = 8;  // lp elements per 16-byte vector
+constexpr int kTileIters = int(kTile / (kReduceThreads * kVec));
+constexpr int kBatch = 16;  // slices loaded before they are added
+constexpr int kAdamThreads = 256;
+constexpr int kGatherStages = 6;
+constexpr unsigned kGatherChunk = 32768;  // bytes per bulk copy
+constexpr long long kDrainPolls = 1ll << 21;
+static_assert(kTile % (kReduceThreads * kVec) == 0, "tile must be whole iterations");
+
+// ---------------------------------------------------------------- memory ops
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_stream_f4(const float4 *p) {
+    float4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_stream_f4(float4 *p, float4 v) { __stcs(p, v); }
+
+__device__ __forceinline__ void st_stream_u4(uint4 *p, uint4 v) { __stcs(p, v); }
+
+// 8 lp values -> 8 floats (exact conversions)
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4 &q, float f[8]) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if constexpr (BF16) {
+            f[2 * k] = __uint_as_float(w[k] << 16);
+            f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        } else {
+            __half2 h = *reinterpret_cast<const __half2 *>(&w[k]);
+            float2 t = __half22float2(h);
+            f[2 * k] = t.x;
+            f[2 * k + 1] = t.y;
+        }
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if constexpr (BF16) {
+        uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+        uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+        return lo | (hi << 16);
+    } else {
+        uint32_t lo = __half_as_ushort(__float2half_rn(a));
+        uint32_t hi = __half_as_ushort(__float2half_rn(b));
+        return lo | (hi << 16);
+    }
+}
+
+// ------------------------------------------------------------------ K1 reduce
+
+template <int MAXN>
+struct ReduceParams {
+    const uint4 *src[MAXN];  // slice j at the bucket start
+    float4 *g;               // output at the bucket start
+    double *partials;        // partial of the bucket's first tile
+    unsigned *overflow;
+    long long len;           // elements in the bucket (multiple of 8)
+    float inv;               // float(1 / (S * N))
+    int n;
+};
+
+template <int MAXN, bool BF16>
+__global__ void __launch_bounds__(kReduceThreads)
+reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
+    __shared__ float warp_sq[kReduceThreads / 32];
+    const long long n_vec = p.len / kVec;
+    const long long n_tiles = (p.len + kTile - 1) / kTile;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    bool bad = false;
+
+    for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        float sq = 0.0f;
+        const long long v0 = tile * (kTile / kVec);
+#pragma unroll 1
+        for (int it = 0; it < kTileIters; ++it) {
+            const long long vi = v0 + (long long)it * kReduceThreads + threadIdx.x;
+            if (vi >= n_vec) break;
+            float s[8];
+            unpack8<BF16>(ld_stream(p.src[0] + vi), s);
+            for (int j0 = 1; j0 < p.n; j0 += kBatch) {
+                uint4 q[kBatch];
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b)
+                    if (j0 + b < p.n) q[b] = ld_stream(p.src[j0 + b] + vi);
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    if (j0 + b < p.n) {
+                        float x[8];
+                        unpack8<BF16>(q[b], x);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], x[k]);
+                    }
+                }
+            }
+            float o[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                bad |= !isfinite(s[k]);
+                o[k] = __fmul_rn(s[k], p.inv);
+                sq = __fadd_rn(sq, __fmul_rn(o[k], o[k]));
+            }
+            st_stream_f4(p.g + 2 * vi, make_float4(o[0], o[1], o[2], o[3]));
+            st_stream_f4(p.g + 2 * vi + 1, make_float4(o[4], o[5], o[6], o[7]));
+        }
+        // fixed-shape tree: lanes, then warps in order (fp64)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, off));
+        if (lane == 0) warp_sq[warp] = sq;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double t = 0.0;
+#pragma unroll
+            for (int w = 0; w < kReduceThreads / 32; ++w) t = __dadd_rn(t, (double)warp_sq[w]);
+            p.partials[tile] = t;
+        }
+        __syncthreads();
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.overflow, 1u);
+}
+
+// ------------------------------------------------------------------ K2 decide
+
+struct DecideParams {
+    const double *partials;
+    long long tiles_per_slot;
+    unsigned long long mask[1024 / 64];
+    int n_slots;
+    double remote_sumsq;
+    int remote_overflow;
+    float clip, loss_scale, beta1, beta2;
+    int growth_interval;
+    StepRecord *rec;
+};
+
+constexpr int kDecideThreads = 1024;
+
+__global__ void __launch_bounds__(kDecideThreads)
+norm_finalize_decide(const __grid_constant__ DecideParams p) {
+    __shared__ double wsum[kDecideThreads / 32];
+    double acc = 0.0;
+    for (int r = 0; r < p.n_slots; ++r) {
+        if (!((p.mask[r >> 6] >> (r & 63)) & 1ull)) continue;
+        const double *q = p.partials + (long long)r * p.tiles_per_slot;
+        for (long long t = threadIdx.x; t < p.tiles_per_slot; t += kDecideThreads)
+            acc = __dadd_rn(acc, q[t]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+
+    StepRecord *rec = p.rec;
+    double sumsq = 0.0;
+    for (int w = 0; w < kDecideThreads / 32; ++w) sumsq = __dadd_rn(sumsq, wsum[w]);
+    sumsq = __dadd_rn(sumsq, p.remote_sumsq);
+    const double norm = sqrt(sumsq);
+    const int skip = (rec->overflow != 0u) || (p.remote_overflow != 0);
+    float coef = 1.0f;
+    if (p.clip > 0.0f) {
+        const double c = __ddiv_rn((double)p.clip, __dadd_rn(norm, 1e-6));
+        if (c < 1.0) coef = __double2float_rn(c);
+    }
+    long long t = rec->step;
+    int good = rec->good_steps;
+    float s = p.loss_scale;
+    if (skip) {
+        s = p.growth_interval > 0 ? fmaxf(__fmul_rn(p.loss_scale, 0.5f), 1.0f) : p.loss_scale;
+        good = 0;
+    } else {
+        good += 1;
+        if (p.growth_interval > 0 && good >= p.growth_interval) {
+            s = __fmul_rn(p.loss_scale, 2.0f);
+            good = 0;
+        }
+        t += 1;
+    }
+    rec->norm = norm;
+    rec->sumsq = sumsq;
+    rec->coef = coef;
+    rec->skip = skip;
+    rec->loss_scale = s;
+    rec->good_steps = good;
+    rec->step = t;
+    rec->bc1 = __double2float_rn(__dsub_rn(1.0, pow((double)p.beta1, (double)t)));
+    rec->bc2 = __double2float_rn(__dsub_rn(1.0, pow((double)p.beta2, (double)t)));
+}
+
+// -------------------------------------------------------------------- K3 adam
+
+struct AdamParams {
+    const float4 *g;
+    float4 *master, *m, *v;
+    uint4 *param;  // 8 lp per uint4; NULL: no cast
+    const StepRecord *rec;
+    long long n_vec;  // len / 8
+    float lr, beta1, beta2, omb1, omb2, eps, wd, decay;
+    int adamw;
+};
+
+struct AdamScalars {
+    float coef, bc1, bc2, lr, beta1, beta2, omb1, omb2, eps, wd, decay;
+    int adamw;
+};
+
+__device__ __forceinline__ void adam1(const AdamScalars &c, float g, float &w, float &m,
+                                      float &v) {
+    float gi = __fmul_rn(g, c.coef);
+    if (!c.adamw) gi = __fadd_rn(gi, __fmul_rn(c.wd, w));
+    m = __fadd_rn(__fmul_rn(c.beta1, m), __fmul_rn(c.omb1, gi));
+    v = __fadd_rn(__fmul_rn(c.beta2, v), __fmul_rn(c.omb2, __fmul_rn(gi, gi)));
+    const float mhat = __fdiv_rn(m, c.bc1);
+    const float vhat = __fdiv_rn(v, c.bc2);
+    const float denom = __fadd_rn(__fsqrt_rn(vhat), c.eps);
+    const float upd = __fdiv_rn(__fmul_rn(c.lr, mhat), denom);
+    if (c.adamw) w = __fmul_rn(w, c.decay);
+    w = __fsub_rn(w, upd);
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kAdamThreads)
+adam_fused_cast(const __grid_constant__ AdamParams p) {
+    const StepRecord *rec = p.rec;
+    if (rec->skip) return;
+    AdamScalars c;
+    c.coef = rec->coef;
+    c.bc1 = rec->bc1;
+    c.bc2 = rec->bc2;
+    c.lr = p.lr;
+    c.beta1 = p.beta1;
+    c.beta2 = p.beta2;
+    c.omb1 = p.omb1;
+    c.omb2 = p.omb2;
+    c.eps = p.eps;
+    c.wd = p.wd;
+    c.decay = p.decay;
+    c.adamw = p.adamw;
+    const long long stride = (long long)gridDim.x * kAdamThreads;
+    for (long long i = (long long)blockIdx.x * kAdamThreads + threadIdx.x; i < p.n_vec; i += stride) {
+        float4 g0 = ld_stream_f4(p.g + 2 * i), g1 = ld_stream_f4(p.g + 2 * i + 1);
+        float4 w0 = ld_stream_f4(p.master + 2 * i), w1 = ld_stream_f4(p.master + 2 * i + 1);
+        float4 m0 = ld_stream_f4(p.m + 2 * i), m1 = ld_stream_f4(p.m + 2 * i + 1);
+        float4 v0 = ld_stream_f4(p.v + 2 * i), v1 = ld_stream_f4(p.v + 2 * i + 1);
+        adam1(c, g0.x, w0.x, m0.x, v0.x);
+        adam1(c, g0.y, w0.y, m0.y, v0.y);
+        adam1(c, g0.z, w0.z, m0.z, v0.z);
+        adam1(c, g0.w, w0.w, m0.w, v0.w);
+        adam1(c, g1.x, w1.x, m1.x, v1.x);
+        adam1(c, g1.y, w1.y, m1.y, v1.y);
+        adam1(c, g1.z, w1.z, m1.z, v1.z);
+        adam1(c, g1.w, w1.w, m1.w, v1.w);
+        st_stream_f4(p.master + 2 * i, w0);
+        st_stream_f4(p.master + 2 * i + 1, w1);
+        st_stream_f4(p.m + 2 * i, m0);
+        st_stream_f4(p.m + 2 * i + 1, m1);
+        st_stream_f4(p.v + 2 * i, v0);
+        st_stream_f4(p.v + 2 * i + 1, v1);
+        if (p.param) {
+            uint4 q;
+            q.x = pack2<BF16>(w0.x, w0.y);
+            q.y = pack2<BF16>(w0.z, w0.w);
+            q.z = pack2<BF16>(w1.x, w1.y);
+            q.w = pack2<BF16>(w1.z, w1.w);
+            st_stream_u4(p.param + i, q);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ K4 gather
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// bounded wait: at most `polls` try_wait polls (0: give up at once)
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long polls) {
+    for (long long i = 0; i < polls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_addr(src_smem)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+template <int MAXN>
+struct GatherParams {
+    const char *src[MAXN];  // shard j at this unit's offset
+    char *dst;
+    long long shard_bytes;
+    long long chunks_per_shard;
+    long long n_chunks;
+    long long spin_limit;
+    int *error;
+    int n;
+};
+
+template <int MAXN>
+__global__ void __launch_bounds__(32)
+gather_layer_tma(const __grid_constant__ GatherParams<MAXN> p) {
+    extern __shared__ __align__(128) unsigned char stage_buf[];
+    __shared__ __align__(8) uint64_t bar[kGatherStages];
+    if (threadIdx.x != 0) return;  // one thread drives the copy engine
+    if (blockIdx.x >= p.n_chunks) return;
+    const long long count = (p.n_chunks - blockIdx.x + gridDim.x - 1) / gridDim.x;
+
+    for (int s = 0; s < kGatherStages; ++s) mbar_init(&bar[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+
+    auto chunk_src = [&](long long k, const char *&src, char *&dst, uint32_t &bytes) {
+        const long long c = blockIdx.x + k * gridDim.x;
+        const long long j = c / p.chunks_per_shard;
+        const long long off = (c - j * p.chunks_per_shard) * (long long)kGatherChunk;
+        const long long rem = p.shard_bytes - off;
+        bytes = rem < (long long)kGatherChunk ? (uint32_t)rem : kGatherChunk;
+        src = p.src[j] + off;
+        dst = p.dst + j * p.shard_bytes + off;
+    };
+    auto issue = [&](long long k) {
+        const char *src;
+        char *dst;
+        uint32_t bytes;
+        chunk_src(k, src, dst, bytes);
+        const int s = (int)(k % kGatherStages);
+        mbar_expect_tx(&bar[s], bytes);
+        bulk_load(stage_buf + (size_t)s * kGatherChunk, src, bytes, &bar[s]);
+    };
+
+    long long issued = 0;
+    for (; issued < count && issued < kGatherStages; ++issued) issue(issued);
+
+    long long k = 0;
+    bool ok = true;
+    for (; k < count; ++k) {
+        const int s = (int)(k % kGatherStages);
+        const uint32_t parity = (uint32_t)((k / kGatherStages) & 1);
+        if (!mbar_wait_bounded(&bar[s], parity, p.spin_limit)) {
+            ok = false;
+            break;
+        }
+        const char *src;
+        char *dst;
+        uint32_t bytes;
+        chunk_src(k, src, dst, bytes);
+        bulk_store(dst, stage_buf + (size_t)s * kGatherChunk, bytes);
+        bulk_commit();
+        // refill the stage of chunk k-1, whose store may still be reading it:
+        // allow only the newest store group (chunk k) to be pending.
+        if (k >= 1 && issued < count) {
+            bulk_wait_read1();
+            issue(issued);
+            ++issued;
+        }
+    }
+    if (!ok) {
+        atomicExch(p.error, 1);
+        // drain: every load issued after the failed wait must land before the
+        // CTA's shared memory is released
+        for (long long kk = k; kk < issued; ++kk) {
+            const int s = (int)(kk % kGatherStages);
+            mbar_wait_bounded(&bar[s], (uint32_t)((kk / kGatherStages) & 1), kDrainPolls);
+        }
+    }
+    bulk_wait_all();
+}
+
+// -------------------------------------------------------------- host helpers
+
+struct DevInfo {
+    int sms = 0;
+};
+
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+template <typename K>
+int occupancy(K kernel, int threads, size_t smem) {
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, smem) != cudaSuccess)
+        blocks = 1;
+    return blocks < 1 ? 1 : blocks;
+}
+
+template <int MAXN, bool BF16>
+cudaError_t reduce_impl(const void *const *slices, int n, int64_t offset, int64_t len, float inv,
+                        float *g, double *partials, unsigned *overflow, cudaStream_t stream) {
+    ReduceParams<MAXN> p;
+    for (int j = 0; j < n; ++j)
+        p.src[j] = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(slices[j]) + offset);
+    for (int j = n; j < MAXN; ++j) p.src[j] = nullptr;
+    p.g = reinterpret_cast<float4 *>(g + offset);
+    p.partials = partials + offset / kTile;
+    p.overflow = overflow;
+    p.len = len;
+    p.inv = inv;
+    p.n = n;
+    static const int occ = occupancy(reduce_unscale_stats<MAXN, BF16>, kReduceThreads, 0);
+    const long long tiles = (len + kTile - 1) / kTile;
+    long long grid = (long long)sm_count() * occ;
+    if (grid > tiles) grid = tiles;
+    if (grid < 1) return cudaSuccess;
+    reduce_unscale_stats<MAXN, BF16><<<(unsigned)grid, kReduceThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t adam_impl(const AdamParams &p, cudaStream_t stream) {
+    static const int occ = occupancy(adam_fused_cast<BF16>, kAdamThreads, 0);
+    long long grid = (long long)sm_count() * occ;
+    const long long need = (p.n_vec + kAdamThreads - 1) / kAdamThreads;
+    if (grid > need) grid = need;
+    if (grid < 1) return cudaSuccess;
+    adam_fused_cast<BF16><<<(unsigned)grid, kAdamThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int MAXN>
+cudaError_t gather_impl(const void *const *shards, int n, int64_t src_off, int64_t shard_bytes,
+                        void *out, int64_t spin_limit, int *error, cudaStream_t stream) {
+    GatherParams<MAXN> p;
+    for (int j = 0; j < n; ++j) p.src[j] = static_cast<const char *>(shards[j]) + src_off;
+    for (int j = n; j < MAXN; ++j) p.src[j] = nullptr;
+    p.dst = static_cast<char *>(out);
+    p.shard_bytes = shard_bytes;
+    p.chunks_per_shard = (shard_bytes + kGatherChunk - 1) / kGatherChunk;
+    p.n_chunks = p.chunks_per_shard * n;
+    p.spin_limit = spin_limit;
+    p.error = error;
+    p.n = n;
+    if (p.n_chunks == 0) return cudaSuccess;
+    const size_t smem = (size_t)kGatherStages * kGatherChunk;
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        gather_layer_tma<MAXN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (attr != cudaSuccess) return attr;
+    long long grid = sm_count();
+    if (grid > p.n_chunks) grid = p.n_chunks;
+    gather_layer_tma<MAXN><<<(unsigned)grid, 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_dev[dev].sms == 0) {
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        g_dev[dev].sms = sms > 0 ? sms : 1;
+    }
+    return g_dev[dev].sms;
+}
+
+cudaError_t launch_reduce(const void *const *slices, int n, int lp, int64_t offset, int64_t len,
+                          float inv, float *g, double *partials, unsigned *overflow,
+                          cudaStream_t stream) {
+    if (n <= 64)
+        return lp ? reduce_impl<64, true>(slices, n, offset, len, inv, g, partials, overflow, stream)
+                  : reduce_impl<64, false>(slices, n, offset, len, inv, g, partials, overflow, stream);
+    return lp ? reduce_impl<1024, true>(slices, n, offset, len, inv, g, partials, overflow, stream)
+              : reduce_impl<1024, false>(slices, n, offset, len, inv, g, partials, overflow, stream);
+}
+
+cudaError_t launch_decide(const double *partials, int64_t tiles_per_slot, const uint64_t *active_mask,
+                          int n_slots, double remote_sumsq, int remote_overflow, float clip,
+                          float loss_scale, int growth_interval, float beta1, float beta2,
+                          StepRecord *rec, cudaStream_t stream) {
+    DecideParams p;
+    p.partials = partials;
+    p.tiles_per_slot = tiles_per_slot;
+    for (int i = 0; i < 1024 / 64; ++i) p.mask[i] = active_mask[i];
+    p.n_slots = n_slots;
+    p.remote_sumsq = remote_sumsq;
+    p.remote_overflow = remote_overflow;
+    p.clip = clip;
+    p.loss_scale = loss_scale;
+    p.beta1 = beta1;
+    p.beta2 = beta2;
+    p.growth_interval = growth_interval;
+    p.rec = rec;
+    norm_finalize_decide<<<1, kDecideThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adam(const float *g, float *master, float *m, float *v, void *param, int lp,
+                        int64_t len, const StepRecord *rec, float lr, float beta1, float beta2,
+                        float omb1, float omb2, float eps, float wd, float decay, int adamw,
+                        cudaStream_t stream) {
+    AdamParams p;
+    p.g = reinterpret_cast<const float4 *>(g);
+    p.master = reinterpret_cast<float4 *>(master);
+    p.m = reinterpret_cast<float4 *>(m);
+    p.v = reinterpret_cast<float4 *>(v);
+    p.param = reinterpret_cast<uint4 *>(param);
+    p.rec = rec;
+    p.n_vec = len / 8;
+    p.lr = lr;
+    p.beta1 = beta1;
+    p.beta2 = beta2;
+    p.omb1 = omb1;
+    p.omb2 = omb2;
+    p.eps = eps;
+    p.wd = wd;
+    p.decay = decay;
+    p.adamw = adamw;
+    return lp ? adam_impl<true>(p, stream) : adam_impl<false>(p, stream);
+}
+
+cudaError_t launch_gather(const void *const *shards, int n, int64_t src_offset_bytes,
+                          int64_t shard_bytes, void *out, int64_t spin_limit, int *error,
+                          cudaStream_t stream) {
+    if (n <= 64)
+        return gather_impl<64>(shards, n, src_offset_bytes, shard_bytes, out, spin_limit, error, stream);
+    return gather_impl<1024>(shards, n, src_offset_bytes, shard_bytes, out, spin_limit, error, stream);
+}
+
+}  // namespace zk

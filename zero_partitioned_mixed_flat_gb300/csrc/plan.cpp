@@ -1,0 +1,489 @@
+// plan.cpp -- host side of libzero: the flat-buffer partitioner, the
+// accounting, argument validation, the per-step state machine and the
+// extern "C" entry points declared in include/zero.h.
+#include "zero.h"
+#include "zero_internal.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+namespace {
+
+thread_local std::string g_last_error;
+
+zero_status fail(zero_status code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+zero_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(ZERO_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t round_up(int64_t x, int64_t q) { return q == 0 ? x : ((x + q - 1) / q) * q; }
+
+enum Phase { kIdle = 0, kReducing = 1, kDecided = 2 };
+
+constexpr int64_t kDefaultSpinLimit = int64_t(1) << 21;
+
+}  // namespace
+
+struct zero_plan {
+    // layout
+    int64_t psi = 0, psi_p = 0, part = 0;
+    int32_t n_ranks = 1, align = 128, stage = 1, lp = 0;
+    std::vector<int64_t> sizes, tensor_off;
+    std::vector<int32_t> unit_of;
+    std::vector<int64_t> unit_off, unit_pad;  // unit_off has n_units + 1 entries
+    int64_t tiles_per_part = 0;
+    int32_t slots = 1;  // partition slots with partial sums (N, or 1 for DDP)
+    // device scratch (allocated on first device call)
+    int device = -1;
+    double *d_partials = nullptr;
+    zk::StepRecord *d_rec = nullptr;
+    // step state (host)
+    Phase phase = kIdle;
+    uint64_t active[ZERO_MAX_RANKS / 64] = {0};
+    int32_t growth_interval = 1000;
+    int64_t spin_limit = kDefaultSpinLimit;
+
+    int32_t n_units() const { return int32_t(unit_pad.size()); }
+    int64_t shard_len(int32_t u) const { return stage == 0 ? unit_pad[u] : unit_pad[u] / n_ranks; }
+};
+
+namespace {
+
+// Build the layout.  The flat buffer is the tensors back to back; every unit
+// (one unit unless stage 3) is padded up to a multiple of n_ranks * align.
+zero_status build_layout(zero_plan *p) {
+    const int64_t quantum = int64_t(p->n_ranks) * p->align;
+    const size_t nt = p->sizes.size();
+    p->tensor_off.assign(nt, 0);
+    p->unit_off.clear();
+    p->unit_pad.clear();
+    int64_t flat = 0, total = 0;
+    size_t t = 0;
+    int32_t unit = 0;
+    do {
+        int64_t fill = 0;
+        p->unit_off.push_back(flat);
+        while (t < nt && (p->unit_of.empty() || p->unit_of[t] == unit)) {
+            p->tensor_off[t] = flat + fill;
+            fill += p->sizes[t];
+            ++t;
+        }
+        const int64_t padded = round_up(fill, quantum);
+        p->unit_pad.push_back(padded);
+        flat += padded;
+        total += fill;
+        ++unit;
+    } while (t < nt);
+    p->unit_off.push_back(flat);
+    p->psi = total;
+    p->psi_p = flat;
+    p->part = p->stage == 0 ? flat : flat / p->n_ranks;
+    p->slots = p->stage == 0 ? 1 : p->n_ranks;
+    p->tiles_per_part = (p->part + zk::kTile - 1) / zk::kTile;
+    return ZERO_OK;
+}
+
+zero_status ensure_device(zero_plan *p) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (p->device >= 0) {
+        if (dev != p->device)
+            return fail(ZERO_EINVAL, "plan scratch lives on device %d, current device is %d", p->device,
+                        dev);
+        return ZERO_OK;
+    }
+    const size_t n_part = size_t(p->slots) * size_t(p->tiles_per_part > 0 ? p->tiles_per_part : 1);
+    e = cudaMalloc(reinterpret_cast<void **>(&p->d_partials), n_part * sizeof(double));
+    if (e != cudaSuccess) {
+        p->d_partials = nullptr;
+        cudaGetLastError();
+        return fail(ZERO_ENOMEM, "cudaMalloc of %zu partial sums failed", n_part);
+    }
+    e = cudaMalloc(reinterpret_cast<void **>(&p->d_rec), sizeof(zk::StepRecord));
+    if (e != cudaSuccess) {
+        cudaFree(p->d_partials);
+        p->d_partials = nullptr;
+        p->d_rec = nullptr;
+        cudaGetLastError();
+        return fail(ZERO_ENOMEM, "cudaMalloc of the step record failed");
+    }
+    zk::StepRecord init;
+    std::memset(&init, 0, sizeof init);
+    init.coef = 1.0f;
+    e = cudaMemcpy(p->d_rec, &init, sizeof init, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step record)");
+    e = cudaMemset(p->d_partials, 0, n_part * sizeof(double));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(partials)");
+    p->device = dev;
+    return ZERO_OK;
+}
+
+zero_status check_rank(const zero_plan *p, int32_t rank) {
+    if (rank < 0 || rank >= p->n_ranks) return fail(ZERO_EINVAL, "rank %d outside [0, %d)", rank, p->n_ranks);
+    if (p->stage == 0 && rank != 0)
+        return fail(ZERO_EINVAL, "stage 0 (DDP) simulates one replica: rank must be 0");
+    return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *zero_last_error(void) { return g_last_error.c_str(); }
+
+zero_status zero_plan_create(int64_t psi, int32_t n_ranks, const int64_t *tensor_sizes,
+                             int32_t n_tensors, int32_t align, int32_t stage,
+                             const int32_t *unit_of_tensor, zero_lp lp, zero_plan **out) {
+    if (!out) return fail(ZERO_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS)
+        return fail(ZERO_EINVAL, "n_ranks %d outside [1, %d]", n_ranks, ZERO_MAX_RANKS);
+    if (align < 8 || align % 8 != 0) return fail(ZERO_EINVAL, "align %d is not a positive multiple of 8", align);
+    if (stage < 0 || stage > 3) return fail(ZERO_EINVAL, "stage %d outside [0, 3]", stage);
+    if (lp != ZERO_FP16 && lp != ZERO_BF16) return fail(ZERO_EINVAL, "unknown lp type %d", int(lp));
+    if (n_tensors < 0) return fail(ZERO_EINVAL, "n_tensors < 0");
+    if (n_tensors > 0 && !tensor_sizes) return fail(ZERO_EINVAL, "tensor_sizes is NULL");
+    zero_plan *p = new (std::nothrow) zero_plan();
+    if (!p) return fail(ZERO_ENOMEM, "host allocation of the plan failed");
+    p->n_ranks = n_ranks;
+    p->align = align;
+    p->stage = stage;
+    p->lp = lp;
+    if (n_tensors == 0 || !tensor_sizes) {
+        if (psi < 0) {
+            delete p;
+            return fail(ZERO_EINVAL, "psi < 0 without a tensor list");
+        }
+        p->sizes.assign(1, psi);
+    } else {
+        int64_t sum = 0;
+        p->sizes.assign(tensor_sizes, tensor_sizes + n_tensors);
+        for (int64_t s : p->sizes) {
+            if (s < 0) {
+                delete p;
+                return fail(ZERO_EINVAL, "negative tensor size");
+            }
+            sum += s;
+        }
+        if (psi >= 0 && psi != sum) {
+            delete p;
+            return fail(ZERO_EINVAL, "psi %lld differs from the tensor sizes' sum %lld", (long long)psi,
+                        (long long)sum);
+        }
+    }
+    if (stage == 3 && unit_of_tensor && n_tensors > 0) {
+        p->unit_of.assign(unit_of_tensor, unit_of_tensor + n_tensors);
+        if (p->unit_of[0] != 0) {
+            delete p;
+            return fail(ZERO_EINVAL, "unit_of_tensor must start at unit 0");
+        }
+        for (int32_t t = 1; t < n_tensors; ++t) {
+            const int32_t d = p->unit_of[t] - p->unit_of[t - 1];
+            if (d != 0 && d != 1) {
+                delete p;
+                return fail(ZERO_EINVAL, "unit_of_tensor must be non-decreasing without gaps");
+            }
+        }
+    }
+    build_layout(p);
+    *out = p;
+    return ZERO_OK;
+}
+
+zero_status zero_plan_query(const zero_plan *p, int64_t *psi_padded, int64_t *part_len,
+                            int64_t *tensor_offsets) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (psi_padded) *psi_padded = p->psi_p;
+    if (part_len) *part_len = p->part;
+    if (tensor_offsets)
+        std::memcpy(tensor_offsets, p->tensor_off.data(), p->tensor_off.size() * sizeof(int64_t));
+    return ZERO_OK;
+}
+
+zero_status zero_plan_units(const zero_plan *p, int32_t *n_units, int64_t *unit_offsets,
+                            int64_t *unit_padded) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (n_units) *n_units = p->n_units();
+    if (unit_offsets) std::memcpy(unit_offsets, p->unit_off.data(), p->unit_off.size() * sizeof(int64_t));
+    if (unit_padded) std::memcpy(unit_padded, p->unit_pad.data(), p->unit_pad.size() * sizeof(int64_t));
+    return ZERO_OK;
+}
+
+zero_status zero_plan_fragments(const zero_plan *p, int32_t rank, int64_t max_frag, int64_t *frag,
+                                int64_t *count) {
+    if (!p || !count) return fail(ZERO_EINVAL, "plan or count is NULL");
+    if (rank < 0 || rank >= p->n_ranks) return fail(ZERO_EINVAL, "rank %d outside [0, %d)", rank, p->n_ranks);
+    if (max_frag > 0 && !frag) return fail(ZERO_EINVAL, "frag is NULL");
+    int64_t n = 0, part_pos = 0;
+    size_t t = 0;
+    for (int32_t u = 0; u < p->n_units(); ++u) {
+        const int64_t shard = p->shard_len(u);
+        const int64_t lo = p->unit_off[u] + (p->stage == 0 ? 0 : rank * shard);
+        const int64_t hi = lo + shard;
+        // tensors of unit u are contiguous in the list
+        for (; t < p->sizes.size() && (p->unit_of.empty() || p->unit_of[t] == u); ++t) {
+            const int64_t a = std::max(lo, p->tensor_off[t]);
+            const int64_t b = std::min(hi, p->tensor_off[t] + p->sizes[t]);
+            if (a >= b) continue;
+            if (n < max_frag) {
+                frag[4 * n + 0] = int64_t(t);
+                frag[4 * n + 1] = a - p->tensor_off[t];
+                frag[4 * n + 2] = part_pos + (a - lo);
+                frag[4 * n + 3] = b - a;
+            }
+            ++n;
+        }
+        part_pos += shard;
+    }
+    *count = n;
+    return ZERO_OK;
+}
+
+zero_status zero_plan_set_loss_scaler(zero_plan *p, int32_t growth_interval) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    p->growth_interval = growth_interval;
+    return ZERO_OK;
+}
+
+zero_status zero_plan_set_spin_limit(zero_plan *p, int64_t polls) {
+    if (!p || polls < 0) return fail(ZERO_EINVAL, "plan is NULL or polls < 0");
+    p->spin_limit = polls;
+    return ZERO_OK;
+}
+
+zero_status zero_plan_set_state(zero_plan *p, int64_t step, int32_t good_steps) {
+    if (!p || step < 0 || good_steps < 0) return fail(ZERO_EINVAL, "bad plan state");
+    zero_status st = ensure_device(p);
+    if (st != ZERO_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    zk::StepRecord rec;
+    e = cudaMemcpy(&rec, p->d_rec, sizeof rec, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step record)");
+    rec.step = step;
+    rec.good_steps = good_steps;
+    e = cudaMemcpy(p->d_rec, &rec, sizeof rec, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step record)");
+    return ZERO_OK;
+}
+
+zero_status zero_reduce_partition(zero_plan *p, int32_t rank, const void *const *grad_slices,
+                                  float *grad_out, float loss_scale, int64_t bucket_elems,
+                                  void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    zero_status st = check_rank(p, rank);
+    if (st != ZERO_OK) return st;
+    if (!grad_slices || (!grad_out && p->part > 0)) return fail(ZERO_EINVAL, "NULL slices or output");
+    if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale))
+        return fail(ZERO_EINVAL, "loss_scale must be finite and > 0");
+    if (bucket_elems < 0) return fail(ZERO_EINVAL, "bucket_elems < 0");
+    for (int32_t j = 0; j < p->n_ranks; ++j) {
+        if (!grad_slices[j] && p->part > 0) return fail(ZERO_EINVAL, "grad_slices[%d] is NULL", j);
+        if (!aligned16(grad_slices[j])) return fail(ZERO_EALIGN, "grad_slices[%d] is not 16-byte aligned", j);
+    }
+    if (!aligned16(grad_out)) return fail(ZERO_EALIGN, "grad_out is not 16-byte aligned");
+    st = ensure_device(p);
+    if (st != ZERO_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->phase != kReducing) {
+        // a new step: forget the previous step's partitions and overflow
+        std::memset(p->active, 0, sizeof p->active);
+        cudaError_t e = cudaMemsetAsync(&p->d_rec->overflow, 0, sizeof(unsigned), s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(overflow)");
+        p->phase = kReducing;
+    }
+    const int32_t slot = p->stage == 0 ? 0 : rank;
+    p->active[slot >> 6] |= uint64_t(1) << (slot & 63);
+    const float inv = float(1.0 / (double(loss_scale) * double(p->n_ranks)));
+    double *partials = p->d_partials + int64_t(slot) * p->tiles_per_part;
+    int64_t bucket = bucket_elems == 0 ? p->part : round_up(bucket_elems, zk::kTile);
+    if (bucket <= 0) bucket = p->part;
+    for (int64_t b0 = 0; b0 < p->part; b0 += bucket) {
+        const int64_t len = std::min(bucket, p->part - b0);
+        cudaError_t e = zk::launch_reduce(grad_slices, p->n_ranks, p->lp, b0, len, inv, grad_out,
+                                          partials, &p->d_rec->overflow, s);
+        if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
+    }
+    return ZERO_OK;
+}
+
+zero_status zero_partition_stats(zero_plan *p, double *sumsq, int32_t *overflow, void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (p->phase != kReducing) return fail(ZERO_ESTATE, "no partition reduced in the current step");
+    zero_status st = ensure_device(p);
+    if (st != ZERO_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    // sum the partials of the active slots on the host, in slot then tile order
+    double acc = 0.0;
+    std::vector<double> host(size_t(p->tiles_per_part));
+    for (int32_t r = 0; r < p->slots; ++r) {
+        if (!((p->active[r >> 6] >> (r & 63)) & 1u)) continue;
+        e = cudaMemcpy(host.data(), p->d_partials + int64_t(r) * p->tiles_per_part,
+                       host.size() * sizeof(double), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(partials)");
+        for (double x : host) acc += x;
+    }
+    unsigned of = 0;
+    e = cudaMemcpy(&of, &p->d_rec->overflow, sizeof of, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(overflow)");
+    if (sumsq) *sumsq = acc;
+    if (overflow) *overflow = of ? 1 : 0;
+    return ZERO_OK;
+}
+
+zero_status zero_adam_step(zero_plan *p, int32_t rank, const float *grad, float *master, float *m,
+                           float *v, void *param_out, float lr, float beta1, float beta2, float eps,
+                           float wd, int32_t adamw, float loss_scale, float clip,
+                           double remote_sumsq, int32_t remote_overflow, void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    zero_status st = check_rank(p, rank);
+    if (st != ZERO_OK) return st;
+    if (p->part > 0 && (!grad || !master || !m || !v)) return fail(ZERO_EINVAL, "NULL state pointer");
+    if (!aligned16(grad) || !aligned16(master) || !aligned16(m) || !aligned16(v) || !aligned16(param_out))
+        return fail(ZERO_EALIGN, "a state or parameter pointer is not 16-byte aligned");
+    if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale))
+        return fail(ZERO_EINVAL, "loss_scale must be finite and > 0");
+    if (!(remote_sumsq >= 0.0)) return fail(ZERO_EINVAL, "remote_sumsq must be >= 0");
+    if (p->phase == kIdle) return fail(ZERO_ESTATE, "zero_adam_step before any zero_reduce_partition");
+    st = ensure_device(p);
+    if (st != ZERO_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->phase == kReducing) {
+        cudaError_t e = zk::launch_decide(p->d_partials, p->tiles_per_part, p->active, p->slots,
+                                          remote_sumsq, remote_overflow ? 1 : 0, clip, loss_scale,
+                                          p->growth_interval, beta1, beta2, p->d_rec, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decide kernel launch");
+        p->phase = kDecided;
+    }
+    const float omb1 = 1.0f - beta1;
+    const float omb2 = 1.0f - beta2;
+    const float decay = float(1.0 - double(lr) * double(wd));
+    void *param = nullptr;
+    if (param_out) {
+        const int64_t off = (p->stage == 3) ? 0 : int64_t(rank) * p->part;
+        param = static_cast<uint16_t *>(param_out) + off;
+    }
+    cudaError_t e = zk::launch_adam(grad, master, m, v, param, p->lp, p->part, p->d_rec, lr, beta1,
+                                    beta2, omb1, omb2, eps, wd, decay, adamw ? 1 : 0, s);
+    if (e != cudaSuccess) return cuda_fail(e, "adam kernel launch");
+    return ZERO_OK;
+}
+
+zero_status zero_step_result(zero_plan *p, double *norm, int32_t *skipped, float *new_loss_scale,
+                             int64_t *step) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    zero_status st = ensure_device(p);
+    if (st != ZERO_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    zk::StepRecord rec;
+    e = cudaMemcpy(&rec, p->d_rec, sizeof rec, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step record)");
+    if (norm) *norm = rec.norm;
+    if (skipped) *skipped = rec.skip;
+    if (new_loss_scale) *new_loss_scale = rec.loss_scale;
+    if (step) *step = rec.step;
+    if (rec.error) {
+        const int zero = 0;
+        e = cudaMemcpy(&p->d_rec->error, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+        return fail(ZERO_ETIMEOUT, "a bounded device wait gave up");
+    }
+    return ZERO_OK;
+}
+
+zero_status zero_plan_check(zero_plan *p) {
+    return zero_step_result(p, nullptr, nullptr, nullptr, nullptr);
+}
+
+zero_status zero_gather_layer(zero_plan *p, int32_t unit, const void *const *shards, void *out,
+                              void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (p->stage != 3) return fail(ZERO_EINVAL, "zero_gather_layer needs a stage-3 plan");
+    if (unit < 0 || unit >= p->n_units()) return fail(ZERO_EINVAL, "unit %d outside [0, %d)", unit, p->n_units());
+    const int64_t shard = p->shard_len(unit);
+    if (!shards || (!out && shard > 0)) return fail(ZERO_EINVAL, "NULL shards or output");
+    for (int32_t j = 0; j < p->n_ranks; ++j) {
+        if (!shards[j] && shard > 0) return fail(ZERO_EINVAL, "shards[%d] is NULL", j);
+        if (!aligned16(shards[j])) return fail(ZERO_EALIGN, "shards[%d] is not 16-byte aligned", j);
+    }
+    if (!aligned16(out)) return fail(ZERO_EALIGN, "out is not 16-byte aligned");
+    zero_status st = ensure_device(p);
+    if (st != ZERO_OK) return st;
+    int64_t off = 0;  // the unit's shard offset inside each rank's partition
+    for (int32_t u = 0; u < unit; ++u) off += p->shard_len(u);
+    cudaError_t e = zk::launch_gather(shards, p->n_ranks, off * 2, shard * 2, out, p->spin_limit,
+                                      &p->d_rec->error, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+    return ZERO_OK;
+}
+
+zero_status zero_memory_report(int64_t psi, int32_t n_ranks, int32_t align, double formula_bytes[4],
+                               int64_t actual_bytes[4], int64_t comm_elems[4]) {
+    if (psi < 0 || n_ranks < 1 || align < 1) return fail(ZERO_EINVAL, "psi < 0, n_ranks < 1 or align < 1");
+    const int64_t n = n_ranks;
+    // x * psi / n as one rounding: whole part plus the remainder's fraction
+    auto per_rank = [&](int64_t mult, int64_t base) {
+        const int64_t num = mult * psi;
+        return double(base + num / n) + double(num % n) / double(n);
+    };
+    if (formula_bytes) {
+        formula_bytes[0] = double(16 * psi);
+        formula_bytes[1] = per_rank(12, 4 * psi);
+        formula_bytes[2] = per_rank(14, 2 * psi);
+        formula_bytes[3] = per_rank(16, 0);
+    }
+    if (actual_bytes) {
+        const int64_t psi_p = round_up(psi, n * align);
+        const int64_t part = psi_p / n;
+        actual_bytes[0] = 16 * psi;
+        actual_bytes[1] = 4 * psi_p + 12 * part;
+        actual_bytes[2] = 2 * psi_p + 14 * part;
+        actual_bytes[3] = 16 * part;
+    }
+    if (comm_elems) {
+        comm_elems[0] = 2 * psi;  // all-reduce = reduce-scatter + all-gather
+        comm_elems[1] = 2 * psi;
+        comm_elems[2] = 2 * psi;
+        comm_elems[3] = 3 * psi;  // + one more all-gather (forward and backward)
+    }
+    return ZERO_OK;
+}
+
+void zero_plan_destroy(zero_plan *p) {
+    if (!p) return;
+    if (p->device >= 0) {
+        int cur = 0;
+        cudaGetDevice(&cur);
+        cudaSetDevice(p->device);
+        cudaDeviceSynchronize();
+        cudaFree(p->d_partials);
+        cudaFree(p->d_rec);
+        cudaSetDevice(cur);
+    }
+    delete p;
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// zero_internal.h -- shared between the host plan (plan.cpp) and the CUDA
+// kernels (kernels.cu) of libzero.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace zk {
+
+// Elements per norm tile.  Each tile's sum of squares is one fp64 partial,
+// computed by one CTA in a fixed order, so the global norm is the same for
+// every grid size and every bucket size (buckets are whole tiles).
+constexpr int64_t kTile = 32768;
+
+// Per-plan device record of the step decision and the optimizer step state.
+struct StepRecord {
+    double norm;          // global gradient norm of the decided step
+    double sumsq;         // local + remote sum of squares
+    float coef;           // clip coefficient (1 when not clipping)
+    float loss_scale;     // S for the next step
+    float bc1, bc2;       // 1 - beta1^t, 1 - beta2^t
+    long long step;       // Adam step counter t
+    int skip;             // 1: overflow, the update is skipped
+    int good_steps;       // consecutive non-skipped steps since the last growth
+    unsigned overflow;    // set by the reduce kernel when a sum is not finite
+    int error;            // set when a bounded device wait gives up
+    int pad_[2];
+};
+
+int sm_count();
+
+cudaError_t launch_reduce(const void *const *slices, int n, int lp,
+                          int64_t offset, int64_t len, float inv, float *g,
+                          double *partials, unsigned *overflow,
+                          cudaStream_t stream);
+
+cudaError_t launch_decide(const double *partials, int64_t tiles_per_slot,
+                          const uint64_t *active_mask, int n_slots,
+                          double remote_sumsq, int remote_overflow, float clip,
+                          float loss_scale, int growth_interval, float beta1,
+                          float beta2, StepRecord *rec, cudaStream_t stream);
+
+cudaError_t launch_adam(const float *g, float *master, float *m, float *v,
+                        void *param, int lp, int64_t len,
+                        const StepRecord *rec, float lr, float beta1,
+                        float beta2, float omb1, float omb2, float eps,
+                        float wd, float decay, int adamw, cudaStream_t stream);
+
+cudaError_t launch_gather(const void *const *shards, int n, int64_t src_offset_bytes,
+                          int64_t shard_bytes, void *out, int64_t spin_limit,
+                          int *error, cudaStream_t stream);
+
+}  // namespace zk

@@ -1,0 +1,82 @@
+"""ZeroPlan: an owning handle around a libzero plan (marshalling only)."""
+from typing import Optional, Sequence
+
+from . import _abi as A
+
+
+class ZeroPlan:
+    """Owns one `zero_plan *`.  Methods map one-to-one onto the C calls."""
+
+    def __init__(self, psi: int, n_ranks: int, tensor_sizes: Optional[Sequence[int]] = None,
+                 align: int = 128, stage: int = 1, unit_of_tensor=None, lp: int = A.ZERO_FP16,
+                 growth_interval: Optional[int] = None):
+        self.handle = A.zero_plan_create(psi, n_ranks, tensor_sizes, align, stage,
+                                         unit_of_tensor, lp)
+        self.n_ranks, self.stage, self.lp, self.align = n_ranks, stage, lp, align
+        self.n_tensors = 0 if tensor_sizes is None else len(tensor_sizes)
+        self.psi_padded, self.part_len, self.tensor_offsets = A.zero_plan_query(
+            self.handle, self.n_tensors)
+        self.n_units, self.unit_offsets, self.unit_padded = A.zero_plan_units(self.handle)
+        if growth_interval is not None:
+            A.zero_plan_set_loss_scaler(self.handle, growth_interval)
+
+    # lifetime
+    def close(self):
+        if self.handle:
+            A.zero_plan_destroy(self.handle)
+            self.handle = 0
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # layout
+    def fragments(self, rank: int):
+        return A.zero_plan_fragments(self.handle, rank)
+
+    def keep_ranges(self, rank: int):
+        """(partition offset, length) of every non-padding run of rank's partition."""
+        return [(int(f[2]), int(f[3])) for f in self.fragments(rank)]
+
+    def shard_len(self, unit: int) -> int:
+        pad = int(self.unit_padded[unit])
+        return pad if self.stage == 0 else pad // self.n_ranks
+
+    def unit_shard_offset(self, unit: int) -> int:
+        return sum(self.shard_len(u) for u in range(unit))
+
+    # the step
+    def reduce(self, rank, grad_slices, grad_out, loss_scale, bucket_elems=0, stream=None):
+        A.zero_reduce_partition(self.handle, rank, grad_slices, grad_out, loss_scale,
+                                bucket_elems, stream)
+
+    def stats(self, stream=None):
+        return A.zero_partition_stats(self.handle, stream)
+
+    def adam(self, rank, grad, master, m, v, param_out, lr, beta1, beta2, eps, wd, adamw,
+             loss_scale, clip, remote_sumsq=0.0, remote_overflow=0, stream=None):
+        A.zero_adam_step(self.handle, rank, grad, master, m, v, param_out, lr, beta1, beta2,
+                         eps, wd, adamw, loss_scale, clip, remote_sumsq, remote_overflow, stream)
+
+    def result(self):
+        return A.zero_step_result(self.handle)
+
+    def check(self):
+        A.zero_plan_check(self.handle)
+
+    def gather(self, unit, shards, out, stream=None):
+        A.zero_gather_layer(self.handle, unit, shards, out, stream)
+
+    def set_state(self, step, good_steps=0):
+        A.zero_plan_set_state(self.handle, step, good_steps)
+
+    def set_spin_limit(self, polls):
+        A.zero_plan_set_spin_limit(self.handle, polls)

@@ -463,12 +463,29 @@ def main():
     return 0
 
 
+def host_mem_available():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
 def measure_e2e(run, steps, stream, sh, ws, dist, dev):
     """Same metric through the public API with host (pinned) gradient slices:
     each step copies the slices host->device, reduces, updates, and reads the
     step result back (a synchronising device->host copy)."""
     import torch
     torch.cuda.synchronize()
+    need = sum(int(t.numel()) * t.element_size() for t in run.slices.values())
+    avail = host_mem_available()
+    if avail is not None and need * 2 > avail:
+        log("e2e skipped: %.1f GB of host buffers needed, %.1f GB available" % (need / 1e9, avail / 1e9))
+        return {"value": None, "unit": UNIT, "skipped": "host memory: %.1f GB needed, %.1f GB "
+                "available" % (need / 1e9, avail / 1e9)}
     host = {}
     try:
         for r in run.ranks:

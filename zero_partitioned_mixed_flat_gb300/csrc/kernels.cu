@@ -90,6 +90,16 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 
 // ------------------------------------------------------------------ K1 reduce
 
+// hi + lo += x, error-free (Knuth's TwoSum: the rounding error of hi + x is
+// recovered exactly with round-to-nearest adds and kept in lo)
+__device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float x) {
+    const float s = __fadd_rn(hi, x);
+    const float bp = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(x, bp));
+    hi = s;
+    lo = __fadd_rn(lo, err);
+}
+
 template <int MAXN>
 struct ReduceParams {
     const uint4 *src[MAXN];  // slice j at the bucket start
@@ -104,14 +114,17 @@ struct ReduceParams {
 template <int MAXN, bool BF16>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
-    __shared__ float warp_sq[kReduceThreads / 32];
+    __shared__ double warp_sq[kReduceThreads / 32];
     const long long n_vec = p.len / kVec;
     const long long n_tiles = (p.len + kTile - 1) / kTile;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     bool bad = false;
 
     for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-        float sq = 0.0f;
+        // per-thread sum of squares as an unevaluated float pair (hi + lo):
+        // compensated, so the tile sum is accurate to ~1e-13 relative and the
+        // clip coefficient derived from it matches a sequential fp64 sum
+        float sq_hi = 0.0f, sq_lo = 0.0f;
         const long long v0 = tile * (kTile / kVec);
 #pragma unroll 1
         for (int it = 0; it < kTileIters; ++it) {
@@ -139,21 +152,22 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
             for (int k = 0; k < 8; ++k) {
                 bad |= !isfinite(s[k]);
                 o[k] = __fmul_rn(s[k], p.inv);
-                sq = __fadd_rn(sq, __fmul_rn(o[k], o[k]));
+                two_sum_acc(sq_hi, sq_lo, __fmul_rn(o[k], o[k]));
             }
             st_stream_f4(p.g + 2 * vi, make_float4(o[0], o[1], o[2], o[3]));
             st_stream_f4(p.g + 2 * vi + 1, make_float4(o[4], o[5], o[6], o[7]));
         }
-        // fixed-shape tree: lanes, then warps in order (fp64)
+        // fixed-shape fp64 tree: lanes (xor butterfly), then warps in order
+        double sq = __dadd_rn((double)sq_hi, (double)sq_lo);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
-            sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, off));
+            sq = __dadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, off));
         if (lane == 0) warp_sq[warp] = sq;
         __syncthreads();
         if (threadIdx.x == 0) {
             double t = 0.0;
 #pragma unroll
-            for (int w = 0; w < kReduceThreads / 32; ++w) t = __dadd_rn(t, (double)warp_sq[w]);
+            for (int w = 0; w < kReduceThreads / 32; ++w) t = __dadd_rn(t, warp_sq[w]);
             p.partials[tile] = t;
         }
         __syncthreads();

@@ -104,6 +104,19 @@ def _make():
         ranks=[0], steps=4, loss_scale=1.0, growth_interval=0,
         grads_times_scale=False,
         notes="13B one flat tensor, N=16 rank 0, bf16, HBM-capacity case")
+    # small cases of the same kernels, for profiler captures (a few GB on the
+    # device, inputs still larger than the 129 MB L2); not benchmark lines
+    w["profile-zero2"] = Workload(
+        name="profile-zero2", sizes=[16 << 25], n_ranks=16, stage=2, lp=1, ranks=[0],
+        steps=4, loss_scale=1.0, growth_interval=0, grads_times_scale=False,
+        notes="13b-zero2 kernels at 2^29 parameters (P = 2^25)")
+    blocks = gpt2_block(1024)
+    w["profile-zero3"] = Workload(
+        name="profile-zero3", sizes=[64 << 20] + blocks + blocks,
+        unit_of_tensor=[0] + [1] * len(blocks) + [2] * len(blocks), n_ranks=64, stage=3,
+        lp=0, ranks=[0], steps=4, loss_scale=65536.0, growth_interval=1000,
+        grads_times_scale=True, gather=True,
+        notes="7.5b-zero3 kernels on 3 units (64M rest + two d=1024 blocks)")
     return w
 
 

@@ -154,6 +154,15 @@ zero_status zero_reduce_partition(zero_plan *plan, int32_t rank,
 zero_status zero_partition_stats(zero_plan *plan, double *sumsq,
                                  int32_t *overflow, void *stream);
 
+/* Multi-rank use: make this step's decision use exactly these global values
+ * (instead of the device's local sum plus remote_sumsq), so that every real
+ * rank, given the same totals, takes the bit-identical decision.  global_sumsq
+ * is the sum over all ranks of zero_partition_stats' sumsq (added in rank
+ * order by the caller); global_overflow the OR of their flags.  Valid after
+ * the step's reduces and before its first zero_adam_step.  Host only. */
+zero_status zero_step_set_global_stats(zero_plan *plan, double global_sumsq,
+                                       int32_t global_overflow);
+
 /* ----------------------------------------------------------------------
  * Decision + fused Adam/AdamW + cast ("10.6 ZeRO 与 FSDP" §10.6.2 Steps 3-4;
  * "年糕切片" §4.2 clipping, §4.3 loss scaling).

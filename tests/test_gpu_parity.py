@@ -255,3 +255,33 @@ def test_gather_wait_timeout_is_reported_and_recoverable(zlib):
     u, out, host = outs2[0]
     assert np.array_equal(synth.to_numpy_codes(out), oracle.gather(host))
     plan2.close()
+
+
+def test_global_stats_replace_the_local_sum(zlib):
+    # multi-rank use: the caller's global totals decide the step exactly
+    dev = torch.device("cuda")
+    n, part = 4, 3 * TILE
+    plan = _plan(n * part, n, 1)
+    sl = [synth.grad_slice(part, 1, 1e-3, 1.0, 0, 1, j, 0, dev) for j in range(n)]
+    g = torch.empty(part, device=dev)
+    w = torch.zeros(part, device=dev); m = torch.zeros(part, device=dev); v = torch.zeros(part, device=dev)
+    plan.reduce(0, sl, g, 1.0)
+    ss, of = plan.stats()
+    plan.set_global_stats(4.0 * ss, 0)
+    plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0, 123.0, 0)
+    r = plan.result()
+    assert r["norm"] == float(np.sqrt(4.0 * ss)) and r["skipped"] == 0
+    d = oracle.decide(4.0 * ss, 0, 1.0, 1.0, 0)
+    assert d["norm"] == r["norm"]
+    # a global overflow skips even though this rank's partition is finite
+    plan.reduce(0, sl, g, 1.0)
+    plan.set_global_stats(ss, 1)
+    before = w.clone()
+    plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0)
+    r = plan.result()
+    assert r["skipped"] == 1 and torch.equal(before, w)
+    # out of order: after the decision the step's stats are fixed
+    with pytest.raises(Z.ZeroError) as e:
+        plan.set_global_stats(ss, 0)
+    assert e.value.code == Z.ZERO_ESTATE
+    plan.close()

@@ -33,6 +33,7 @@ SIGNATURES = {
     "zero_plan_set_spin_limit": (_i32, [_vp, _i64]),
     "zero_reduce_partition": (_i32, [_vp, _i32, _vp, _vp, _f32, _i64, _vp]),
     "zero_partition_stats": (_i32, [_vp, _vp, _vp, _vp]),
+    "zero_step_set_global_stats": (_i32, [_vp, _f64, _i32]),
     "zero_adam_step": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32,
                               _f32, _i32, _f32, _f32, _f64, _i32, _vp]),
     "zero_step_result": (_i32, [_vp, _vp, _vp, _vp, _vp]),
@@ -175,6 +176,11 @@ def zero_partition_stats(plan: int, stream=None):
     _check(load().zero_partition_stats(plan, C.byref(ss), C.byref(of), _stream(stream)),
            "zero_partition_stats")
     return ss.value, of.value
+
+
+def zero_step_set_global_stats(plan: int, global_sumsq: float, global_overflow: int):
+    _check(load().zero_step_set_global_stats(plan, global_sumsq, int(global_overflow)),
+           "zero_step_set_global_stats")
 
 
 def zero_adam_step(plan: int, rank: int, grad, master, m, v, param_out, lr: float,

@@ -183,7 +183,9 @@ struct DecideParams {
     unsigned long long mask[1024 / 64];
     int n_slots;
     double remote_sumsq;
+    double global_sumsq;
     int remote_overflow;
+    int use_global;  // 1: the caller's global sum replaces local + remote
     float clip, loss_scale, beta1, beta2;
     int growth_interval;
     StepRecord *rec;
@@ -211,7 +213,7 @@ norm_finalize_decide(const __grid_constant__ DecideParams p) {
     StepRecord *rec = p.rec;
     double sumsq = 0.0;
     for (int w = 0; w < kDecideThreads / 32; ++w) sumsq = __dadd_rn(sumsq, wsum[w]);
-    sumsq = __dadd_rn(sumsq, p.remote_sumsq);
+    sumsq = p.use_global ? p.global_sumsq : __dadd_rn(sumsq, p.remote_sumsq);
     const double norm = sqrt(sumsq);
     const int skip = (rec->overflow != 0u) || (p.remote_overflow != 0);
     float coef = 1.0f;
@@ -565,9 +567,9 @@ cudaError_t launch_reduce(const void *const *slices, int n, int lp, int64_t offs
 }
 
 cudaError_t launch_decide(const double *partials, int64_t tiles_per_slot, const uint64_t *active_mask,
-                          int n_slots, double remote_sumsq, int remote_overflow, float clip,
-                          float loss_scale, int growth_interval, float beta1, float beta2,
-                          StepRecord *rec, cudaStream_t stream) {
+                          int n_slots, double remote_sumsq, int remote_overflow, int use_global,
+                          double global_sumsq, float clip, float loss_scale, int growth_interval,
+                          float beta1, float beta2, StepRecord *rec, cudaStream_t stream) {
     DecideParams p;
     p.partials = partials;
     p.tiles_per_slot = tiles_per_slot;
@@ -575,6 +577,8 @@ cudaError_t launch_decide(const double *partials, int64_t tiles_per_slot, const 
     p.n_slots = n_slots;
     p.remote_sumsq = remote_sumsq;
     p.remote_overflow = remote_overflow;
+    p.use_global = use_global;
+    p.global_sumsq = global_sumsq;
     p.clip = clip;
     p.loss_scale = loss_scale;
     p.beta1 = beta1;

@@ -61,6 +61,9 @@ struct zero_plan {
     uint64_t active[ZERO_MAX_RANKS / 64] = {0};
     int32_t growth_interval = 1000;
     int64_t spin_limit = kDefaultSpinLimit;
+    bool use_global = false;  // zero_step_set_global_stats was called this step
+    double global_sumsq = 0.0;
+    int32_t global_overflow = 0;
 
     int32_t n_units() const { return int32_t(unit_pad.size()); }
     int64_t shard_len(int32_t u) const { return stage == 0 ? unit_pad[u] : unit_pad[u] / n_ranks; }
@@ -308,6 +311,7 @@ zero_status zero_reduce_partition(zero_plan *p, int32_t rank, const void *const 
     if (p->phase != kReducing) {
         // a new step: forget the previous step's partitions and overflow
         std::memset(p->active, 0, sizeof p->active);
+        p->use_global = false;
         cudaError_t e = cudaMemsetAsync(&p->d_rec->overflow, 0, sizeof(unsigned), s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(overflow)");
         p->phase = kReducing;
@@ -353,6 +357,17 @@ zero_status zero_partition_stats(zero_plan *p, double *sumsq, int32_t *overflow,
     return ZERO_OK;
 }
 
+zero_status zero_step_set_global_stats(zero_plan *p, double global_sumsq, int32_t global_overflow) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (global_sumsq < 0.0) return fail(ZERO_EINVAL, "global_sumsq must be >= 0");
+    if (p->phase != kReducing)
+        return fail(ZERO_ESTATE, "global stats belong between a step's reduces and its first Adam call");
+    p->use_global = true;
+    p->global_sumsq = global_sumsq;
+    p->global_overflow = global_overflow ? 1 : 0;
+    return ZERO_OK;
+}
+
 zero_status zero_adam_step(zero_plan *p, int32_t rank, const float *grad, float *master, float *m,
                            float *v, void *param_out, float lr, float beta1, float beta2, float eps,
                            float wd, int32_t adamw, float loss_scale, float clip,
@@ -371,9 +386,11 @@ zero_status zero_adam_step(zero_plan *p, int32_t rank, const float *grad, float 
     if (st != ZERO_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->phase == kReducing) {
+        const int r_of = p->use_global ? (p->global_overflow ? 1 : 0) : (remote_overflow ? 1 : 0);
         cudaError_t e = zk::launch_decide(p->d_partials, p->tiles_per_part, p->active, p->slots,
-                                          remote_sumsq, remote_overflow ? 1 : 0, clip, loss_scale,
-                                          p->growth_interval, beta1, beta2, p->d_rec, s);
+                                          remote_sumsq, r_of, p->use_global ? 1 : 0,
+                                          p->global_sumsq, clip, loss_scale, p->growth_interval,
+                                          beta1, beta2, p->d_rec, s);
         if (e != cudaSuccess) return cuda_fail(e, "decide kernel launch");
         p->phase = kDecided;
     }

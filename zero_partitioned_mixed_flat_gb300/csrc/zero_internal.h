@@ -36,7 +36,8 @@ cudaError_t launch_reduce(const void *const *slices, int n, int lp,
 
 cudaError_t launch_decide(const double *partials, int64_t tiles_per_slot,
                           const uint64_t *active_mask, int n_slots,
-                          double remote_sumsq, int remote_overflow, float clip,
+                          double remote_sumsq, int remote_overflow,
+                          int use_global, double global_sumsq, float clip,
                           float loss_scale, int growth_interval, float beta1,
                           float beta2, StepRecord *rec, cudaStream_t stream);
 

@@ -61,6 +61,9 @@ class ZeroPlan:
     def stats(self, stream=None):
         return A.zero_partition_stats(self.handle, stream)
 
+    def set_global_stats(self, global_sumsq, global_overflow):
+        A.zero_step_set_global_stats(self.handle, global_sumsq, global_overflow)
+
     def adam(self, rank, grad, master, m, v, param_out, lr, beta1, beta2, eps, wd, adamw,
              loss_scale, clip, remote_sumsq=0.0, remote_overflow=0, stream=None):
         A.zero_adam_step(self.handle, rank, grad, master, m, v, param_out, lr, beta1, beta2,

@@ -221,6 +221,41 @@ zero_status zero_gather_layer(zero_plan *plan, int32_t unit,
                               void *stream);
 
 /* ----------------------------------------------------------------------
+ * Allocation-free reduce.  The paper has no counterpart: this is a service
+ * for callers that cannot allocate device memory -- e.g. code whose device
+ * memory is entirely owned by a framework's caching allocator (an extra
+ * cudaMalloc would fail or fragment that pool), or a latency-critical loop
+ * that must not pay cudaMalloc's implicit synchronisation.
+ *
+ * Computes exactly what zero_reduce_partition computes for one partition in
+ * one bucket (same kernel, same bits): grad_out[i] = (sum over j of
+ * grad_slices[j][i]) * float(1/(loss_scale*n_ranks)) for i < len, plus
+ * *sumsq_out (device double) = the partition's sum of grad_out^2 and
+ * *overflow_out (device int32) = 1 if any sum is not finite, else 0.
+ * No plan is involved and no step state is touched.
+ *
+ * Scratch: one fixed array of ZERO_NOALLOC_SCRATCH_BYTES in device memory
+ * that belongs to the library image (present on every GPU that loads the
+ * library until the process exits); no cudaMalloc/cudaFree or other
+ * allocating call is made.  len is limited to ZERO_NOALLOC_MAX_ELEMS (a
+ * multiple of 8); larger len returns ZERO_EINVAL.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ * All calls share the array and it keeps the last call's contents (the
+ * overflow word is cleared by every call); calls whose device work overlaps
+ * in time (other streams or host threads) race on it and must be serialised
+ * by the caller.  Inputs and outputs are caller-owned device memory, as for
+ * every other call.  Asynchronous on `stream`.
+ */
+#define ZERO_NOALLOC_MAX_ELEMS (8192LL * 32768LL)
+#define ZERO_NOALLOC_SCRATCH_BYTES (8192 * 8 + 256)
+zero_status zero_reduce_partition_noalloc(int32_t n_ranks, zero_lp lp,
+                                          const void *const *grad_slices,
+                                          int64_t len, float loss_scale,
+                                          float *grad_out, double *sumsq_out,
+                                          int32_t *overflow_out, void *stream);
+
+/* ----------------------------------------------------------------------
  * Accounting ("10.6 ZeRO 与 FSDP" Table 10-2; "第13篇 · ZeRO" §3.2, §3.4).
  * formula_bytes: per-GPU model-state bytes from the closed forms
  *   [0] DDP 16Ψ, [1] stage 1 4Ψ+12Ψ/N, [2] stage 2 2Ψ+14Ψ/N, [3] stage 3 16Ψ/N

@@ -39,6 +39,7 @@ SIGNATURES = {
     "zero_step_result": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "zero_plan_check": (_i32, [_vp]),
     "zero_gather_layer": (_i32, [_vp, _i32, _vp, _vp, _vp]),
+    "zero_reduce_partition_noalloc": (_i32, [_i32, _i32, _vp, _i64, _f32, _vp, _vp, _vp, _vp]),
     "zero_memory_report": (_i32, [_i64, _i32, _i32, _vp, _vp, _vp]),
     "zero_plan_destroy": (None, [_vp]),
     "zero_last_error": (C.c_char_p, []),
@@ -208,6 +209,21 @@ def zero_plan_check(plan: int):
 def zero_gather_layer(plan: int, unit: int, shards: Sequence, out, stream=None):
     _check(load().zero_gather_layer(plan, unit, C.cast(_ptr_array(shards), _vp), _ptr(out),
                                     _stream(stream)), "zero_gather_layer")
+
+
+ZERO_NOALLOC_MAX_ELEMS = 8192 * 32768
+
+
+def zero_reduce_partition_noalloc(n_ranks: int, lp: int, grad_slices: Sequence, length: int,
+                                  loss_scale: float, grad_out, sumsq_out, overflow_out,
+                                  stream=None):
+    """Allocation-free reduce of one partition (see include/zero.h): for callers
+    that cannot allocate device memory.  sumsq_out: device float64[1];
+    overflow_out: device int32[1]."""
+    _check(load().zero_reduce_partition_noalloc(n_ranks, lp, C.cast(_ptr_array(grad_slices), _vp),
+                                                length, loss_scale, _ptr(grad_out),
+                                                _ptr(sumsq_out), _ptr(overflow_out),
+                                                _stream(stream)), "zero_reduce_partition_noalloc")
 
 
 def zero_memory_report(psi: int, n_ranks: int, align: int = 1):

@@ -43,6 +43,10 @@ constexpr int64_t kDefaultSpinLimit = int64_t(1) << 21;
 
 }  // namespace
 
+namespace zk {
+void set_last_error(const char *msg) { g_last_error = msg ? msg : ""; }
+}  // namespace zk
+
 struct zero_plan {
     // layout
     int64_t psi = 0, psi_p = 0, part = 0;

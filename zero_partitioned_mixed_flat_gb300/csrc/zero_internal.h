@@ -29,6 +29,9 @@ struct StepRecord {
 
 int sm_count();
 
+// message for zero_last_error() on the calling thread
+void set_last_error(const char *msg);
+
 cudaError_t launch_reduce(const void *const *slices, int n, int lp,
                           int64_t offset, int64_t len, float inv, float *g,
                           double *partials, unsigned *overflow,

@@ -20,6 +20,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 namespace zk {
@@ -246,6 +248,95 @@ norm_finalize_decide(const __grid_constant__ DecideParams p) {
     rec->bc2 = __double2float_rn(__dsub_rn(1.0, pow((double)p.beta2, (double)t)));
 }
 
+// ------------------------------------------------- TMA / mbarrier primitives
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// bounded wait: at most `polls` try_wait polls (0: give up at once)
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long polls) {
+    for (long long i = 0; i < polls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_addr(src_smem)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// make this thread's generic-proxy shared-memory writes visible to later
+// bulk (async-proxy) reads of the same bytes
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// named barrier over `count` threads that also ORs a predicate across them
+__device__ __forceinline__ bool named_barrier_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void named_barrier(int id, int count) {
+    asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // -------------------------------------------------------------------- K3 adam
 
 struct AdamParams {
@@ -326,66 +417,172 @@ adam_fused_cast(const __grid_constant__ AdamParams p) {
     }
 }
 
+// K3 (pipelined): the same per-element arithmetic, with the memory traffic
+// moved onto the TMA engine.  Warp 0 (one thread) streams 2048-element tiles of
+// g, master, m, v into 4 shared-memory stages with cp.async.bulk (completion on
+// an mbarrier per stage); 16 consumer warps update 4 elements per thread,
+// release the input stage (empty mbarrier), write master/m/v/param into one of
+// 2 output stages, and one consumer thread stores them back with bulk copies.
+// Every mbarrier wait is bounded; a wait that gives up makes all consumers
+// leave together (the barrier vote), sets the error word, and the producer
+// drains the loads it issued before the CTA exits.
+constexpr int kAdamTile = 2048;
+constexpr int kAdamInStages = 4;
+constexpr int kAdamOutStages = 2;
+constexpr int kAdamConsumerWarps = 16;
+constexpr int kAdamConsumers = kAdamConsumerWarps * 32;
+constexpr int kAdamTmaThreads = kAdamConsumers + 32;
+constexpr size_t kAdamInStageBytes = 4 * kAdamTile * sizeof(float);
+constexpr size_t kAdamOutStageBytes = 3 * kAdamTile * sizeof(float) + kAdamTile * 2;
+constexpr size_t kAdamTmaSmem = kAdamInStages * kAdamInStageBytes + kAdamOutStages * kAdamOutStageBytes;
+constexpr long long kPipePolls = 1ll << 22;
+static_assert(kAdamTile == kAdamConsumers * 4, "4 elements per consumer thread");
+
+struct AdamTmaParams {
+    const float *g;
+    float *master, *m, *v;
+    uint16_t *param;  // NULL: no cast
+    const StepRecord *rec;
+    int *error;
+    long long len;  // multiple of 8
+    float lr, beta1, beta2, omb1, omb2, eps, wd, decay;
+    int adamw;
+};
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kAdamTmaThreads, 1)
+adam_fused_cast_tma(const __grid_constant__ AdamTmaParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[kAdamInStages];
+    __shared__ __align__(8) uint64_t empty[kAdamInStages];
+    const StepRecord *rec = p.rec;
+    if (rec->skip) return;
+    const long long n_tiles = (p.len + kAdamTile - 1) / kAdamTile;
+    if ((long long)blockIdx.x >= n_tiles) return;
+    const long long count = (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    unsigned char *in_base = smem;
+    unsigned char *out_base = smem + kAdamInStages * kAdamInStageBytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kAdamInStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kAdamConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {  // ---------------------------------------------- producer
+        if (lane != 0) return;
+        long long k = 0;
+        bool ok = true;
+        for (; k < count; ++k) {
+            const int s = (int)(k % kAdamInStages);
+            if (k >= kAdamInStages &&
+                !mbar_wait_bounded(&empty[s], (uint32_t)(((k / kAdamInStages) - 1) & 1), kPipePolls)) {
+                ok = false;
+                break;
+            }
+            const long long e0 = (blockIdx.x + k * gridDim.x) * (long long)kAdamTile;
+            const long long n = p.len - e0 < kAdamTile ? p.len - e0 : kAdamTile;
+            const uint32_t bytes = (uint32_t)(n * sizeof(float));
+            unsigned char *dst = in_base + (size_t)s * kAdamInStageBytes;
+            mbar_expect_tx(&full[s], 4 * bytes);
+            bulk_load(dst, p.g + e0, bytes, &full[s]);
+            bulk_load(dst + 1 * kAdamTile * sizeof(float), p.master + e0, bytes, &full[s]);
+            bulk_load(dst + 2 * kAdamTile * sizeof(float), p.m + e0, bytes, &full[s]);
+            bulk_load(dst + 3 * kAdamTile * sizeof(float), p.v + e0, bytes, &full[s]);
+        }
+        if (!ok) {
+            atomicExch(p.error, 1);
+            const long long first = k > kAdamInStages ? k - kAdamInStages : 0;
+            for (long long kk = first; kk < k; ++kk)
+                mbar_wait_bounded(&full[kk % kAdamInStages], (uint32_t)((kk / kAdamInStages) & 1),
+                                  kDrainPolls);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------- consumers
+    const int ct = threadIdx.x - 32;  // 0 .. kAdamConsumers-1
+    AdamScalars c;
+    c.coef = rec->coef;
+    c.bc1 = rec->bc1;
+    c.bc2 = rec->bc2;
+    c.lr = p.lr;
+    c.beta1 = p.beta1;
+    c.beta2 = p.beta2;
+    c.omb1 = p.omb1;
+    c.omb2 = p.omb2;
+    c.eps = p.eps;
+    c.wd = p.wd;
+    c.decay = p.decay;
+    c.adamw = p.adamw;
+    bool ok = true;
+    for (long long k = 0; k < count; ++k) {
+        const int s = (int)(k % kAdamInStages);
+        const int so = (int)(k % kAdamOutStages);
+        const long long e0 = (blockIdx.x + k * gridDim.x) * (long long)kAdamTile;
+        const int n = (int)(p.len - e0 < kAdamTile ? p.len - e0 : kAdamTile);
+        const bool got = mbar_wait_bounded(&full[s], (uint32_t)((k / kAdamInStages) & 1), kPipePolls);
+        const bool mine = got && ct * 4 < n;
+        float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f), w4 = g4, m4 = g4, v4 = g4;
+        if (mine) {
+            const float4 *in = reinterpret_cast<const float4 *>(in_base + (size_t)s * kAdamInStageBytes);
+            g4 = in[ct];
+            w4 = in[kAdamTile / 4 + ct];
+            m4 = in[2 * (kAdamTile / 4) + ct];
+            v4 = in[3 * (kAdamTile / 4) + ct];
+        }
+        __syncwarp();
+        if (got && lane == 0) mbar_arrive(&empty[s]);
+        if (mine) {
+            adam1(c, g4.x, w4.x, m4.x, v4.x);
+            adam1(c, g4.y, w4.y, m4.y, v4.y);
+            adam1(c, g4.z, w4.z, m4.z, v4.z);
+            adam1(c, g4.w, w4.w, m4.w, v4.w);
+        }
+        // the store issued kAdamOutStages tiles ago must have read stage `so`
+        if (ct == 0) bulk_wait_read<kAdamOutStages - 1>();
+        if (named_barrier_or(1, kAdamConsumers, !got)) {
+            ok = false;
+            break;
+        }
+        unsigned char *ob = out_base + (size_t)so * kAdamOutStageBytes;
+        if (mine) {
+            float4 *o = reinterpret_cast<float4 *>(ob);
+            o[ct] = w4;
+            o[kAdamTile / 4 + ct] = m4;
+            o[2 * (kAdamTile / 4) + ct] = v4;
+            uint2 q;
+            q.x = pack2<BF16>(w4.x, w4.y);
+            q.y = pack2<BF16>(w4.z, w4.w);
+            reinterpret_cast<uint2 *>(ob + 3 * kAdamTile * sizeof(float))[ct] = q;
+        }
+        fence_proxy_async_smem();
+        named_barrier(1, kAdamConsumers);
+        if (ct == 0) {
+            const uint32_t bytes = (uint32_t)(n * sizeof(float));
+            bulk_store(p.master + e0, ob, bytes);
+            bulk_store(p.m + e0, ob + kAdamTile * sizeof(float), bytes);
+            bulk_store(p.v + e0, ob + 2 * kAdamTile * sizeof(float), bytes);
+            if (p.param) bulk_store(p.param + e0, ob + 3 * kAdamTile * sizeof(float), (uint32_t)(n * 2));
+            bulk_commit();
+        }
+    }
+    if (ct == 0) {
+        bulk_wait_all();
+        if (!ok) atomicExch(p.error, 1);
+    }
+}
+
 // ------------------------------------------------------------------ K4 gather
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// bounded wait: at most `polls` try_wait polls (0: give up at once)
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long polls) {
-    for (long long i = 0; i < polls; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes,
-                                          uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst_smem)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                 "r"(smem_addr(src_smem)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-__device__ __forceinline__ void bulk_wait_read1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 
 template <int MAXN>
 struct GatherParams {
@@ -508,6 +705,27 @@ cudaError_t reduce_impl(const void *const *slices, int n, int64_t offset, int64_
 }
 
 template <bool BF16>
+cudaError_t adam_tma_impl(const AdamTmaParams &p, cudaStream_t stream) {
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        adam_fused_cast_tma<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAdamTmaSmem);
+    if (attr != cudaSuccess) return attr;
+    const long long tiles = (p.len + kAdamTile - 1) / kAdamTile;
+    long long grid = sm_count();
+    if (grid > tiles) grid = tiles;
+    if (grid < 1) return cudaSuccess;
+    adam_fused_cast_tma<BF16><<<(unsigned)grid, kAdamTmaThreads, kAdamTmaSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+bool use_simt_adam() {
+    static const bool simt = [] {
+        const char *e = std::getenv("ZERO_ADAM_KERNEL");
+        return e && std::strcmp(e, "simt") == 0;
+    }();
+    return simt;
+}
+
+template <bool BF16>
 cudaError_t adam_impl(const AdamParams &p, cudaStream_t stream) {
     static const int occ = occupancy(adam_fused_cast<BF16>, kAdamThreads, 0);
     long long grid = (long long)sm_count() * occ;
@@ -590,9 +808,9 @@ cudaError_t launch_decide(const double *partials, int64_t tiles_per_slot, const 
 }
 
 cudaError_t launch_adam(const float *g, float *master, float *m, float *v, void *param, int lp,
-                        int64_t len, const StepRecord *rec, float lr, float beta1, float beta2,
-                        float omb1, float omb2, float eps, float wd, float decay, int adamw,
-                        cudaStream_t stream) {
+                        int64_t len, const StepRecord *rec, int *error, float lr, float beta1,
+                        float beta2, float omb1, float omb2, float eps, float wd, float decay,
+                        int adamw, cudaStream_t stream) {
     AdamParams p;
     p.g = reinterpret_cast<const float4 *>(g);
     p.master = reinterpret_cast<float4 *>(master);
@@ -610,7 +828,26 @@ cudaError_t launch_adam(const float *g, float *master, float *m, float *v, void 
     p.wd = wd;
     p.decay = decay;
     p.adamw = adamw;
-    return lp ? adam_impl<true>(p, stream) : adam_impl<false>(p, stream);
+    if (use_simt_adam() || !error) return lp ? adam_impl<true>(p, stream) : adam_impl<false>(p, stream);
+    AdamTmaParams q;
+    q.g = g;
+    q.master = master;
+    q.m = m;
+    q.v = v;
+    q.param = static_cast<uint16_t *>(param);
+    q.rec = rec;
+    q.error = error;
+    q.len = len;
+    q.lr = lr;
+    q.beta1 = beta1;
+    q.beta2 = beta2;
+    q.omb1 = omb1;
+    q.omb2 = omb2;
+    q.eps = eps;
+    q.wd = wd;
+    q.decay = decay;
+    q.adamw = adamw;
+    return lp ? adam_tma_impl<true>(q, stream) : adam_tma_impl<false>(q, stream);
 }
 
 cudaError_t launch_gather(const void *const *shards, int n, int64_t src_offset_bytes,

@@ -406,8 +406,9 @@ zero_status zero_adam_step(zero_plan *p, int32_t rank, const float *grad, float 
         const int64_t off = (p->stage == 3) ? 0 : int64_t(rank) * p->part;
         param = static_cast<uint16_t *>(param_out) + off;
     }
-    cudaError_t e = zk::launch_adam(grad, master, m, v, param, p->lp, p->part, p->d_rec, lr, beta1,
-                                    beta2, omb1, omb2, eps, wd, decay, adamw ? 1 : 0, s);
+    cudaError_t e = zk::launch_adam(grad, master, m, v, param, p->lp, p->part, p->d_rec,
+                                    &p->d_rec->error, lr, beta1, beta2, omb1, omb2, eps, wd, decay,
+                                    adamw ? 1 : 0, s);
     if (e != cudaSuccess) return cuda_fail(e, "adam kernel launch");
     return ZERO_OK;
 }

@@ -46,7 +46,7 @@ cudaError_t launch_decide(const double *partials, int64_t tiles_per_slot,
 
 cudaError_t launch_adam(const float *g, float *master, float *m, float *v,
                         void *param, int lp, int64_t len,
-                        const StepRecord *rec, float lr, float beta1,
+                        const StepRecord *rec, int *error, float lr, float beta1,
                         float beta2, float omb1, float omb2, float eps,
                         float wd, float decay, int adamw, cudaStream_t stream);
 

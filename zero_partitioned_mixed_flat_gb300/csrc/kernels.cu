@@ -7,7 +7,8 @@
 // K2 norm_finalize_decide  global norm, clip coefficient, skip and loss-scale
 //                          decision, step counter ("年糕切片" §4.2-§4.3).
 // K3 adam_fused_cast       Adam/AdamW on fp32 master/m/v + lp cast into the
-//                          all-gather destination (§10.6.2 Steps 3-4).
+//                          all-gather destination (§10.6.2 Steps 3-4); a
+//                          warp-specialised TMA bulk-copy pipeline.
 // K4 gather_layer_tma      stage-3 per-layer all-gather of N shards
 //                          (§10.6.4 step 1), TMA bulk copies through shared
 //                          memory with bounded mbarrier waits.
@@ -20,8 +21,6 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include <cstdlib>
-#include <cstring>
 #include <mutex>
 
 namespace zk {
@@ -31,7 +30,6 @@ constexpr int kReduceThreads = 256;
 constexpr int kVec = 8;  // lp elements per 16-byte vector
 constexpr int kTileIters = int(kTile / (kReduceThreads * kVec));
 constexpr int kBatch = 16;  // slices loaded before they are added
-constexpr int kAdamThreads = 256;
 constexpr int kGatherStages = 6;
 constexpr unsigned kGatherChunk = 32768;  // bytes per bulk copy
 constexpr long long kDrainPolls = 1ll << 21;
@@ -47,17 +45,7 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     return r;
 }
 
-__device__ __forceinline__ float4 ld_stream_f4(const float4 *p) {
-    float4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
-                 : "l"(p));
-    return r;
-}
-
 __device__ __forceinline__ void st_stream_f4(float4 *p, float4 v) { __stcs(p, v); }
-
-__device__ __forceinline__ void st_stream_u4(uint4 *p, uint4 v) { __stcs(p, v); }
 
 // 8 lp values -> 8 floats (exact conversions)
 template <bool BF16>
@@ -339,16 +327,6 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 
 // -------------------------------------------------------------------- K3 adam
 
-struct AdamParams {
-    const float4 *g;
-    float4 *master, *m, *v;
-    uint4 *param;  // 8 lp per uint4; NULL: no cast
-    const StepRecord *rec;
-    long long n_vec;  // len / 8
-    float lr, beta1, beta2, omb1, omb2, eps, wd, decay;
-    int adamw;
-};
-
 struct AdamScalars {
     float coef, bc1, bc2, lr, beta1, beta2, omb1, omb2, eps, wd, decay;
     int adamw;
@@ -368,57 +346,7 @@ __device__ __forceinline__ void adam1(const AdamScalars &c, float g, float &w, f
     w = __fsub_rn(w, upd);
 }
 
-template <bool BF16>
-__global__ void __launch_bounds__(kAdamThreads)
-adam_fused_cast(const __grid_constant__ AdamParams p) {
-    const StepRecord *rec = p.rec;
-    if (rec->skip) return;
-    AdamScalars c;
-    c.coef = rec->coef;
-    c.bc1 = rec->bc1;
-    c.bc2 = rec->bc2;
-    c.lr = p.lr;
-    c.beta1 = p.beta1;
-    c.beta2 = p.beta2;
-    c.omb1 = p.omb1;
-    c.omb2 = p.omb2;
-    c.eps = p.eps;
-    c.wd = p.wd;
-    c.decay = p.decay;
-    c.adamw = p.adamw;
-    const long long stride = (long long)gridDim.x * kAdamThreads;
-    for (long long i = (long long)blockIdx.x * kAdamThreads + threadIdx.x; i < p.n_vec; i += stride) {
-        float4 g0 = ld_stream_f4(p.g + 2 * i), g1 = ld_stream_f4(p.g + 2 * i + 1);
-        float4 w0 = ld_stream_f4(p.master + 2 * i), w1 = ld_stream_f4(p.master + 2 * i + 1);
-        float4 m0 = ld_stream_f4(p.m + 2 * i), m1 = ld_stream_f4(p.m + 2 * i + 1);
-        float4 v0 = ld_stream_f4(p.v + 2 * i), v1 = ld_stream_f4(p.v + 2 * i + 1);
-        adam1(c, g0.x, w0.x, m0.x, v0.x);
-        adam1(c, g0.y, w0.y, m0.y, v0.y);
-        adam1(c, g0.z, w0.z, m0.z, v0.z);
-        adam1(c, g0.w, w0.w, m0.w, v0.w);
-        adam1(c, g1.x, w1.x, m1.x, v1.x);
-        adam1(c, g1.y, w1.y, m1.y, v1.y);
-        adam1(c, g1.z, w1.z, m1.z, v1.z);
-        adam1(c, g1.w, w1.w, m1.w, v1.w);
-        st_stream_f4(p.master + 2 * i, w0);
-        st_stream_f4(p.master + 2 * i + 1, w1);
-        st_stream_f4(p.m + 2 * i, m0);
-        st_stream_f4(p.m + 2 * i + 1, m1);
-        st_stream_f4(p.v + 2 * i, v0);
-        st_stream_f4(p.v + 2 * i + 1, v1);
-        if (p.param) {
-            uint4 q;
-            q.x = pack2<BF16>(w0.x, w0.y);
-            q.y = pack2<BF16>(w0.z, w0.w);
-            q.z = pack2<BF16>(w1.x, w1.y);
-            q.w = pack2<BF16>(w1.z, w1.w);
-            st_stream_u4(p.param + i, q);
-        }
-    }
-}
-
-// K3 (pipelined): the same per-element arithmetic, with the memory traffic
-// moved onto the TMA engine.  Warp 0 (one thread) streams 2048-element tiles of
+// K3: Adam/AdamW + cast with the memory traffic on the TMA engine.  Warp 0 (one thread) streams 2048-element tiles of
 // g, master, m, v into 4 shared-memory stages with cp.async.bulk (completion on
 // an mbarrier per stage); 16 consumer warps update 4 elements per thread,
 // release the input stage (empty mbarrier), write master/m/v/param into one of
@@ -456,7 +384,7 @@ __device__ __forceinline__ void bulk_wait_read() {
 
 template <bool BF16>
 __global__ void __launch_bounds__(kAdamTmaThreads, 1)
-adam_fused_cast_tma(const __grid_constant__ AdamTmaParams p) {
+adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[kAdamInStages];
     __shared__ __align__(8) uint64_t empty[kAdamInStages];
@@ -707,32 +635,13 @@ cudaError_t reduce_impl(const void *const *slices, int n, int64_t offset, int64_
 template <bool BF16>
 cudaError_t adam_tma_impl(const AdamTmaParams &p, cudaStream_t stream) {
     static const cudaError_t attr = cudaFuncSetAttribute(
-        adam_fused_cast_tma<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAdamTmaSmem);
+        adam_fused_cast<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAdamTmaSmem);
     if (attr != cudaSuccess) return attr;
     const long long tiles = (p.len + kAdamTile - 1) / kAdamTile;
     long long grid = sm_count();
     if (grid > tiles) grid = tiles;
     if (grid < 1) return cudaSuccess;
-    adam_fused_cast_tma<BF16><<<(unsigned)grid, kAdamTmaThreads, kAdamTmaSmem, stream>>>(p);
-    return cudaGetLastError();
-}
-
-bool use_simt_adam() {
-    static const bool simt = [] {
-        const char *e = std::getenv("ZERO_ADAM_KERNEL");
-        return e && std::strcmp(e, "simt") == 0;
-    }();
-    return simt;
-}
-
-template <bool BF16>
-cudaError_t adam_impl(const AdamParams &p, cudaStream_t stream) {
-    static const int occ = occupancy(adam_fused_cast<BF16>, kAdamThreads, 0);
-    long long grid = (long long)sm_count() * occ;
-    const long long need = (p.n_vec + kAdamThreads - 1) / kAdamThreads;
-    if (grid > need) grid = need;
-    if (grid < 1) return cudaSuccess;
-    adam_fused_cast<BF16><<<(unsigned)grid, kAdamThreads, 0, stream>>>(p);
+    adam_fused_cast<BF16><<<(unsigned)grid, kAdamTmaThreads, kAdamTmaSmem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -811,24 +720,6 @@ cudaError_t launch_adam(const float *g, float *master, float *m, float *v, void 
                         int64_t len, const StepRecord *rec, int *error, float lr, float beta1,
                         float beta2, float omb1, float omb2, float eps, float wd, float decay,
                         int adamw, cudaStream_t stream) {
-    AdamParams p;
-    p.g = reinterpret_cast<const float4 *>(g);
-    p.master = reinterpret_cast<float4 *>(master);
-    p.m = reinterpret_cast<float4 *>(m);
-    p.v = reinterpret_cast<float4 *>(v);
-    p.param = reinterpret_cast<uint4 *>(param);
-    p.rec = rec;
-    p.n_vec = len / 8;
-    p.lr = lr;
-    p.beta1 = beta1;
-    p.beta2 = beta2;
-    p.omb1 = omb1;
-    p.omb2 = omb2;
-    p.eps = eps;
-    p.wd = wd;
-    p.decay = decay;
-    p.adamw = adamw;
-    if (use_simt_adam() || !error) return lp ? adam_impl<true>(p, stream) : adam_impl<false>(p, stream);
     AdamTmaParams q;
     q.g = g;
     q.master = master;

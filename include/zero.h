@@ -115,6 +115,15 @@ zero_status zero_plan_fragments(const zero_plan *plan, int32_t rank,
  * are still skipped).  Default 1000.  Host only. */
 zero_status zero_plan_set_loss_scaler(zero_plan *plan, int32_t growth_interval);
 
+/* Reduce precision ("10.6 ZeRO 与 FSDP" §10.6.7: MixedPrecision with
+ * reduce_dtype=float16, gradients communicated and summed in fp16).
+ * accumulate_in_lp = 0 (default): the N slices are summed in float.
+ * accumulate_in_lp = 1: every partial sum is rounded to the plan's lp type
+ * (nearest, ties to even) before the next rank's value is added, in rank
+ * order; the final lp sum is then widened, unscaled and checked as usual
+ * (an lp overflow shows up as an overflow).  Host only. */
+zero_status zero_plan_set_reduce_precision(zero_plan *plan, int32_t accumulate_in_lp);
+
 /* Resume: set the device step counter t and the good-step count (e.g. from a
  * checkpoint).  Synchronises the device. */
 zero_status zero_plan_set_state(zero_plan *plan, int64_t step,

@@ -56,6 +56,8 @@ def lib():
         L.orc_memory.restype = _i32
         L.orc_reduce.argtypes = [_i32, _vp, _i32, _i64, _f32, _vp, _vp, _vp]
         L.orc_reduce.restype = None
+        L.orc_reduce_lp_accum.argtypes = [_i32, _vp, _i32, _i64, _f32, _vp, _vp, _vp]
+        L.orc_reduce_lp_accum.restype = None
         L.orc_decide.argtypes = [_f64, _f64, _i32, _i32, _f32, _f32, _i64, _i32,
                                  _i32, _f32, _f32, C.POINTER(Decision)]
         L.orc_decide.restype = None
@@ -164,6 +166,19 @@ def reduce(slices, lp, loss_scale, sumsq=0.0, overflow=0, out=None):
     return g, acc.value, of.value
 
 
+def reduce_lp_accum(slices, lp, loss_scale, sumsq=0.0, overflow=0, out=None):
+    """Like reduce(), with every partial sum rounded to the lp type."""
+    slices = [_c(s, np.uint16) for s in slices]
+    n = len(slices)
+    length = slices[0].size
+    g = np.empty(length, np.float32) if out is None else out
+    acc = _f64(sumsq)
+    of = _i32(overflow)
+    lib().orc_reduce_lp_accum(n, C.cast(_ptr_array(slices), _vp), lp, length, loss_scale,
+                              _ptr(g), C.byref(acc), C.byref(of))
+    return g, acc.value, of.value
+
+
 def decide(sumsq, overflow, clip, loss_scale, step, good_steps=0, growth_interval=1000,
            beta1=0.9, beta2=0.999, remote_sumsq=0.0, remote_overflow=0):
     d = Decision()
@@ -195,5 +210,5 @@ def gather(shards):
 
 LIB_PATH = _build.LIB
 __all__ = ["lib", "lp_to_float", "float_to_lp", "layout", "partition_to_flat",
-           "fragments", "memory", "reduce", "decide", "adam", "gather", "LIB_PATH",
+           "fragments", "memory", "reduce", "reduce_lp_accum", "decide", "adam", "gather", "LIB_PATH",
            "Decision"]

@@ -349,6 +349,36 @@ void orc_reduce(int32_t n, const uint16_t *const *slices, int32_t lp,
     *overflow = of;
 }
 
+/* The low-precision accumulation: the exact sum of the running lp value and
+ * the next rank's lp value, rounded to the lp type.  The float addition is
+ * that exact sum rounded to 24 bits; a second rounding to 11 (fp16) or 8
+ * (bf16) bits then equals one direct rounding, because 24 >= 2p + 2
+ * (Figueroa, "When is double rounding innocuous?", 1995). */
+void orc_reduce_lp_accum(int32_t n, const uint16_t *const *slices, int32_t lp,
+                         int64_t len, float loss_scale, float *g, double *sumsq,
+                         int32_t *overflow)
+{
+    const float inv = (float)(1.0 / ((double)loss_scale * (double)n));
+    double acc = *sumsq;
+    int32_t of = *overflow;
+    for (int64_t i = 0; i < len; ++i) {
+        uint16_t run = slices[0][i];
+        float s, gi, sq;
+        for (int32_t j = 1; j < n; ++j)
+            run = orc_float_to_lp(orc_lp_to_float(run, lp) +
+                                      orc_lp_to_float(slices[j][i], lp), lp);
+        s = orc_lp_to_float(run, lp);
+        if (!isfinite(s))
+            of = 1;
+        gi = s * inv;
+        g[i] = gi;
+        sq = gi * gi;
+        acc = acc + (double)sq;
+    }
+    *sumsq = acc;
+    *overflow = of;
+}
+
 /* ------------------------------------------------------------------------
  * Decision.  [P2] §4.2: "gradient_clipping": 1.0 -- clip by the global L2
  * norm of the (unscaled, averaged) gradient, coef = clip / (norm + 1e-6)

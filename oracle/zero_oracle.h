@@ -93,6 +93,15 @@ void orc_reduce(int32_t n, const uint16_t *const *slices, int32_t lp,
                 int64_t len, float loss_scale, float *g, double *sumsq,
                 int32_t *overflow);
 
+/* Same, with the sum kept in the low-precision type: each partial sum is
+ * rounded to fp16/bf16 (nearest, ties to even) before the next rank's value
+ * is added -- the reduce_dtype=float16 mixed-precision setting of "10.6 ZeRO
+ * 与 FSDP" §10.6.7.  Rank order 0..N-1; the final lp sum is widened to float,
+ * multiplied by float(1/(S*N)); overflow if that sum is not finite.        */
+void orc_reduce_lp_accum(int32_t n, const uint16_t *const *slices, int32_t lp,
+                         int64_t len, float loss_scale, float *g,
+                         double *sumsq, int32_t *overflow);
+
 /* ---- global-norm clip, skip and loss-scale decision -------------------
  * [P2] §4.2 "gradient_clipping": 1.0, §4.3 loss scaling.                  */
 typedef struct {

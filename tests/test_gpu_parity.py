@@ -25,17 +25,19 @@ def _plan(psi, n, lp, stage=1, align=8, sizes=None, units=None):
     return Z.ZeroPlan(psi if sizes is None else -1, n, sizes, align, stage, units, lp)
 
 
-def _reduce_case(zlib, n, part, lp, scale, bucket=0, rank=0, seed=0):
+def _reduce_case(zlib, n, part, lp, scale, bucket=0, rank=0, seed=0, acc_lp=False):
     psi = n * part
     plan = _plan(psi, n, lp)
     assert plan.part_len == part
+    if acc_lp:
+        plan.set_reduce_precision(1)
     dev = torch.device("cuda")
     slices = [synth.grad_slice(part, lp, 1.0, scale, seed, 1, j, rank, dev) for j in range(n)]
     g = torch.empty(part, dtype=torch.float32, device=dev)
     plan.reduce(rank, slices, g, scale, bucket)
     ss, of = plan.stats()
     host = [synth.to_numpy_codes(t) for t in slices]
-    og, oss, oof = oracle.reduce(host, lp, scale)
+    og, oss, oof = (oracle.reduce_lp_accum if acc_lp else oracle.reduce)(host, lp, scale)
     assert same_floats(g.cpu().numpy(), og)
     assert of == oof
     assert abs(ss - oss) <= 1e-6 * oss
@@ -48,6 +50,13 @@ def _reduce_case(zlib, n, part, lp, scale, bucket=0, rank=0, seed=0):
 def test_reduce_ragged_and_wide(zlib, n, lp):
     # 3 whole norm tiles plus a ragged tail of 136 elements
     _reduce_case(zlib, n, 3 * TILE + 136, lp, 1024.0 if lp == 0 else 1.0)
+
+
+@pytest.mark.parametrize("n", [2, 3, 16, 64, 65])
+@pytest.mark.parametrize("lp", [0, 1])
+def test_reduce_in_lp_dtype(zlib, n, lp):
+    # sums rounded to fp16/bf16 at every rank (reduce_dtype=float16)
+    _reduce_case(zlib, n, 2 * TILE + 72, lp, 64.0 if lp == 0 else 1.0, acc_lp=True)
 
 
 @pytest.mark.parametrize("part", [8, 64, 4096, TILE - 8, TILE, TILE + 8, 7 * TILE + 4000])
@@ -128,6 +137,8 @@ def test_ddp_replica_equals_sharded_step(zlib):
     dict(n_ranks=3, ranks=[0, 1, 2], sizes=[100_000, 7, 33_333]),  # odd N, ragged
     dict(n_ranks=1, ranks=[0]),                            # N = 1: plain mixed-precision Adam
     dict(bucket_elems=40_000),                             # several buckets
+    dict(reduce_lp_accum=True),                            # fp16 reduce dtype
+    dict(reduce_lp_accum=True, lp=1, loss_scale=1.0, grads_times_scale=False),
 ])
 def test_tiny_variants(zlib, kw):
     h = Harness(_tiny(**kw))

@@ -45,6 +45,8 @@ MUTANTS = {
     "memory_stage2_k": ("int_plus_ratio(2 * psi, 14 * psi, n_ranks)",
                         "int_plus_ratio(2 * psi, 12 * psi, n_ranks)"),
     "comm_stage3": ("comm[3] = 3 * psi;", "comm[3] = 2 * psi;"),
+    "lp_accum_not_rounded": ("run = orc_float_to_lp(orc_lp_to_float(run, lp) +\n                                      orc_lp_to_float(slices[j][i], lp), lp);",
+                             "run = orc_float_to_lp(orc_lp_to_float(run, lp), lp);"),
 }
 
 

@@ -321,6 +321,46 @@ def test_sumsq_matches_fsum_and_runs_on(orc):
     assert acc == ss
 
 
+def test_reduce_lp_accum_hand_cases(orc):
+    # fp16: 2048 + 1 = 2049 is a tie between 2048 and 2050 -> even (2048), twice
+    x = [_half([2048.0]), _half([1.0]), _half([1.0])]
+    third = np.float32(1.0 / 3.0)                   # g = s * float(1/(S*N))
+    g, _, of = orc.reduce_lp_accum(x, 0, 1.0)
+    assert g[0] == np.float32(2048.0) * third and of == 0
+    g, _, _ = orc.reduce(x, 0, 1.0)                 # float accumulation keeps both ones
+    assert g[0] == np.float32(2050.0) * third
+    # bf16: 256 + 1 ties to 256 the same way
+    b = [np.array([0x4380], np.uint16), np.array([0x3F80], np.uint16), np.array([0x3F80], np.uint16)]
+    g, _, _ = orc.reduce_lp_accum(b, 1, 1.0)
+    assert g[0] == np.float32(256.0) * third
+    # fp16: 65504 + 16 = 65520 rounds up to 65536, which overflows to inf
+    o = [_half([65504.0]), _half([16.0])]
+    assert orc.reduce_lp_accum(o, 0, 1.0)[2] == 1
+    assert orc.reduce(o, 0, 1.0)[2] == 0            # finite in float
+
+
+def test_reduce_lp_accum_matches_library_sequential_sums(orc):
+    rng = np.random.default_rng(12)
+    for n in (2, 3, 8, 17):
+        vals = rng.standard_normal((n, 20_000)) * 10.0 ** rng.integers(-6, 4, (n, 20_000))
+        h = vals.astype(np.float16)
+        with np.errstate(over="ignore"):
+            acc = h[0].copy()
+            for j in range(1, n):
+                acc = (acc + h[j]).astype(np.float16)   # numpy half add: rounded to half
+        g, _, _ = orc.reduce_lp_accum(list(h.view(np.uint16)), 0, 1.0)
+        ref = acc.astype(np.float32) * np.float32(1.0 / n)
+        fin = np.isfinite(ref)
+        assert np.array_equal(g[fin].view(U32), ref[fin].view(U32))
+        t = torch.from_numpy(vals.astype(np.float32)).to(torch.bfloat16)
+        acc = t[0].clone()
+        for j in range(1, n):
+            acc = acc + t[j]                            # torch bf16 add: rounded to bf16
+        g, _, _ = orc.reduce_lp_accum(list(t.view(torch.int16).numpy().view(np.uint16)), 1, 1.0)
+        ref = acc.float().numpy() * np.float32(1.0 / n)
+        assert np.array_equal(g.view(U32), ref.view(U32))
+
+
 # ----------------------------------------------------- decision (clip/scale)
 
 def test_clip_coefficient_closed_form(orc):

@@ -99,6 +99,9 @@ class Harness:
         self.bucket = w.bucket_elems if bucket is None else bucket
         self.plan = Z.ZeroPlan(-1, w.n_ranks, w.sizes, w.align, self.stage, w.unit_of_tensor,
                                w.lp, growth_interval=w.growth_interval)
+        if w.reduce_lp_accum:
+            self.plan.set_reduce_precision(1)
+        self.o_reduce = oracle.reduce_lp_accum if w.reduce_lp_accum else oracle.reduce
         self.lay = oracle.layout(w.sizes, w.n_ranks, w.align, self.stage, w.unit_of_tensor)
         assert self.plan.psi_padded == self.lay["psi_padded"]
         assert self.plan.part_len == self.lay["part_len"]
@@ -178,7 +181,7 @@ class Harness:
         idx = s.idx
 
         def work(c0, c1, host_slices, host_g):
-            g, ss, of = oracle.reduce(host_slices, w.lp, self.S)
+            g, ss, of = self.o_reduce(host_slices, w.lp, self.S)
             ok = same_floats(g, host_g)
             lo, hi = np.searchsorted(idx, [c0, c1])
             return ss, of, ok, g[idx[lo:hi] - c0]

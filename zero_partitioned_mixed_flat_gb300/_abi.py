@@ -31,6 +31,7 @@ SIGNATURES = {
     "zero_plan_set_loss_scaler": (_i32, [_vp, _i32]),
     "zero_plan_set_state": (_i32, [_vp, _i64, _i32]),
     "zero_plan_set_spin_limit": (_i32, [_vp, _i64]),
+    "zero_plan_set_reduce_precision": (_i32, [_vp, _i32]),
     "zero_reduce_partition": (_i32, [_vp, _i32, _vp, _vp, _f32, _i64, _vp]),
     "zero_partition_stats": (_i32, [_vp, _vp, _vp, _vp]),
     "zero_step_set_global_stats": (_i32, [_vp, _f64, _i32]),
@@ -151,6 +152,11 @@ def zero_plan_set_state(plan: int, step: int, good_steps: int = 0):
 
 def zero_plan_set_spin_limit(plan: int, polls: int):
     _check(load().zero_plan_set_spin_limit(plan, polls), "zero_plan_set_spin_limit")
+
+
+def zero_plan_set_reduce_precision(plan: int, accumulate_in_lp: int):
+    _check(load().zero_plan_set_reduce_precision(plan, int(accumulate_in_lp)),
+           "zero_plan_set_reduce_precision")
 
 
 def zero_plan_destroy(plan: int):

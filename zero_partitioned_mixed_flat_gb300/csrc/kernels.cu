@@ -30,7 +30,7 @@ constexpr int kReduceThreads = 256;
 constexpr int kVec = 8;  // lp elements per 16-byte vector
 constexpr int kTileIters = int(kTile / (kReduceThreads * kVec));
 constexpr int kBatch = 16;  // slices loaded before they are added
-constexpr int kGatherStages = 6;
+constexpr int kGatherStages = 3;
 constexpr unsigned kGatherChunk = 32768;  // bytes per bulk copy
 constexpr long long kDrainPolls = 1ll << 21;
 static_assert(kTile % (kReduceThreads * kVec) == 0, "tile must be whole iterations");
@@ -101,7 +101,25 @@ struct ReduceParams {
     int n;
 };
 
-template <int MAXN, bool BF16>
+// round a float to the lp type and back (nearest, ties to even)
+template <bool BF16>
+__device__ __forceinline__ void round_lp_pair(float &a, float &b) {
+    if constexpr (BF16) {
+        const float2 t = __bfloat1622float2(__floats2bfloat162_rn(a, b));
+        a = t.x;
+        b = t.y;
+    } else {
+        const float2 t = __half22float2(__floats2half2_rn(a, b));
+        a = t.x;
+        b = t.y;
+    }
+}
+
+// ACC_LP: every partial sum is rounded to the lp type before the next rank's
+// value is added (reduce in the low-precision dtype).  The float add of two lp
+// values followed by that rounding equals the correctly rounded lp sum (24
+// float bits >= 2p + 2, so the double rounding is innocuous).
+template <int MAXN, bool BF16, bool ACC_LP>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
     __shared__ double warp_sq[kReduceThreads / 32];
@@ -134,6 +152,10 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
                         unpack8<BF16>(q[b], x);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], x[k]);
+                        if constexpr (ACC_LP) {
+#pragma unroll
+                            for (int k = 0; k < 8; k += 2) round_lp_pair<BF16>(s[k], s[k + 1]);
+                        }
                     }
                 }
             }
@@ -346,24 +368,27 @@ __device__ __forceinline__ void adam1(const AdamScalars &c, float g, float &w, f
     w = __fsub_rn(w, upd);
 }
 
-// K3: Adam/AdamW + cast with the memory traffic on the TMA engine.  Warp 0 (one thread) streams 2048-element tiles of
-// g, master, m, v into 4 shared-memory stages with cp.async.bulk (completion on
-// an mbarrier per stage); 16 consumer warps update 4 elements per thread,
-// release the input stage (empty mbarrier), write master/m/v/param into one of
-// 2 output stages, and one consumer thread stores them back with bulk copies.
+// K3: Adam/AdamW + cast with the memory traffic on the TMA engine.  Warp 0
+// (one thread) streams 1024-element tiles of g, master, m, v into 4
+// shared-memory stages with cp.async.bulk (completion on an mbarrier per
+// stage); 8 consumer warps update 4 elements per thread, release the input
+// stage (empty mbarrier), write master/m/v/param into one of 2 output stages,
+// and one consumer thread stores them back with bulk copies.  Two such
+// pipelines (CTAs, 92 KB of shared memory each) run per SM.
 // Every mbarrier wait is bounded; a wait that gives up makes all consumers
 // leave together (the barrier vote), sets the error word, and the producer
 // drains the loads it issued before the CTA exits.
-constexpr int kAdamTile = 2048;
+constexpr int kAdamTile = 1024;
 constexpr int kAdamInStages = 4;
 constexpr int kAdamOutStages = 2;
-constexpr int kAdamConsumerWarps = 16;
+constexpr int kAdamConsumerWarps = 8;
 constexpr int kAdamConsumers = kAdamConsumerWarps * 32;
 constexpr int kAdamTmaThreads = kAdamConsumers + 32;
 constexpr size_t kAdamInStageBytes = 4 * kAdamTile * sizeof(float);
 constexpr size_t kAdamOutStageBytes = 3 * kAdamTile * sizeof(float) + kAdamTile * 2;
 constexpr size_t kAdamTmaSmem = kAdamInStages * kAdamInStageBytes + kAdamOutStages * kAdamOutStageBytes;
 constexpr long long kPipePolls = 1ll << 22;
+constexpr int kAdamCtasPerSm = 2;
 static_assert(kAdamTile == kAdamConsumers * 4, "4 elements per consumer thread");
 
 struct AdamTmaParams {
@@ -383,7 +408,7 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kAdamTmaThreads, 1)
+__global__ void __launch_bounds__(kAdamTmaThreads, kAdamCtasPerSm)
 adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[kAdamInStages];
@@ -610,7 +635,7 @@ int occupancy(K kernel, int threads, size_t smem) {
     return blocks < 1 ? 1 : blocks;
 }
 
-template <int MAXN, bool BF16>
+template <int MAXN, bool BF16, bool ACC_LP>
 cudaError_t reduce_impl(const void *const *slices, int n, int64_t offset, int64_t len, float inv,
                         float *g, double *partials, unsigned *overflow, cudaStream_t stream) {
     ReduceParams<MAXN> p;
@@ -623,12 +648,12 @@ cudaError_t reduce_impl(const void *const *slices, int n, int64_t offset, int64_
     p.len = len;
     p.inv = inv;
     p.n = n;
-    static const int occ = occupancy(reduce_unscale_stats<MAXN, BF16>, kReduceThreads, 0);
+    static const int occ = occupancy(reduce_unscale_stats<MAXN, BF16, ACC_LP>, kReduceThreads, 0);
     const long long tiles = (len + kTile - 1) / kTile;
     long long grid = (long long)sm_count() * occ;
     if (grid > tiles) grid = tiles;
     if (grid < 1) return cudaSuccess;
-    reduce_unscale_stats<MAXN, BF16><<<(unsigned)grid, kReduceThreads, 0, stream>>>(p);
+    reduce_unscale_stats<MAXN, BF16, ACC_LP><<<(unsigned)grid, kReduceThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -638,7 +663,8 @@ cudaError_t adam_tma_impl(const AdamTmaParams &p, cudaStream_t stream) {
         adam_fused_cast<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAdamTmaSmem);
     if (attr != cudaSuccess) return attr;
     const long long tiles = (p.len + kAdamTile - 1) / kAdamTile;
-    long long grid = sm_count();
+    static const int occ = occupancy(adam_fused_cast<BF16>, kAdamTmaThreads, kAdamTmaSmem);
+    long long grid = (long long)sm_count() * occ;
     if (grid > tiles) grid = tiles;
     if (grid < 1) return cudaSuccess;
     adam_fused_cast<BF16><<<(unsigned)grid, kAdamTmaThreads, kAdamTmaSmem, stream>>>(p);
@@ -663,7 +689,8 @@ cudaError_t gather_impl(const void *const *shards, int n, int64_t src_off, int64
     static const cudaError_t attr = cudaFuncSetAttribute(
         gather_layer_tma<MAXN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (attr != cudaSuccess) return attr;
-    long long grid = sm_count();
+    static const int occ = occupancy(gather_layer_tma<MAXN>, 32, smem);
+    long long grid = (long long)sm_count() * occ;
     if (grid > p.n_chunks) grid = p.n_chunks;
     gather_layer_tma<MAXN><<<(unsigned)grid, 32, smem, stream>>>(p);
     return cudaGetLastError();
@@ -683,14 +710,23 @@ int sm_count() {
     return g_dev[dev].sms;
 }
 
-cudaError_t launch_reduce(const void *const *slices, int n, int lp, int64_t offset, int64_t len,
-                          float inv, float *g, double *partials, unsigned *overflow,
+template <int MAXN>
+cudaError_t reduce_dispatch(const void *const *slices, int n, int lp, bool acc_lp, int64_t offset,
+                            int64_t len, float inv, float *g, double *partials, unsigned *overflow,
+                            cudaStream_t stream) {
+    if (lp)
+        return acc_lp ? reduce_impl<MAXN, true, true>(slices, n, offset, len, inv, g, partials, overflow, stream)
+                      : reduce_impl<MAXN, true, false>(slices, n, offset, len, inv, g, partials, overflow, stream);
+    return acc_lp ? reduce_impl<MAXN, false, true>(slices, n, offset, len, inv, g, partials, overflow, stream)
+                  : reduce_impl<MAXN, false, false>(slices, n, offset, len, inv, g, partials, overflow, stream);
+}
+
+cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp, int64_t offset,
+                          int64_t len, float inv, float *g, double *partials, unsigned *overflow,
                           cudaStream_t stream) {
     if (n <= 64)
-        return lp ? reduce_impl<64, true>(slices, n, offset, len, inv, g, partials, overflow, stream)
-                  : reduce_impl<64, false>(slices, n, offset, len, inv, g, partials, overflow, stream);
-    return lp ? reduce_impl<1024, true>(slices, n, offset, len, inv, g, partials, overflow, stream)
-              : reduce_impl<1024, false>(slices, n, offset, len, inv, g, partials, overflow, stream);
+        return reduce_dispatch<64>(slices, n, lp, acc_lp != 0, offset, len, inv, g, partials, overflow, stream);
+    return reduce_dispatch<1024>(slices, n, lp, acc_lp != 0, offset, len, inv, g, partials, overflow, stream);
 }
 
 cudaError_t launch_decide(const double *partials, int64_t tiles_per_slot, const uint64_t *active_mask,

@@ -64,6 +64,7 @@ struct zero_plan {
     Phase phase = kIdle;
     uint64_t active[ZERO_MAX_RANKS / 64] = {0};
     int32_t growth_interval = 1000;
+    int32_t reduce_lp_accum = 0;  // 1: partial sums rounded to the lp type
     int64_t spin_limit = kDefaultSpinLimit;
     bool use_global = false;  // zero_step_set_global_stats was called this step
     double global_sumsq = 0.0;
@@ -272,6 +273,13 @@ zero_status zero_plan_set_loss_scaler(zero_plan *p, int32_t growth_interval) {
     return ZERO_OK;
 }
 
+zero_status zero_plan_set_reduce_precision(zero_plan *p, int32_t accumulate_in_lp) {
+    if (!p || (accumulate_in_lp != 0 && accumulate_in_lp != 1))
+        return fail(ZERO_EINVAL, "plan is NULL or accumulate_in_lp is not 0/1");
+    p->reduce_lp_accum = accumulate_in_lp;
+    return ZERO_OK;
+}
+
 zero_status zero_plan_set_spin_limit(zero_plan *p, int64_t polls) {
     if (!p || polls < 0) return fail(ZERO_EINVAL, "plan is NULL or polls < 0");
     p->spin_limit = polls;
@@ -328,8 +336,8 @@ zero_status zero_reduce_partition(zero_plan *p, int32_t rank, const void *const 
     if (bucket <= 0) bucket = p->part;
     for (int64_t b0 = 0; b0 < p->part; b0 += bucket) {
         const int64_t len = std::min(bucket, p->part - b0);
-        cudaError_t e = zk::launch_reduce(grad_slices, p->n_ranks, p->lp, b0, len, inv, grad_out,
-                                          partials, &p->d_rec->overflow, s);
+        cudaError_t e = zk::launch_reduce(grad_slices, p->n_ranks, p->lp, p->reduce_lp_accum, b0, len,
+                                          inv, grad_out, partials, &p->d_rec->overflow, s);
         if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
     }
     return ZERO_OK;

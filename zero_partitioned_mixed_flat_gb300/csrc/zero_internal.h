@@ -32,7 +32,7 @@ int sm_count();
 // message for zero_last_error() on the calling thread
 void set_last_error(const char *msg);
 
-cudaError_t launch_reduce(const void *const *slices, int n, int lp,
+cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp,
                           int64_t offset, int64_t len, float inv, float *g,
                           double *partials, unsigned *overflow,
                           cudaStream_t stream);

@@ -81,5 +81,8 @@ class ZeroPlan:
     def set_state(self, step, good_steps=0):
         A.zero_plan_set_state(self.handle, step, good_steps)
 
+    def set_reduce_precision(self, accumulate_in_lp):
+        A.zero_plan_set_reduce_precision(self.handle, accumulate_in_lp)
+
     def set_spin_limit(self, polls):
         A.zero_plan_set_spin_limit(self.handle, polls)

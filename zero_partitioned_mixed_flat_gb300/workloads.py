@@ -73,6 +73,7 @@ class Workload:
     wd: float = 0.01
     adamw: bool = True
     clip: float = 1.0
+    reduce_lp_accum: bool = False  # partial sums rounded to the lp type
     notes: str = field(default="")
 
 

@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--quantized-gather", action="store_true",
+                    help="stage-3 workloads: int8 block-quantized gathers")
     return ap.parse_args()
 
 
@@ -179,6 +181,7 @@ class Run:
         self.param = None if w.stage == 3 else torch.zeros(self.plan.psi_padded, dtype=lpd,
                                                            device=dev)
         self.gather_shards = None
+        self.quantized = bool(w.stage == 3 and w.gather and w.gather_quantized)
         if w.stage == 3 and w.gather:
             r0 = self.ranks[0]
             others = [synth.lp_shard(P, w.lp, w.master_std, 0, j, dev)
@@ -186,6 +189,16 @@ class Run:
             self.gather_shards = others[:r0] + [self.shard[r0]] + others[r0:]
             biggest = max(self.plan.shard_len(u) for u in range(self.plan.n_units)) * w.n_ranks
             self.gather_out = torch.empty(biggest, dtype=lpd, device=dev)
+            if self.quantized:
+                # every rank's int8 codes + block scales (ZeRO++-style gather);
+                # the other ranks quantize their shards once here
+                self.codes = [torch.empty(P, dtype=torch.int8, device=dev) for _ in range(w.n_ranks)]
+                self.scales = [torch.empty(P // 128, dtype=torch.float32, device=dev)
+                               for _ in range(w.n_ranks)]
+                for j in range(w.n_ranks):
+                    self.plan.quantize(self.gather_shards[j], self.codes[j], self.scales[j])
+                del others
+                self.gather_shards = [None] * w.n_ranks
         self.slice_lists = {r: [self.slices[r][j] for j in range(w.n_ranks)] for r in self.ranks}
         bucket = w.bucket_elems
         tile = 32768
@@ -198,14 +211,17 @@ class Run:
     def launches_per_step(self):
         n = len(self.ranks)
         gathers = 2 * self.plan.n_units if self.gather_shards is not None else 0
-        return n * self.buckets + 1 + n + gathers
+        return n * self.buckets + 1 + n + gathers + (n if self.quantized else 0)
 
     def gathers(self, stream, events=None):
         if self.gather_shards is None:
             return
         units = list(range(self.plan.n_units))
         for u in units + units[::-1]:        # forward, then backward
-            self.plan.gather(u, self.gather_shards, self.gather_out, stream)
+            if self.quantized:
+                self.plan.gather_quantized(u, self.codes, self.scales, self.gather_out, stream)
+            else:
+                self.plan.gather(u, self.gather_shards, self.gather_out, stream)
 
     def reduce(self, stream):
         for r in self.ranks:
@@ -217,13 +233,21 @@ class Run:
             out = self.shard[r] if w.stage == 3 else self.param
             self.plan.adam(r, self.g[r], self.master[r], self.m[r], self.v[r], out, w.lr, w.beta1,
                            w.beta2, w.eps, w.wd, int(w.adamw), self.S, w.clip, 0.0, 0, stream)
+            if self.quantized:   # the updated shard, ready for the next step's gathers
+                self.plan.quantize(self.shard[r], self.codes[r], self.scales[r], stream)
+
+    def gather_bytes_per_element(self):
+        # lp gather: 2 B in + 2 B out; quantized: 1 B code + 4/128 B scale in, 2 B out
+        return (3 + 4 / 128) if self.quantized else 4
 
     def bytes_per_step(self):
         b = bytes_per_element(self.w.n_ranks)
         step = b["step"] * self.P * len(self.ranks)
         if self.gather_shards is not None:
-            step += 2 * 4 * int(sum(self.plan.unit_padded))
-        return step
+            step += 2 * self.gather_bytes_per_element() * int(sum(self.plan.unit_padded))
+        if self.quantized:
+            step += (3 + 4 / 128) * self.P * len(self.ranks)
+        return int(step)
 
 
 def dist_setup(n_gpus):
@@ -341,6 +365,9 @@ def main():
     ws, rank, local, dist = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
+    if args.quantized_gather:
+        import dataclasses
+        w = dataclasses.replace(w, gather_quantized=True)
     # weak scaling: every GPU owns its own partition(s) of the simulated job
     part_ranks = [(r + rank) % w.n_ranks for r in w.ranks]
     t_setup = time.perf_counter()
@@ -408,14 +435,15 @@ def main():
     if run.gather_shards is not None:
         n_gathers = 2 * run.plan.n_units
         per_call_ms["gather"] = statistics.mean(gather_ms) / n_gathers
-        kernel_bytes["gather"] = 4 * int(sum(run.plan.unit_padded)) // run.plan.n_units
+        kernel_bytes["gather"] = (run.gather_bytes_per_element() * int(sum(run.plan.unit_padded))
+                                  / run.plan.n_units)
     # dominant kernel = the one with the largest share of the step
     share = {"reduce": statistics.mean(reduce_ms), "adam": statistics.mean(adam_ms)}
     if run.gather_shards is not None:
         share["gather"] = statistics.mean(gather_ms)
     dom = max(share, key=share.get)
     kname = {"reduce": "reduce_unscale_stats", "adam": "adam_fused_cast",
-             "gather": "gather_layer_tma"}[dom]
+             "gather": "gather_dequant" if run.quantized else "gather_layer_tma"}[dom]
     achieved = kernel_bytes[dom] / (per_call_ms[dom] / 1e3) / 1e9
     step_gbs = run.bytes_per_step() / (ms_per_step / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,

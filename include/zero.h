@@ -230,6 +230,33 @@ zero_status zero_gather_layer(zero_plan *plan, int32_t unit,
                               void *stream);
 
 /* ----------------------------------------------------------------------
+ * Quantized stage-3 gather ("ZeRO-1/2/3 vs DDP" note, ZeRO++: the
+ * all-gathered parameters are quantized to cut the traffic).  Stage-3 plans
+ * whose align is a multiple of ZERO_QUANT_BLOCK.
+ *
+ * zero_quantize_shard: shard (P lp elements, this rank's own shard buffer)
+ * -> codes (P int8) and scales (P / ZERO_QUANT_BLOCK floats), per block of
+ * ZERO_QUANT_BLOCK elements:
+ *   amax = max |x|,  scale = amax / 127 (float division),
+ *   code = nearest integer (ties to even) to x / scale, clamped to
+ *          [-127, 127]; 0 when scale == 0.
+ * zero_gather_layer_quantized: like zero_gather_layer, from every rank's
+ * codes/scales (the buffers zero_quantize_shard wrote, whole-partition
+ * pointers; the library adds the unit's offset):
+ *   out[j * (U_p/N) + k] = lp(code_j[o + k] * scale_j[(o + k) / BLOCK])
+ * with o the unit's shard offset; the product is a float multiply rounded to
+ * the lp type (nearest even).  1 B + 4/128 B read per element instead of 2 B.
+ * All pointers 16-byte aligned, device memory, asynchronous on `stream`.
+ */
+#define ZERO_QUANT_BLOCK 128
+zero_status zero_quantize_shard(zero_plan *plan, const void *shard, int8_t *codes,
+                                float *scales, void *stream);
+zero_status zero_gather_layer_quantized(zero_plan *plan, int32_t unit,
+                                        const int8_t *const *codes,
+                                        const float *const *scales, void *out,
+                                        void *stream);
+
+/* ----------------------------------------------------------------------
  * Allocation-free reduce.  The paper has no counterpart: this is a service
  * for callers that cannot allocate device memory -- e.g. code whose device
  * memory is entirely owned by a framework's caching allocator (an extra

@@ -64,6 +64,10 @@ def lib():
         L.orc_adam.argtypes = [_i64, _vp, _vp, _vp, _vp, _vp, _i32, _f32, _i32,
                                _f32, _f32, _f32, _f32, _f32, _i32, _f32, _f32]
         L.orc_adam.restype = None
+        L.orc_quantize_blocks.argtypes = [_i64, _vp, _i32, _i32, _vp, _vp]
+        L.orc_quantize_blocks.restype = None
+        L.orc_dequant_gather.argtypes = [_i32, _vp, _vp, _i64, _i32, _i32, _vp]
+        L.orc_dequant_gather.restype = None
         L.orc_gather.argtypes = [_i32, _vp, _i64, _vp]
         L.orc_gather.restype = None
         _LIB = L
@@ -208,7 +212,27 @@ def gather(shards):
     return out
 
 
+def quantize_blocks(x_codes, lp, block=128):
+    x = _c(x_codes, np.uint16)
+    assert x.size % block == 0
+    q = np.empty(x.size, np.int8)
+    sc = np.empty(x.size // block, np.float32)
+    lib().orc_quantize_blocks(x.size, _ptr(x), lp, block, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def dequant_gather(qs, scales, lp, block=128):
+    qs = [_c(q, np.int8) for q in qs]
+    scales = [_c(s, np.float32) for s in scales]
+    length = qs[0].size
+    out = np.empty(length * len(qs), np.uint16)
+    lib().orc_dequant_gather(len(qs), C.cast(_ptr_array(qs), _vp), C.cast(_ptr_array(scales), _vp),
+                             length, block, lp, _ptr(out))
+    return out
+
+
 LIB_PATH = _build.LIB
 __all__ = ["lib", "lp_to_float", "float_to_lp", "layout", "partition_to_flat",
-           "fragments", "memory", "reduce", "reduce_lp_accum", "decide", "adam", "gather", "LIB_PATH",
+           "fragments", "memory", "reduce", "reduce_lp_accum", "decide", "quantize_blocks",
+           "dequant_gather", "adam", "gather", "LIB_PATH",
            "Decision"]

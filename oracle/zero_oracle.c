@@ -482,3 +482,45 @@ void orc_gather(int32_t n, const uint16_t *const *shards, int64_t shard_len,
         for (int64_t k = 0; k < shard_len; ++k)
             out[(int64_t)j * shard_len + k] = shards[j][k];
 }
+
+/* ------------------------------------------------------------------------
+ * Quantized all-gather.  [P1] "ZeRO++": ZeRO++ quantizes the parameters that
+ * the all-gather moves.  Symmetric int8 with one scale per block (the pages
+ * give no block size or rounding rule; the readings are listed in the design
+ * notes): the largest magnitude of the block maps to 127.
+ * ---------------------------------------------------------------------- */
+void orc_quantize_blocks(int64_t len, const uint16_t *x, int32_t lp, int32_t block,
+                         int8_t *q, float *scales)
+{
+    for (int64_t b0 = 0; b0 < len; b0 += block) {
+        float amax = 0.0f, scale;
+        for (int32_t k = 0; k < block; ++k) {
+            float a = fabsf(orc_lp_to_float(x[b0 + k], lp));
+            if (a > amax)
+                amax = a;
+        }
+        scale = amax / 127.0f;
+        scales[b0 / block] = scale;
+        for (int32_t k = 0; k < block; ++k) {
+            float r = 0.0f;
+            if (scale > 0.0f) {
+                r = nearbyintf(orc_lp_to_float(x[b0 + k], lp) / scale);
+                if (r > 127.0f)
+                    r = 127.0f;
+                if (r < -127.0f)
+                    r = -127.0f;
+            }
+            q[b0 + k] = (int8_t)r;
+        }
+    }
+}
+
+void orc_dequant_gather(int32_t n, const int8_t *const *q, const float *const *scales,
+                        int64_t shard_len, int32_t block, int32_t lp, uint16_t *out)
+{
+    for (int32_t j = 0; j < n; ++j)
+        for (int64_t k = 0; k < shard_len; ++k) {
+            float y = (float)q[j][k] * scales[j][k / block];
+            out[(int64_t)j * shard_len + k] = orc_float_to_lp(y, lp);
+        }
+}

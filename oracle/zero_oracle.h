@@ -133,6 +133,21 @@ void orc_adam(int64_t len, const float *g, float *master, float *m, float *v,
 void orc_gather(int32_t n, const uint16_t *const *shards, int64_t shard_len,
                 uint16_t *out);
 
+/* ---- quantized all-gather ([P1] "ZeRO++": the all-gathered parameters are
+ * quantized to cut the traffic) ------------------------------------------
+ * Blocks of `block` consecutive elements share one float scale:
+ *   amax  = max |x| over the block (x = the lp parameter widened to float)
+ *   scale = amax / 127                               (float division)
+ *   q     = nearest integer to x / scale, ties to even, in [-127, 127]
+ *           (q = 0 when scale == 0)
+ * and the receiver's value is lp(q * scale) (float product, rounded to lp).
+ * len must be a multiple of block.                                        */
+void orc_quantize_blocks(int64_t len, const uint16_t *x, int32_t lp, int32_t block,
+                         int8_t *q, float *scales);
+/* out[j * shard_len + k] = lp(q_j[k] * scale_j[k / block]) */
+void orc_dequant_gather(int32_t n, const int8_t *const *q, const float *const *scales,
+                        int64_t shard_len, int32_t block, int32_t lp, uint16_t *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -296,3 +296,49 @@ def test_global_stats_replace_the_local_sum(zlib):
         plan.set_global_stats(ss, 0)
     assert e.value.code == Z.ZERO_ESTATE
     plan.close()
+
+
+# ------------------------------------------------------ quantized gather
+
+def _quant_case(n, sizes, units, lp):
+    dev = torch.device("cuda")
+    plan = _plan(-1, n, lp, stage=3, align=128, sizes=sizes, units=units)
+    P = plan.part_len
+    shards = [synth.lp_shard(P, lp, 0.02, 5, j, dev) for j in range(n)]
+    shards[0][:256].zero_()                       # whole zero blocks: scale 0
+    codes = [torch.empty(P, dtype=torch.int8, device=dev) for _ in range(n)]
+    scales = [torch.empty(P // 128, dtype=torch.float32, device=dev) for _ in range(n)]
+    for j in range(n):
+        plan.quantize(shards[j], codes[j], scales[j])
+    torch.cuda.synchronize()
+    host_q = []
+    for j in range(n):
+        oq, osc = oracle.quantize_blocks(synth.to_numpy_codes(shards[j]), lp, 128)
+        assert np.array_equal(codes[j].cpu().numpy(), oq), j
+        assert np.array_equal(scales[j].cpu().numpy().view(np.uint32), osc.view(np.uint32)), j
+        host_q.append((oq, osc))
+    for u in range(plan.n_units):
+        sl, off = plan.shard_len(u), plan.unit_shard_offset(u)
+        out = torch.full((sl * n,), 3, dtype=synth.LP_DTYPES[lp], device=dev)
+        plan.gather_quantized(u, codes, scales, out)
+        exp = oracle.dequant_gather([q[off:off + sl] for q, _ in host_q],
+                                    [c[off // 128:(off + sl) // 128] for _, c in host_q], lp, 128)
+        assert np.array_equal(synth.to_numpy_codes(out), exp), u
+    plan.close()
+
+
+@pytest.mark.parametrize("n", [2, 3, 64, 65])
+@pytest.mark.parametrize("lp", [0, 1])
+def test_quantize_and_dequant_gather(zlib, n, lp):
+    _quant_case(n, [5000, 128, 40_000, 3, 70_000], [0, 0, 1, 2, 2], lp)
+
+
+def test_quantized_gather_rejects_small_align(zlib):
+    plan = _plan(-1, 2, 0, stage=3, align=8, sizes=[64, 64], units=[0, 1])
+    buf = torch.zeros(1024, dtype=torch.float16, device="cuda")
+    q = torch.zeros(1024, dtype=torch.int8, device="cuda")
+    sc = torch.zeros(8, dtype=torch.float32, device="cuda")
+    with pytest.raises(Z.ZeroError) as e:
+        plan.quantize(buf, q, sc)
+    assert e.value.code == Z.ZERO_EINVAL
+    plan.close()

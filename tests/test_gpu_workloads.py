@@ -41,35 +41,58 @@ def test_gpt2_xl_zero2_overflow_step(zlib, rank):
     assert seen == [(0, 65536.0, 1), (1, 32768.0, 1), (0, 32768.0, 2)]
 
 
-def _check_gathers(h, others, gen):
+def _synthetic_shards(plan, w, dev):
+    """Every rank's lp shard buffer as seeded synthetic data: the gathers are
+    checked on inputs that no kernel produced."""
+    return [synth.lp_shard(plan.part_len, w.lp, w.master_std, 9, j, dev) for j in range(w.n_ranks)]
+
+
+def _windows(sl, gen):
+    """Block-aligned (128) windows of one unit shard: both ends + 6 random."""
+    L = min(2048, sl)
+    starts = {0, (sl - L) // 128 * 128}
+    starts |= {int(x) // 128 * 128 for x in gen.integers(0, max(1, sl - L), 6)}
+    return [(k0, min(L, sl - k0)) for k0 in sorted(starts)]
+
+
+def _check_gathers(plan, w, shards, gen, quantized):
     """Gather every unit (forward order) and compare sampled windows with the
-    oracle's concatenation of the same windows of the N shards."""
-    plan, n = h.plan, h.w.n_ranks
-    shards = [h.st[0].shard] + others
+    oracle's gather (or quantize + dequantizing gather) of the same windows."""
+    n, dev = w.n_ranks, shards[0].device
     biggest = max(plan.shard_len(u) for u in range(plan.n_units)) * n
-    out = torch.empty(biggest, dtype=synth.LP_DTYPES[h.w.lp], device=h.dev)
+    out = torch.empty(biggest, dtype=synth.LP_DTYPES[w.lp], device=dev)
+    if quantized:
+        codes = [torch.empty(plan.part_len, dtype=torch.int8, device=dev) for _ in range(n)]
+        scales = [torch.empty(plan.part_len // 128, dtype=torch.float32, device=dev) for _ in range(n)]
+        for j in range(n):
+            plan.quantize(shards[j], codes[j], scales[j])
     for u in range(plan.n_units):
         sl, off = plan.shard_len(u), plan.unit_shard_offset(u)
-        plan.gather(u, shards, out)
+        if quantized:
+            plan.gather_quantized(u, codes, scales, out)
+        else:
+            plan.gather(u, shards, out)
         torch.cuda.synchronize()
-        starts = [0, max(0, sl - 2048)] + list(gen.integers(0, max(1, sl - 2048), 6))
-        for k0 in starts:
-            L = min(2048, sl - k0)
-            win = [synth.to_numpy_codes(s[off + k0: off + k0 + L]) for s in shards]
-            exp = oracle.gather(win).reshape(n, L)
+        for k0, L in _windows(sl, gen):
+            win = [synth.to_numpy_codes(t[off + k0: off + k0 + L]) for t in shards]
+            if quantized:
+                qs = [oracle.quantize_blocks(x, w.lp, 128) for x in win]
+                exp = oracle.dequant_gather([q for q, _ in qs], [c for _, c in qs], w.lp, 128)
+            else:
+                exp = oracle.gather(win)
             got = synth.to_numpy_codes(out[:sl * n].view(n, sl)[:, k0:k0 + L])
-            assert np.array_equal(got, exp), (u, k0)
+            assert np.array_equal(got, exp.reshape(n, L)), (u, k0)
     plan.check()
 
 
 def test_7p5b_zero3_with_gathers(zlib):
     w = WORKLOADS["7.5b-zero3"]
     h = Harness(w, full=False, threads=16, chunk=1 << 21)
-    others = [synth.lp_shard(h.P, w.lp, w.master_std, 0, j, h.dev) for j in range(1, w.n_ranks)]
-    gen = np.random.default_rng(7)
     for _ in range(w.steps):
         h.step()
-        _check_gathers(h, others, gen)
+    shards = _synthetic_shards(h.plan, w, h.dev)
+    _check_gathers(h.plan, w, shards, np.random.default_rng(7), quantized=False)
+    _check_gathers(h.plan, w, shards, np.random.default_rng(8), quantized=True)
     h.close()
 
 

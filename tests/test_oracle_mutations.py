@@ -45,6 +45,10 @@ MUTANTS = {
     "memory_stage2_k": ("int_plus_ratio(2 * psi, 14 * psi, n_ranks)",
                         "int_plus_ratio(2 * psi, 12 * psi, n_ranks)"),
     "comm_stage3": ("comm[3] = 3 * psi;", "comm[3] = 2 * psi;"),
+    "quant_scale_255": ("scale = amax / 127.0f;", "scale = amax / 255.0f;"),
+    "quant_truncates": ("r = nearbyintf(orc_lp_to_float(x[b0 + k], lp) / scale);",
+                        "r = truncf(orc_lp_to_float(x[b0 + k], lp) / scale);"),
+    "dequant_wrong_block": ("scales[j][k / block]", "scales[j][k / block / 2]"),
     "lp_accum_not_rounded": ("run = orc_float_to_lp(orc_lp_to_float(run, lp) +\n                                      orc_lp_to_float(slices[j][i], lp), lp);",
                              "run = orc_float_to_lp(orc_lp_to_float(run, lp), lp);"),
 }

@@ -588,3 +588,47 @@ def test_sharded_step_equals_ddp(orc, n, stage):
 @pytest.mark.parametrize("n", [2, 3, 8])
 def test_sharded_stage3_units_equals_ddp(orc, n):
     _ddp_vs_sharded(orc, [300, 17, 64, 64, 1, 999], [0, 0, 1, 2, 2, 3], n, 3, 0, 2, 0.05, 10 + n)
+
+
+# ------------------------------------------------ quantized gather (ZeRO++)
+
+def test_quantize_hand_block(orc):
+    # one 8-element block with amax 127: scale 1, codes are x rounded to even
+    x = _half([127.0, -127.0, 0.5, 1.5, 2.5, -0.5, -3.5, 0.0])
+    q, sc = orc.quantize_blocks(x, 0, block=8)
+    assert sc.tolist() == [1.0]
+    assert q.tolist() == [127, -127, 0, 2, 2, 0, -4, 0]
+    y = orc.dequant_gather([q], [sc], 0, block=8)
+    assert orc.lp_to_float(y, 0).tolist() == [127.0, -127.0, 0.0, 2.0, 2.0, 0.0, -4.0, 0.0]
+    # an all-zero block: scale 0, codes 0, values 0
+    q, sc = orc.quantize_blocks(_half([0.0] * 8), 0, block=8)
+    assert sc.tolist() == [0.0] and not q.any()
+
+
+def test_quantize_matches_numpy_rint_and_bounds(orc):
+    rng = np.random.default_rng(21)
+    for lp in (0, 1):
+        x = (rng.standard_normal(128 * 400) * 10.0 ** rng.integers(-3, 2, 128 * 400)).astype(np.float32)
+        codes = orc.float_to_lp(x, lp)
+        xf = orc.lp_to_float(codes, lp).reshape(-1, 128)
+        q, sc = orc.quantize_blocks(codes, lp, 128)
+        amax = np.abs(xf).max(axis=1)
+        assert np.array_equal(sc, (amax / np.float32(127)).astype(np.float32))
+        ref = np.rint(xf / sc[:, None]).astype(np.int8)          # numpy: RN-even
+        assert np.array_equal(q.reshape(-1, 128), ref)
+        # the block maximum maps to +-127 and every code is within the range
+        assert np.all(np.abs(q.reshape(-1, 128)).max(axis=1) == 127)
+        # dequantized error within half a step (plus the lp rounding)
+        y = orc.lp_to_float(orc.dequant_gather([q], [sc], lp, 128), lp).reshape(-1, 128)
+        lp_ulp = 2.0 ** (-10 if lp == 0 else -7)
+        assert np.all(np.abs(y - xf) <= sc[:, None] * 0.5 * (1 + 1e-6) + np.abs(y) * lp_ulp)
+
+
+def test_dequant_gather_layout(orc):
+    rng = np.random.default_rng(22)
+    shards = [orc.float_to_lp(rng.standard_normal(256).astype(np.float32), 0) for _ in range(3)]
+    qs = [orc.quantize_blocks(s, 0, 128) for s in shards]
+    out = orc.dequant_gather([q for q, _ in qs], [c for _, c in qs], 0, 128)
+    for j in range(3):
+        one = orc.dequant_gather([qs[j][0]], [qs[j][1]], 0, 128)
+        assert np.array_equal(out[j * 256:(j + 1) * 256], one)

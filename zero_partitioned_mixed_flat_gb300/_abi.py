@@ -40,6 +40,8 @@ SIGNATURES = {
     "zero_step_result": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "zero_plan_check": (_i32, [_vp]),
     "zero_gather_layer": (_i32, [_vp, _i32, _vp, _vp, _vp]),
+    "zero_quantize_shard": (_i32, [_vp, _vp, _vp, _vp, _vp]),
+    "zero_gather_layer_quantized": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     "zero_reduce_partition_noalloc": (_i32, [_i32, _i32, _vp, _i64, _f32, _vp, _vp, _vp, _vp]),
     "zero_memory_report": (_i32, [_i64, _i32, _i32, _vp, _vp, _vp]),
     "zero_plan_destroy": (None, [_vp]),
@@ -215,6 +217,21 @@ def zero_plan_check(plan: int):
 def zero_gather_layer(plan: int, unit: int, shards: Sequence, out, stream=None):
     _check(load().zero_gather_layer(plan, unit, C.cast(_ptr_array(shards), _vp), _ptr(out),
                                     _stream(stream)), "zero_gather_layer")
+
+
+ZERO_QUANT_BLOCK = 128
+
+
+def zero_quantize_shard(plan: int, shard, codes, scales, stream=None):
+    _check(load().zero_quantize_shard(plan, _ptr(shard), _ptr(codes), _ptr(scales),
+                                      _stream(stream)), "zero_quantize_shard")
+
+
+def zero_gather_layer_quantized(plan: int, unit: int, codes: Sequence, scales: Sequence, out,
+                                stream=None):
+    _check(load().zero_gather_layer_quantized(plan, unit, C.cast(_ptr_array(codes), _vp),
+                                              C.cast(_ptr_array(scales), _vp), _ptr(out),
+                                              _stream(stream)), "zero_gather_layer_quantized")
 
 
 ZERO_NOALLOC_MAX_ELEMS = 8192 * 32768

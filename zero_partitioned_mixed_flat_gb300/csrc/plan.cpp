@@ -470,6 +470,47 @@ zero_status zero_gather_layer(zero_plan *p, int32_t unit, const void *const *sha
     return ZERO_OK;
 }
 
+zero_status zero_quantize_shard(zero_plan *p, const void *shard, int8_t *codes, float *scales,
+                                void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (p->stage != 3) return fail(ZERO_EINVAL, "the quantized gather needs a stage-3 plan");
+    if (p->align % ZERO_QUANT_BLOCK != 0)
+        return fail(ZERO_EINVAL, "the quantized gather needs align to be a multiple of %d", ZERO_QUANT_BLOCK);
+    if (p->part > 0 && (!shard || !codes || !scales)) return fail(ZERO_EINVAL, "NULL pointer argument");
+    if (!aligned16(shard) || !aligned16(codes) || !aligned16(scales))
+        return fail(ZERO_EALIGN, "shard, codes or scales is not 16-byte aligned");
+    zero_status st = ensure_device(p);
+    if (st != ZERO_OK) return st;
+    cudaError_t e = zk::launch_quantize(shard, p->lp, p->part, codes, scales, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "quantize kernel launch");
+    return ZERO_OK;
+}
+
+zero_status zero_gather_layer_quantized(zero_plan *p, int32_t unit, const int8_t *const *codes,
+                                        const float *const *scales, void *out, void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (p->stage != 3) return fail(ZERO_EINVAL, "the quantized gather needs a stage-3 plan");
+    if (p->align % ZERO_QUANT_BLOCK != 0)
+        return fail(ZERO_EINVAL, "the quantized gather needs align to be a multiple of %d", ZERO_QUANT_BLOCK);
+    if (unit < 0 || unit >= p->n_units()) return fail(ZERO_EINVAL, "unit %d outside [0, %d)", unit, p->n_units());
+    const int64_t shard = p->shard_len(unit);
+    if (!codes || !scales || (!out && shard > 0)) return fail(ZERO_EINVAL, "NULL codes, scales or output");
+    for (int32_t j = 0; j < p->n_ranks; ++j) {
+        if (shard > 0 && (!codes[j] || !scales[j])) return fail(ZERO_EINVAL, "codes[%d] or scales[%d] is NULL", j, j);
+        if (!aligned16(codes[j]) || !aligned16(scales[j]))
+            return fail(ZERO_EALIGN, "codes[%d] or scales[%d] is not 16-byte aligned", j, j);
+    }
+    if (!aligned16(out)) return fail(ZERO_EALIGN, "out is not 16-byte aligned");
+    zero_status st = ensure_device(p);
+    if (st != ZERO_OK) return st;
+    int64_t off = 0;
+    for (int32_t u = 0; u < unit; ++u) off += p->shard_len(u);
+    cudaError_t e = zk::launch_dequant_gather(codes, scales, p->n_ranks, p->lp, off, shard, out,
+                                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dequantizing gather kernel launch");
+    return ZERO_OK;
+}
+
 zero_status zero_memory_report(int64_t psi, int32_t n_ranks, int32_t align, double formula_bytes[4],
                                int64_t actual_bytes[4], int64_t comm_elems[4]) {
     if (psi < 0 || n_ranks < 1 || align < 1) return fail(ZERO_EINVAL, "psi < 0, n_ranks < 1 or align < 1");

@@ -78,6 +78,12 @@ class ZeroPlan:
     def gather(self, unit, shards, out, stream=None):
         A.zero_gather_layer(self.handle, unit, shards, out, stream)
 
+    def quantize(self, shard, codes, scales, stream=None):
+        A.zero_quantize_shard(self.handle, shard, codes, scales, stream)
+
+    def gather_quantized(self, unit, codes, scales, out, stream=None):
+        A.zero_gather_layer_quantized(self.handle, unit, codes, scales, out, stream)
+
     def set_state(self, step, good_steps=0):
         A.zero_plan_set_state(self.handle, step, good_steps)
 

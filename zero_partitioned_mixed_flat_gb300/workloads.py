@@ -74,6 +74,7 @@ class Workload:
     adamw: bool = True
     clip: float = 1.0
     reduce_lp_accum: bool = False  # partial sums rounded to the lp type
+    gather_quantized: bool = False  # stage 3: int8 block-quantized gathers
     notes: str = field(default="")
 
 
@@ -100,6 +101,11 @@ def _make():
         ranks=[0], steps=4, loss_scale=65536.0, growth_interval=1000,
         grads_times_scale=True, gather=True,
         notes="7.5B, 33 units (rest + 32 d=4096 blocks), N=64 rank 0, fp16, gathers")
+    w["7.5b-zero3-q8"] = Workload(
+        name="7.5b-zero3-q8", sizes=s, unit_of_tensor=u, n_ranks=64, stage=3, lp=0,
+        ranks=[0], steps=4, loss_scale=65536.0, growth_interval=1000,
+        grads_times_scale=True, gather=True, gather_quantized=True,
+        notes="7.5b-zero3 with ZeRO++-style int8 block-quantized gathers")
     w["13b-zero2"] = Workload(
         name="13b-zero2", sizes=[13_000_000_000], n_ranks=16, stage=2, lp=1,
         ranks=[0], steps=4, loss_scale=1.0, growth_interval=0,

@@ -139,8 +139,12 @@ zero_status zero_plan_set_spin_limit(zero_plan *plan, int64_t polls);
  * Reduce ("10.6 ZeRO 与 FSDP" §10.6.1 Reduce-Scatter, §10.6.2 Step 2; average
  * over ranks per "ZeRO-1/2/3 vs DDP" ZeRO-2; unscale per "年糕切片" §4.3).
  *
- * grad_slices: N device pointers; grad_slices[j] holds P lp elements, rank
- * j's gradient over rank `rank`'s partition.  For every i < P:
+ * grad_slices: N pointers; grad_slices[j] holds P lp elements, rank j's
+ * gradient over rank `rank`'s partition.  They may be device memory of the
+ * current device, managed memory, pinned host memory (cudaHostAlloc /
+ * cudaHostRegister: the kernel then reads it in place, over NVLink-C2C on
+ * Grace systems, with no staging copy), or pageable host memory where the
+ * device reads host page tables; anything else is ZERO_EINVAL.  For i < P:
  *   s = g_0[i] + g_1[i] + ... + g_{N-1}[i]   (float, in rank order)
  *   grad_out[i] = s * float(1 / (loss_scale * N))
  * and, over the partition, the overflow flag (any s not finite) and the

@@ -342,3 +342,24 @@ def test_quantized_gather_rejects_small_align(zlib):
         plan.quantize(buf, q, sc)
     assert e.value.code == Z.ZERO_EINVAL
     plan.close()
+
+
+@pytest.mark.parametrize("lp", [0, 1])
+def test_reduce_reads_pinned_host_slices(zlib, lp):
+    # the slices may stay in pinned host memory: the kernel reads them in place
+    n, part = 8, 3 * TILE + 64
+    dev = torch.device("cuda")
+    dslices = [synth.grad_slice(part, lp, 1e-3, 1.0, 3, 1, j, 0, dev) for j in range(n)]
+    hslices = [torch.empty(part, dtype=t.dtype, pin_memory=True) for t in dslices]
+    for h, d in zip(hslices, dslices):
+        h.copy_(d)
+    torch.cuda.synchronize()
+    out = []
+    for sl in (dslices, hslices):
+        plan = _plan(n * part, n, lp)
+        g = torch.empty(part, dtype=torch.float32, device=dev)
+        plan.reduce(0, sl, g, 1.0)
+        out.append((g, plan.stats()))
+        plan.close()
+    assert same_floats(out[0][0].cpu().numpy(), out[1][0].cpu().numpy())
+    assert out[0][1] == out[1][1]

@@ -618,92 +618,6 @@ gather_layer_tma(const __grid_constant__ GatherParams<MAXN> p) {
     bulk_wait_all();
 }
 
-// ------------------------------------------------- K5/K6 quantized gather
-// ZeRO++ ("ZeRO-1/2/3 vs DDP" note, ZeRO++: the all-gathered parameters are
-// quantized): each rank turns its lp shard into int8 codes with one float
-// scale per 128-element block (symmetric, block max -> 127, nearest-even),
-// and the gather expands codes * scale back to lp while it concatenates.
-// Per element the gather moves 1 B + 4/128 B in and 2 B out, against 2 B in
-// and 2 B out for the lp gather.
-
-constexpr int kQuantThreads = 256;
-
-template <bool BF16>
-__global__ void __launch_bounds__(kQuantThreads)
-quantize_shard_blocks(const uint2 *__restrict__ x, uint32_t *__restrict__ q, float *__restrict__ scales,
-                      long long n_blocks) {
-    const int lane = threadIdx.x & 31;
-    const long long warps = (long long)gridDim.x * (kQuantThreads / 32);
-    for (long long b = (long long)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5); b < n_blocks;
-         b += warps) {
-        // lane holds elements 4*lane .. 4*lane+3 of block b
-        const uint2 raw = __ldcs(x + b * 32 + lane);
-        float v[4];
-        const uint32_t w[2] = {raw.x, raw.y};
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            if constexpr (BF16) {
-                v[2 * k] = __uint_as_float(w[k] << 16);
-                v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-            } else {
-                const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
-                v[2 * k] = t.x;
-                v[2 * k + 1] = t.y;
-            }
-        }
-        float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float scale = __fdiv_rn(amax, 127.0f);
-        uint32_t packed = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            int c = 0;
-            if (scale > 0.0f) {
-                c = __float2int_rn(__fdiv_rn(v[k], scale));
-                c = c > 127 ? 127 : (c < -127 ? -127 : c);
-            }
-            packed |= (uint32_t)(c & 0xff) << (8 * k);
-        }
-        __stcs(q + b * 32 + lane, packed);
-        if (lane == 0) scales[b] = scale;
-    }
-}
-
-template <int MAXN>
-struct DequantGatherParams {
-    const uint4 *codes[MAXN];    // rank j's codes at this unit's offset (16 per uint4)
-    const float *scales[MAXN];   // rank j's scales at this unit's first block
-    uint4 *out;                  // 8 lp per uint4
-    long long vec_per_shard;     // shard_len / 16
-    long long n_items;           // n * vec_per_shard
-};
-
-template <int MAXN, bool BF16>
-__global__ void __launch_bounds__(kQuantThreads)
-gather_dequant(const __grid_constant__ DequantGatherParams<MAXN> p) {
-    const long long stride = (long long)gridDim.x * kQuantThreads;
-    for (long long i = (long long)blockIdx.x * kQuantThreads + threadIdx.x; i < p.n_items; i += stride) {
-        const long long j = i / p.vec_per_shard;
-        const long long k16 = i - j * p.vec_per_shard;
-        const uint4 c = ld_stream(p.codes[j] + k16);
-        const float scale = __ldg(p.scales[j] + (k16 >> 3));  // 16 codes lie in one 128-block
-        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-        uint32_t o[8];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            float y[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                y[k] = __fmul_rn((float)(int8_t)((w[t] >> (8 * k)) & 0xff), scale);
-            o[2 * t] = pack2<BF16>(y[0], y[1]);
-            o[2 * t + 1] = pack2<BF16>(y[2], y[3]);
-        }
-        __stcs(p.out + 2 * i, make_uint4(o[0], o[1], o[2], o[3]));
-        __stcs(p.out + 2 * i + 1, make_uint4(o[4], o[5], o[6], o[7]));
-    }
-}
-
 // -------------------------------------------------------------- host helpers
 
 struct DevInfo {
@@ -869,58 +783,6 @@ cudaError_t launch_gather(const void *const *shards, int n, int64_t src_offset_b
     if (n <= 64)
         return gather_impl<64>(shards, n, src_offset_bytes, shard_bytes, out, spin_limit, error, stream);
     return gather_impl<1024>(shards, n, src_offset_bytes, shard_bytes, out, spin_limit, error, stream);
-}
-
-cudaError_t launch_quantize(const void *shard, int lp, int64_t len, int8_t *codes, float *scales,
-                            cudaStream_t stream) {
-    const long long blocks = len / 128;
-    if (blocks == 0) return cudaSuccess;
-    const int occ = lp ? occupancy(quantize_shard_blocks<true>, kQuantThreads, 0)
-                       : occupancy(quantize_shard_blocks<false>, kQuantThreads, 0);
-    long long grid = (long long)sm_count() * occ;
-    const long long need = (blocks + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
-    if (grid > need) grid = need;
-    const uint2 *x = static_cast<const uint2 *>(shard);
-    uint32_t *q = reinterpret_cast<uint32_t *>(codes);
-    if (lp)
-        quantize_shard_blocks<true><<<(unsigned)grid, kQuantThreads, 0, stream>>>(x, q, scales, blocks);
-    else
-        quantize_shard_blocks<false><<<(unsigned)grid, kQuantThreads, 0, stream>>>(x, q, scales, blocks);
-    return cudaGetLastError();
-}
-
-template <int MAXN>
-cudaError_t dequant_gather_impl(const int8_t *const *codes, const float *const *scales, int n, int lp,
-                                int64_t offset, int64_t shard_len, void *out, cudaStream_t stream) {
-    DequantGatherParams<MAXN> p;
-    for (int j = 0; j < n; ++j) {
-        p.codes[j] = reinterpret_cast<const uint4 *>(codes[j] + offset);
-        p.scales[j] = scales[j] + offset / 128;
-    }
-    for (int j = n; j < MAXN; ++j) {
-        p.codes[j] = nullptr;
-        p.scales[j] = nullptr;
-    }
-    p.out = static_cast<uint4 *>(out);
-    p.vec_per_shard = shard_len / 16;
-    p.n_items = p.vec_per_shard * n;
-    if (p.n_items == 0) return cudaSuccess;
-    const int occ = lp ? occupancy(gather_dequant<MAXN, true>, kQuantThreads, 0)
-                       : occupancy(gather_dequant<MAXN, false>, kQuantThreads, 0);
-    long long grid = (long long)sm_count() * occ;
-    const long long need = (p.n_items + kQuantThreads - 1) / kQuantThreads;
-    if (grid > need) grid = need;
-    if (lp)
-        gather_dequant<MAXN, true><<<(unsigned)grid, kQuantThreads, 0, stream>>>(p);
-    else
-        gather_dequant<MAXN, false><<<(unsigned)grid, kQuantThreads, 0, stream>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_dequant_gather(const int8_t *const *codes, const float *const *scales, int n, int lp,
-                                  int64_t offset, int64_t shard_len, void *out, cudaStream_t stream) {
-    if (n <= 64) return dequant_gather_impl<64>(codes, scales, n, lp, offset, shard_len, out, stream);
-    return dequant_gather_impl<1024>(codes, scales, n, lp, offset, shard_len, out, stream);
 }
 
 }  // namespace zk

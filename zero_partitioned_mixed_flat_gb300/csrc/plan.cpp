@@ -146,6 +146,47 @@ zero_status ensure_device(zero_plan *p) {
     return ZERO_OK;
 }
 
+// Where the device can read an input buffer from: its own memory, managed
+// memory, pinned host memory (through the pinned buffer's device address;
+// over NVLink-C2C on Grace systems), or pageable host memory when the device
+// reads the host page tables.  Anything else is refused before any launch.
+zero_status readable_by_device(const void *ptr, int dev, const char *what, int32_t j,
+                               const void **out) {
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ZERO_EINVAL, "%s[%d]: cudaPointerGetAttributes: %s", what, j, cudaGetErrorString(e));
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice:
+        if (a.device != dev)
+            return fail(ZERO_EINVAL, "%s[%d] lives on device %d, the current device is %d", what, j,
+                        a.device, dev);
+        *out = ptr;
+        return ZERO_OK;
+    case cudaMemoryTypeManaged:
+        *out = ptr;
+        return ZERO_OK;
+    case cudaMemoryTypeHost:
+        if (!a.devicePointer) return fail(ZERO_EINVAL, "%s[%d]: pinned host memory without a device mapping", what, j);
+        if (!aligned16(a.devicePointer)) return fail(ZERO_EALIGN, "%s[%d]: device mapping not 16-byte aligned", what, j);
+        *out = a.devicePointer;
+        return ZERO_OK;
+    default: {
+        int pageable = 0;
+        if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess) {
+            cudaGetLastError();
+            pageable = 0;
+        }
+        if (!pageable)
+            return fail(ZERO_EINVAL, "%s[%d] is pageable host memory this device cannot read; pin it", what, j);
+        *out = ptr;
+        return ZERO_OK;
+    }
+    }
+}
+
 zero_status check_rank(const zero_plan *p, int32_t rank) {
     if (rank < 0 || rank >= p->n_ranks) return fail(ZERO_EINVAL, "rank %d outside [0, %d)", rank, p->n_ranks);
     if (p->stage == 0 && rank != 0)
@@ -319,6 +360,12 @@ zero_status zero_reduce_partition(zero_plan *p, int32_t rank, const void *const 
     if (!aligned16(grad_out)) return fail(ZERO_EALIGN, "grad_out is not 16-byte aligned");
     st = ensure_device(p);
     if (st != ZERO_OK) return st;
+    std::vector<const void *> src(size_t(p->n_ranks), nullptr);
+    if (p->part > 0)
+        for (int32_t j = 0; j < p->n_ranks; ++j) {
+            st = readable_by_device(grad_slices[j], p->device, "grad_slices", j, &src[size_t(j)]);
+            if (st != ZERO_OK) return st;
+        }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->phase != kReducing) {
         // a new step: forget the previous step's partitions and overflow
@@ -336,7 +383,7 @@ zero_status zero_reduce_partition(zero_plan *p, int32_t rank, const void *const 
     if (bucket <= 0) bucket = p->part;
     for (int64_t b0 = 0; b0 < p->part; b0 += bucket) {
         const int64_t len = std::min(bucket, p->part - b0);
-        cudaError_t e = zk::launch_reduce(grad_slices, p->n_ranks, p->lp, p->reduce_lp_accum, b0, len,
+        cudaError_t e = zk::launch_reduce(src.data(), p->n_ranks, p->lp, p->reduce_lp_accum, b0, len,
                                           inv, grad_out, partials, &p->d_rec->overflow, s);
         if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
     }

@@ -1,0 +1,212 @@
+// quant.cu -- the quantized stage-3 gather (sm_103a).
+//
+// ZeRO++ ("ZeRO-1/2/3 分别优化了什么" note, ZeRO++: the all-gathered
+// parameters are quantized to cut the traffic): each rank turns its lp shard
+// into int8 codes with one float scale per 128-element block (symmetric,
+// block max -> 127, nearest-even), and the gather expands code * scale back to
+// lp while it concatenates the ranks' shards.  Per layer element the gather
+// moves 1 B + 4/128 B in and 2 B out, against 2 B in and 2 B out for the lp
+// gather.  Both kernels are plain streaming kernels; each thread keeps several
+// independent 16-byte (or 8-byte) loads in flight before it computes.
+#include "zero_internal.h"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace zk {
+namespace {
+
+constexpr int kQuantThreads = 256;
+constexpr int kQuantUnroll = 4;   // blocks per warp (quantize) / items per thread (gather)
+
+__device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t to_lp2(float a, float b) {
+    if constexpr (BF16) {
+        return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+    } else {
+        return uint32_t(__half_as_ushort(__float2half_rn(a))) |
+               (uint32_t(__half_as_ushort(__float2half_rn(b))) << 16);
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void from_lp4(uint2 raw, float v[4]) {
+    const uint32_t w[2] = {raw.x, raw.y};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        if constexpr (BF16) {
+            v[2 * k] = __uint_as_float(w[k] << 16);
+            v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        } else {
+            const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            v[2 * k] = t.x;
+            v[2 * k + 1] = t.y;
+        }
+    }
+}
+
+// One warp per 128-element block, kQuantUnroll blocks per warp per pass: lane
+// l holds elements 4l..4l+3 of each block.  scale = amax / 127 (float
+// division), code = nearest-even integer of x / scale, clamped to +-127.
+template <bool BF16>
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_shard_blocks(const uint2 *__restrict__ x, uint32_t *__restrict__ q, float *__restrict__ scales,
+                      long long n_blocks) {
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (kQuantThreads / 32);
+    const long long w0 = (long long)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
+    for (long long base = w0; base < n_blocks; base += warps * kQuantUnroll) {
+        uint2 raw[kQuantUnroll];
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const long long b = base + u * warps;
+            raw[u] = b < n_blocks ? __ldcs(x + b * 32 + lane) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const long long b = base + u * warps;
+            if (b >= n_blocks) break;  // uniform across the warp
+            float v[4];
+            from_lp4<BF16>(raw[u], v);
+            float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            const float scale = __fdiv_rn(amax, 127.0f);
+            uint32_t packed = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                int c = 0;
+                if (scale > 0.0f) {
+                    c = __float2int_rn(__fdiv_rn(v[k], scale));
+                    c = c > 127 ? 127 : (c < -127 ? -127 : c);
+                }
+                packed |= (uint32_t)(c & 0xff) << (8 * k);
+            }
+            __stcs(q + b * 32 + lane, packed);
+            if (lane == 0) scales[b] = scale;
+        }
+    }
+}
+
+template <int MAXN>
+struct DequantGatherParams {
+    const uint4 *codes[MAXN];   // rank j's codes at this unit's offset (16 per uint4)
+    const float *scales[MAXN];  // rank j's scales at this unit's first block
+    uint4 *out;                 // 8 lp per uint4
+    long long vec_per_shard;    // shard_len / 16
+    long long n_items;          // n * vec_per_shard
+};
+
+// out[j * shard + k] = lp(code_j[k] * scale_j[k / 128]); a thread takes
+// kQuantUnroll items of 16 codes (one load each, all issued before any use).
+template <int MAXN, bool BF16>
+__global__ void __launch_bounds__(kQuantThreads)
+gather_dequant(const __grid_constant__ DequantGatherParams<MAXN> p) {
+    const long long stride = (long long)gridDim.x * kQuantThreads;
+    for (long long i0 = (long long)blockIdx.x * kQuantThreads + threadIdx.x; i0 < p.n_items;
+         i0 += stride * kQuantUnroll) {
+        uint4 c[kQuantUnroll];
+        float sc[kQuantUnroll];
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const long long i = i0 + u * stride;
+            if (i < p.n_items) {
+                const long long j = i / p.vec_per_shard;
+                const long long k16 = i - j * p.vec_per_shard;
+                c[u] = ld_stream16(p.codes[j] + k16);
+                sc[u] = __ldg(p.scales[j] + (k16 >> 3));  // 16 codes lie in one 128-block
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const long long i = i0 + u * stride;
+            if (i >= p.n_items) break;
+            const uint32_t w[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                float y[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    y[k] = __fmul_rn((float)(int8_t)((w[t] >> (8 * k)) & 0xff), sc[u]);
+                o[2 * t] = to_lp2<BF16>(y[0], y[1]);
+                o[2 * t + 1] = to_lp2<BF16>(y[2], y[3]);
+            }
+            __stcs(p.out + 2 * i, make_uint4(o[0], o[1], o[2], o[3]));
+            __stcs(p.out + 2 * i + 1, make_uint4(o[4], o[5], o[6], o[7]));
+        }
+    }
+}
+
+template <typename K>
+int blocks_per_sm(K kernel) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kQuantThreads, 0) != cudaSuccess) b = 1;
+    return b < 1 ? 1 : b;
+}
+
+template <int MAXN, bool BF16>
+cudaError_t dequant_gather_impl(const int8_t *const *codes, const float *const *scales, int n,
+                                int64_t offset, int64_t shard_len, void *out, cudaStream_t stream) {
+    DequantGatherParams<MAXN> p;
+    for (int j = 0; j < n; ++j) {
+        p.codes[j] = reinterpret_cast<const uint4 *>(codes[j] + offset);
+        p.scales[j] = scales[j] + offset / 128;
+    }
+    for (int j = n; j < MAXN; ++j) {
+        p.codes[j] = nullptr;
+        p.scales[j] = nullptr;
+    }
+    p.out = static_cast<uint4 *>(out);
+    p.vec_per_shard = shard_len / 16;
+    p.n_items = p.vec_per_shard * n;
+    if (p.n_items == 0) return cudaSuccess;
+    static const int occ = blocks_per_sm(gather_dequant<MAXN, BF16>);
+    long long grid = (long long)sm_count() * occ;
+    const long long need = (p.n_items + kQuantThreads * kQuantUnroll - 1) / (kQuantThreads * kQuantUnroll);
+    if (grid > need) grid = need;
+    gather_dequant<MAXN, BF16><<<(unsigned)grid, kQuantThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t quantize_impl(const void *shard, int64_t len, int8_t *codes, float *scales, cudaStream_t stream) {
+    const long long blocks = len / 128;
+    if (blocks == 0) return cudaSuccess;
+    static const int occ = blocks_per_sm(quantize_shard_blocks<BF16>);
+    long long grid = (long long)sm_count() * occ;
+    const long long per_cta = (kQuantThreads / 32) * kQuantUnroll;
+    const long long need = (blocks + per_cta - 1) / per_cta;
+    if (grid > need) grid = need;
+    quantize_shard_blocks<BF16><<<(unsigned)grid, kQuantThreads, 0, stream>>>(
+        static_cast<const uint2 *>(shard), reinterpret_cast<uint32_t *>(codes), scales, blocks);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const void *shard, int lp, int64_t len, int8_t *codes, float *scales,
+                            cudaStream_t stream) {
+    return lp ? quantize_impl<true>(shard, len, codes, scales, stream)
+              : quantize_impl<false>(shard, len, codes, scales, stream);
+}
+
+cudaError_t launch_dequant_gather(const int8_t *const *codes, const float *const *scales, int n, int lp,
+                                  int64_t offset, int64_t shard_len, void *out, cudaStream_t stream) {
+    if (n <= 64)
+        return lp ? dequant_gather_impl<64, true>(codes, scales, n, offset, shard_len, out, stream)
+                  : dequant_gather_impl<64, false>(codes, scales, n, offset, shard_len, out, stream);
+    return lp ? dequant_gather_impl<1024, true>(codes, scales, n, offset, shard_len, out, stream)
+              : dequant_gather_impl<1024, false>(codes, scales, n, offset, shard_len, out, stream);
+}
+
+}  // namespace zk

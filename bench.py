@@ -208,46 +208,61 @@ class Run:
         else:
             self.buckets = 1 if P else 0
 
-    def launches_per_step(self):
-        n = len(self.ranks)
-        gathers = 2 * self.plan.n_units if self.gather_shards is not None else 0
-        return n * self.buckets + 1 + n + gathers + (n if self.quantized else 0)
+    def calls(self, stream, slice_lists=None):
+        """The step as an ordered list of (kind, algorithmic HBM bytes, kernel
+        launches, callable).  Stage 3 follows the pages' order: forward gathers
+        of every unit, then per unit in reverse order its backward gather and
+        its reduce-scatter, then the local update."""
+        w, P = self.w, self.P
+        lists = slice_lists or self.slice_lists
+        out = []
+        red_b = 2 * w.n_ranks + 4
+        if self.gather_shards is not None:
+            units = list(range(self.plan.n_units))
+            gb = self.gather_bytes_per_element()
 
-    def gathers(self, stream, events=None):
-        if self.gather_shards is None:
-            return
-        units = list(range(self.plan.n_units))
-        for u in units + units[::-1]:        # forward, then backward
+            def gather(u):
+                if self.quantized:
+                    self.plan.gather_quantized(u, self.codes, self.scales, self.gather_out, stream)
+                else:
+                    self.plan.gather(u, self.gather_shards, self.gather_out, stream)
+            for u in units:
+                out.append(("gather", gb * int(self.plan.unit_padded[u]), 1, lambda u=u: gather(u)))
+            for u in units[::-1]:
+                out.append(("gather", gb * int(self.plan.unit_padded[u]), 1, lambda u=u: gather(u)))
+                for r in self.ranks:
+                    out.append(("reduce", red_b * self.plan.shard_len(u), 1,
+                                lambda u=u, r=r: self.plan.reduce_unit(r, u, lists[r], self.g[r],
+                                                                       self.S, stream)))
+        else:
+            launches = self.buckets * (self.plan.n_units if w.stage == 3 else 1)
+            for r in self.ranks:
+                out.append(("reduce", red_b * P, launches,
+                            lambda r=r: self.plan.reduce(r, lists[r], self.g[r], self.S,
+                                                         w.bucket_elems, stream)))
+        for i, r in enumerate(self.ranks):
+            out.append(("adam", 30 * P, 1 + (i == 0), lambda r=r: self._adam(r, stream)))
             if self.quantized:
-                self.plan.gather_quantized(u, self.codes, self.scales, self.gather_out, stream)
-            else:
-                self.plan.gather(u, self.gather_shards, self.gather_out, stream)
+                out.append(("quantize", int((3 + 4 / 128) * P), 1,
+                            lambda r=r: self.plan.quantize(self.shard[r], self.codes[r],
+                                                           self.scales[r], stream)))
+        return out
 
-    def reduce(self, stream):
-        for r in self.ranks:
-            self.plan.reduce(r, self.slice_lists[r], self.g[r], self.S, self.w.bucket_elems, stream)
-
-    def adam(self, stream):
+    def _adam(self, r, stream):
         w = self.w
-        for r in self.ranks:
-            out = self.shard[r] if w.stage == 3 else self.param
-            self.plan.adam(r, self.g[r], self.master[r], self.m[r], self.v[r], out, w.lr, w.beta1,
-                           w.beta2, w.eps, w.wd, int(w.adamw), self.S, w.clip, 0.0, 0, stream)
-            if self.quantized:   # the updated shard, ready for the next step's gathers
-                self.plan.quantize(self.shard[r], self.codes[r], self.scales[r], stream)
+        out = self.shard[r] if w.stage == 3 else self.param
+        self.plan.adam(r, self.g[r], self.master[r], self.m[r], self.v[r], out, w.lr, w.beta1,
+                       w.beta2, w.eps, w.wd, int(w.adamw), self.S, w.clip, 0.0, 0, stream)
+
+    def launches_per_step(self):
+        return sum(c[2] for c in self.calls(0))
 
     def gather_bytes_per_element(self):
         # lp gather: 2 B in + 2 B out; quantized: 1 B code + 4/128 B scale in, 2 B out
         return (3 + 4 / 128) if self.quantized else 4
 
     def bytes_per_step(self):
-        b = bytes_per_element(self.w.n_ranks)
-        step = b["step"] * self.P * len(self.ranks)
-        if self.gather_shards is not None:
-            step += 2 * self.gather_bytes_per_element() * int(sum(self.plan.unit_padded))
-        if self.quantized:
-            step += (3 + 4 / 128) * self.P * len(self.ranks)
-        return int(step)
+        return int(sum(c[1] for c in self.calls(0)))
 
 
 def dist_setup(n_gpus):
@@ -378,24 +393,22 @@ def main():
     stream = torch.cuda.current_stream()
     sh = int(stream.cuda_stream)
 
+    calls = run.calls(sh)
+    kinds = sorted({c[0] for c in calls})
+
     def step(evs=None):
         if evs is not None:
             evs[0].record(stream)
-        run.gathers(sh)
-        if evs is not None:
-            evs[1].record(stream)
-        run.reduce(sh)
-        if evs is not None:
-            evs[2].record(stream)
-        run.adam(sh)
-        if evs is not None:
-            evs[3].record(stream)
+        for i, c in enumerate(calls):
+            c[3]()
+            if evs is not None:
+                evs[i + 1].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(enabled=not args.no_clocks)
@@ -420,40 +433,37 @@ def main():
     res = run.plan.result()
     if res["skipped"]:
         log("warning: a timed step was skipped (overflow)")
-    gather_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    reduce_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    adam_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    # per kind: time per step (sum of its calls), bytes per step, launches per step
+    t_kind = {k: 0.0 for k in kinds}
+    for e in evs:
+        for i, c in enumerate(calls):
+            t_kind[c[0]] += e[i].elapsed_time(e[i + 1])
+    t_kind = {k: v / K for k, v in t_kind.items()}
+    b_kind = {k: sum(c[1] for c in calls if c[0] == k) for k in kinds}
+    n_kind = {k: sum(1 for c in calls if c[0] == k) for k in kinds}
     ms_per_step = total_ms / K
     elems = run.P * len(run.ranks)
     value = elems * ws / (ms_per_step / 1e3)
     peak, peak_kind = load_peaks()
     b = bytes_per_element(w.n_ranks)
-    n_part = len(run.ranks)
-    per_call_ms = {"reduce": statistics.mean(reduce_ms) / n_part,
-                   "adam": statistics.mean(adam_ms) / n_part}
-    kernel_bytes = {"reduce": b["reduce"] * run.P, "adam": b["adam"] * run.P}
-    if run.gather_shards is not None:
-        n_gathers = 2 * run.plan.n_units
-        per_call_ms["gather"] = statistics.mean(gather_ms) / n_gathers
-        kernel_bytes["gather"] = (run.gather_bytes_per_element() * int(sum(run.plan.unit_padded))
-                                  / run.plan.n_units)
     # dominant kernel = the one with the largest share of the step
-    share = {"reduce": statistics.mean(reduce_ms), "adam": statistics.mean(adam_ms)}
-    if run.gather_shards is not None:
-        share["gather"] = statistics.mean(gather_ms)
-    dom = max(share, key=share.get)
+    dom = max(t_kind, key=t_kind.get)
     kname = {"reduce": "reduce_unscale_stats", "adam": "adam_fused_cast",
-             "gather": "gather_dequant" if run.quantized else "gather_layer_tma"}[dom]
-    achieved = kernel_bytes[dom] / (per_call_ms[dom] / 1e3) / 1e9
+             "gather": "gather_dequant" if run.quantized else "gather_layer_tma",
+             "quantize": "quantize_shard_blocks"}[dom]
+    achieved = b_kind[dom] / (t_kind[dom] / 1e3) / 1e9
     step_gbs = run.bytes_per_step() / (ms_per_step / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": traffic_for(kname, w.name),
-                "algorithmic_bytes_per_launch": kernel_bytes[dom],
-                "avg_launch_ms": per_call_ms[dom]}
-    kernels = {k: {"avg_ms": per_call_ms[k], "GBps": kernel_bytes[k] / (per_call_ms[k] / 1e3) / 1e9,
-                   "frac_of_peak": kernel_bytes[k] / (per_call_ms[k] / 1e3) / 1e9 / peak}
-               for k in per_call_ms}
+                "algorithmic_bytes_per_launch": b_kind[dom] / n_kind[dom],
+                "avg_launch_ms": t_kind[dom] / n_kind[dom],
+                "launches_per_step": n_kind[dom]}
+    kernels = {k: {"calls_per_step": n_kind[k], "avg_ms": t_kind[k] / n_kind[k],
+                   "ms_per_step": t_kind[k], "share": t_kind[k] / ms_per_step,
+                   "GBps": b_kind[k] / (t_kind[k] / 1e3) / 1e9,
+                   "frac_of_peak": b_kind[k] / (t_kind[k] / 1e3) / 1e9 / peak}
+               for k in kinds}
 
     # ---- end to end through the ABI, host buffers, copies inside the timed region
     e2e = None
@@ -532,19 +542,19 @@ def measure_e2e(run, steps, stream, sh, ws, dist, dev):
     h2d = sum(int(t.numel()) * t.element_size() for t in host.values())
     host_lists = {r: [host[r][j] for j in range(run.w.n_ranks)] for r in run.ranks}
 
+    staged_calls = run.calls(sh)
+    direct_calls = run.calls(sh, slice_lists=host_lists)
+
     def staged():
         for r in run.ranks:
             run.slices[r].copy_(host[r], non_blocking=True)
-        run.gathers(sh)
-        run.reduce(sh)
-        run.adam(sh)
+        for c in staged_calls:
+            c[3]()
         return run.plan.result()          # synchronises and reads the record
 
     def direct():
-        run.gathers(sh)
-        for r in run.ranks:
-            run.plan.reduce(r, host_lists[r], run.g[r], run.S, run.w.bucket_elems, sh)
-        run.adam(sh)
+        for c in direct_calls:
+            c[3]()
         return run.plan.result()
 
     def timed(fn):

@@ -151,7 +151,8 @@ zero_status zero_plan_set_spin_limit(zero_plan *plan, int64_t polls);
  * partial sums of grad_out^2 that feed the global norm.
  * grad_out: P floats (device).  bucket_elems: reduce in buckets of this many
  * elements (rounded up to a whole number of 32768-element norm tiles, so
- * results are bit-identical for every bucket size); 0 = one bucket.
+ * results are bit-identical for every bucket size); 0 = one bucket.  In
+ * stage 3 buckets and tiles are counted within each unit's shard.
  * The first reduce after a step's Adam call starts a new step; every
  * partition reduced before the next zero_adam_step joins that step's norm
  * and overflow decision.  Stage 0: rank must be 0, slices hold Ψ_p elements.
@@ -160,6 +161,18 @@ zero_status zero_reduce_partition(zero_plan *plan, int32_t rank,
                                   const void *const *grad_slices,
                                   float *grad_out, float loss_scale,
                                   int64_t bucket_elems, void *stream);
+
+/* Stage 3: reduce only unit `unit`'s shard of rank `rank`'s partition ("10.6
+ * ZeRO 与 FSDP" §10.6.4 backward step 4: each layer's gradients are
+ * reduce-scattered as soon as the layer's backward is done, in reverse layer
+ * order).  Same arguments and arithmetic as zero_reduce_partition (the
+ * slices and grad_out are whole-partition buffers; only the unit's range is
+ * read and written); the unit joins the current step like a partition.  The
+ * norm's tiles restart at every unit, so reducing the units one by one, in
+ * any order, gives exactly the bits of one zero_reduce_partition call. */
+zero_status zero_reduce_unit(zero_plan *plan, int32_t rank, int32_t unit,
+                             const void *const *grad_slices, float *grad_out,
+                             float loss_scale, void *stream);
 
 /* Local result of the reduces of the current step: sum of squares (fp64)
  * and overflow flag, for exchanging with other real ranks (pass the others'

@@ -363,3 +363,49 @@ def test_reduce_reads_pinned_host_slices(zlib, lp):
         plan.close()
     assert same_floats(out[0][0].cpu().numpy(), out[1][0].cpu().numpy())
     assert out[0][1] == out[1][1]
+
+
+@pytest.mark.parametrize("lp", [0, 1])
+def test_stage3_unit_by_unit_reduce_equals_partition_reduce(zlib, lp):
+    # backward order: each unit reduce-scattered on its own, last unit first;
+    # norm tiles restart per unit, so the bits equal one whole-partition call
+    dev = torch.device("cuda")
+    n = 4
+    sizes, units = [70_000, 5, 33_000, 100_000, 7, TILE * 2], [0, 0, 1, 2, 3, 4]
+    res = []
+    for mode in ("partition", "units"):
+        plan = _plan(-1, n, lp, stage=3, align=8, sizes=sizes, units=units)
+        P = plan.part_len
+        sl = [synth.grad_slice(P, lp, 1e-2, 1.0, 4, 1, j, 1, dev) for j in range(n)]
+        g = torch.full((P,), float("nan"), dtype=torch.float32, device=dev)
+        if mode == "partition":
+            plan.reduce(1, sl, g, 1.0)
+        else:
+            for u in reversed(range(plan.n_units)):
+                plan.reduce_unit(1, u, sl, g, 1.0)
+        res.append((g.cpu().numpy(), plan.stats(), [synth.to_numpy_codes(t) for t in sl]))
+        plan.close()
+    assert same_floats(res[0][0], res[1][0])
+    assert res[0][1] == res[1][1]
+    og, oss, oof = oracle.reduce(res[0][2], lp, 1.0)
+    assert same_floats(res[0][0], og) and oof == res[0][1][1]
+    assert abs(res[0][1][0] - oss) <= 1e-9 * oss
+
+
+def test_partly_reduced_partition_counts_only_its_part(zlib):
+    # a unit reduced alone contributes only its own tiles to the step's norm
+    dev = torch.device("cuda")
+    n = 2
+    plan = _plan(-1, n, 0, stage=3, align=8, sizes=[50_000, 60_000], units=[0, 1])
+    P = plan.part_len
+    sl = [synth.grad_slice(P, 0, 1e-2, 1.0, 6, 1, j, 0, dev) for j in range(n)]
+    g = torch.zeros(P, dtype=torch.float32, device=dev)
+    plan.reduce(0, sl, g, 1.0)                       # step 1: everything
+    w = torch.zeros(P, device=dev); m = torch.zeros(P, device=dev); v = torch.zeros(P, device=dev)
+    plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 0.0)
+    plan.reduce_unit(0, 1, sl, g, 1.0)              # step 2: unit 1 only
+    ss, _ = plan.stats()
+    off = plan.unit_shard_offset(1)
+    _, oss, _ = oracle.reduce([synth.to_numpy_codes(t[off:]) for t in sl], 0, 1.0)
+    assert abs(ss - oss) <= 1e-9 * oss
+    plan.close()

@@ -643,7 +643,7 @@ cudaError_t reduce_impl(const void *const *slices, int n, int64_t offset, int64_
         p.src[j] = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(slices[j]) + offset);
     for (int j = n; j < MAXN; ++j) p.src[j] = nullptr;
     p.g = reinterpret_cast<float4 *>(g + offset);
-    p.partials = partials + offset / kTile;
+    p.partials = partials;
     p.overflow = overflow;
     p.len = len;
     p.inv = inv;

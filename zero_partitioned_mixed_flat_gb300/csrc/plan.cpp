@@ -55,6 +55,10 @@ struct zero_plan {
     std::vector<int32_t> unit_of;
     std::vector<int64_t> unit_off, unit_pad;  // unit_off has n_units + 1 entries
     int64_t tiles_per_part = 0;
+    // norm tiles restart at every unit's shard (one unit unless stage 3), so a
+    // unit reduced alone gives the same bits as the whole partition
+    std::vector<int64_t> unit_tile_base;  // first tile of each unit's shard
+    std::vector<int64_t> unit_part_off;   // each unit's shard offset in the partition
     int32_t slots = 1;  // partition slots with partial sums (N, or 1 for DDP)
     // device scratch (allocated on first device call)
     int device = -1;
@@ -106,7 +110,17 @@ zero_status build_layout(zero_plan *p) {
     p->psi_p = flat;
     p->part = p->stage == 0 ? flat : flat / p->n_ranks;
     p->slots = p->stage == 0 ? 1 : p->n_ranks;
-    p->tiles_per_part = (p->part + zk::kTile - 1) / zk::kTile;
+    p->unit_tile_base.assign(p->unit_pad.size(), 0);
+    p->unit_part_off.assign(p->unit_pad.size(), 0);
+    int64_t tiles = 0, off = 0;
+    for (size_t u = 0; u < p->unit_pad.size(); ++u) {
+        p->unit_tile_base[u] = tiles;
+        p->unit_part_off[u] = off;
+        const int64_t shard = p->shard_len(int32_t(u));
+        tiles += (shard + zk::kTile - 1) / zk::kTile;
+        off += shard;
+    }
+    p->tiles_per_part = tiles;
     return ZERO_OK;
 }
 
@@ -343,10 +357,15 @@ zero_status zero_plan_set_state(zero_plan *p, int64_t step, int32_t good_steps) 
     return ZERO_OK;
 }
 
-zero_status zero_reduce_partition(zero_plan *p, int32_t rank, const void *const *grad_slices,
-                                  float *grad_out, float loss_scale, int64_t bucket_elems,
-                                  void *stream) {
-    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+}  // extern "C"
+
+namespace {
+
+// Validation, pointer classification and (on the first reduce of a step) the
+// step reset shared by zero_reduce_partition and zero_reduce_unit.
+zero_status begin_reduce(zero_plan *p, int32_t rank, const void *const *grad_slices, float *grad_out,
+                         float loss_scale, int64_t bucket_elems, cudaStream_t s,
+                         std::vector<const void *> *src) {
     zero_status st = check_rank(p, rank);
     if (st != ZERO_OK) return st;
     if (!grad_slices || (!grad_out && p->part > 0)) return fail(ZERO_EINVAL, "NULL slices or output");
@@ -360,34 +379,80 @@ zero_status zero_reduce_partition(zero_plan *p, int32_t rank, const void *const 
     if (!aligned16(grad_out)) return fail(ZERO_EALIGN, "grad_out is not 16-byte aligned");
     st = ensure_device(p);
     if (st != ZERO_OK) return st;
-    std::vector<const void *> src(size_t(p->n_ranks), nullptr);
+    src->assign(size_t(p->n_ranks), nullptr);
     if (p->part > 0)
         for (int32_t j = 0; j < p->n_ranks; ++j) {
-            st = readable_by_device(grad_slices[j], p->device, "grad_slices", j, &src[size_t(j)]);
+            st = readable_by_device(grad_slices[j], p->device, "grad_slices", j, &(*src)[size_t(j)]);
             if (st != ZERO_OK) return st;
         }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->phase != kReducing) {
-        // a new step: forget the previous step's partitions and overflow
+        // a new step: forget the previous step's partitions, partial sums and
+        // overflow (a partition reduced only in part then adds only that part)
         std::memset(p->active, 0, sizeof p->active);
         p->use_global = false;
         cudaError_t e = cudaMemsetAsync(&p->d_rec->overflow, 0, sizeof(unsigned), s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(overflow)");
+        if (p->tiles_per_part > 0) {
+            e = cudaMemsetAsync(p->d_partials, 0, size_t(p->slots) * size_t(p->tiles_per_part) * sizeof(double), s);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(partials)");
+        }
         p->phase = kReducing;
     }
-    const int32_t slot = p->stage == 0 ? 0 : rank;
-    p->active[slot >> 6] |= uint64_t(1) << (slot & 63);
+    return ZERO_OK;
+}
+
+// Reduce unit u's range of the partition (the whole partition when there is
+// one unit), in buckets of whole norm tiles counted from the unit's start.
+zero_status reduce_unit_range(zero_plan *p, int32_t slot, int32_t u, const void *const *src, float *grad_out,
+                              float loss_scale, int64_t bucket_elems, cudaStream_t s) {
+    const int64_t shard = p->shard_len(u);
+    const int64_t base = p->unit_part_off[size_t(u)];
     const float inv = float(1.0 / (double(loss_scale) * double(p->n_ranks)));
-    double *partials = p->d_partials + int64_t(slot) * p->tiles_per_part;
-    int64_t bucket = bucket_elems == 0 ? p->part : round_up(bucket_elems, zk::kTile);
-    if (bucket <= 0) bucket = p->part;
-    for (int64_t b0 = 0; b0 < p->part; b0 += bucket) {
-        const int64_t len = std::min(bucket, p->part - b0);
-        cudaError_t e = zk::launch_reduce(src.data(), p->n_ranks, p->lp, p->reduce_lp_accum, b0, len,
-                                          inv, grad_out, partials, &p->d_rec->overflow, s);
+    double *partials = p->d_partials + int64_t(slot) * p->tiles_per_part + p->unit_tile_base[size_t(u)];
+    int64_t bucket = bucket_elems == 0 ? shard : round_up(bucket_elems, zk::kTile);
+    if (bucket <= 0) bucket = shard;
+    for (int64_t b0 = 0; b0 < shard; b0 += bucket) {
+        const int64_t len = std::min(bucket, shard - b0);
+        cudaError_t e = zk::launch_reduce(src, p->n_ranks, p->lp, p->reduce_lp_accum, base + b0, len, inv,
+                                          grad_out, partials + b0 / zk::kTile, &p->d_rec->overflow, s);
         if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
     }
     return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+zero_status zero_reduce_partition(zero_plan *p, int32_t rank, const void *const *grad_slices,
+                                  float *grad_out, float loss_scale, int64_t bucket_elems,
+                                  void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::vector<const void *> src;
+    zero_status st = begin_reduce(p, rank, grad_slices, grad_out, loss_scale, bucket_elems, s, &src);
+    if (st != ZERO_OK) return st;
+    const int32_t slot = p->stage == 0 ? 0 : rank;
+    p->active[slot >> 6] |= uint64_t(1) << (slot & 63);
+    for (int32_t u = 0; u < p->n_units(); ++u) {
+        st = reduce_unit_range(p, slot, u, src.data(), grad_out, loss_scale, bucket_elems, s);
+        if (st != ZERO_OK) return st;
+    }
+    return ZERO_OK;
+}
+
+zero_status zero_reduce_unit(zero_plan *p, int32_t rank, int32_t unit, const void *const *grad_slices,
+                             float *grad_out, float loss_scale, void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (p->stage != 3) return fail(ZERO_EINVAL, "zero_reduce_unit needs a stage-3 plan");
+    if (unit < 0 || unit >= p->n_units()) return fail(ZERO_EINVAL, "unit %d outside [0, %d)", unit, p->n_units());
+    std::vector<const void *> src;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    zero_status st = begin_reduce(p, rank, grad_slices, grad_out, loss_scale, 0, s, &src);
+    if (st != ZERO_OK) return st;
+    const int32_t slot = rank;
+    p->active[slot >> 6] |= uint64_t(1) << (slot & 63);
+    return reduce_unit_range(p, slot, unit, src.data(), grad_out, loss_scale, 0, s);
 }
 
 zero_status zero_partition_stats(zero_plan *p, double *sumsq, int32_t *overflow, void *stream) {

@@ -27,15 +27,25 @@ __device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
     return r;
 }
 
+// two floats -> two lp values in one packed conversion (each rounded to
+// nearest, ties to even, as a separate conversion would)
 template <bool BF16>
-__device__ __forceinline__ uint32_t to_lp2(float a, float b) {
+__device__ __forceinline__ uint32_t to_lp2_packed(float a, float b) {
     if constexpr (BF16) {
-        return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
-               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
     } else {
-        return uint32_t(__half_as_ushort(__float2half_rn(a))) |
-               (uint32_t(__half_as_ushort(__float2half_rn(b))) << 16);
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
     }
+}
+
+// byte k of w (a signed code) as an exact float without the conversion unit:
+// w ^ 0x80808080 holds code + 128 in each byte; one byte permute places it in
+// the low mantissa bits of 2^23, and subtracting 2^23 + 128 is exact.
+__device__ __forceinline__ float code_to_float(uint32_t biased, int k) {
+    const uint32_t bits = __byte_perm(biased, 0x4B000000u, 0x7540u + (uint32_t)k);
+    return __fsub_rn(__uint_as_float(bits), 8388736.0f);
 }
 
 template <bool BF16>
@@ -130,16 +140,16 @@ gather_dequant(const __grid_constant__ DequantGatherParams<MAXN> p) {
         for (int u = 0; u < kQuantUnroll; ++u) {
             const long long i = i0 + u * stride;
             if (i >= p.n_items) break;
-            const uint32_t w[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+            const uint32_t w[4] = {c[u].x ^ 0x80808080u, c[u].y ^ 0x80808080u,
+                                   c[u].z ^ 0x80808080u, c[u].w ^ 0x80808080u};
             uint32_t o[8];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 float y[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    y[k] = __fmul_rn((float)(int8_t)((w[t] >> (8 * k)) & 0xff), sc[u]);
-                o[2 * t] = to_lp2<BF16>(y[0], y[1]);
-                o[2 * t + 1] = to_lp2<BF16>(y[2], y[3]);
+                for (int k = 0; k < 4; ++k) y[k] = __fmul_rn(code_to_float(w[t], k), sc[u]);
+                o[2 * t] = to_lp2_packed<BF16>(y[0], y[1]);
+                o[2 * t + 1] = to_lp2_packed<BF16>(y[2], y[3]);
             }
             __stcs(p.out + 2 * i, make_uint4(o[0], o[1], o[2], o[3]));
             __stcs(p.out + 2 * i + 1, make_uint4(o[4], o[5], o[6], o[7]));

@@ -32,6 +32,9 @@ int sm_count();
 // message for zero_last_error() on the calling thread
 void set_last_error(const char *msg);
 
+// Reduce elements [offset, offset + len) of the slices into g[offset ...);
+// partials receives the sums of squares of the bucket's tiles (tile t of the
+// bucket -> partials[t]); overflow is OR-ed.
 cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp,
                           int64_t offset, int64_t len, float inv, float *g,
                           double *partials, unsigned *overflow,

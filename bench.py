@@ -74,22 +74,28 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {"reduce_unscale_stats": "kernels.cu", "norm_finalize_decide": "kernels.cu",
+                  "adam_fused_cast": "kernels.cu", "gather_layer_tma": "kernels.cu",
+                  "gather_dequant": "quant.cu", "quantize_shard_blocks": "quant.cu"}
+
+
+def source_hash(fname):
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "zero_partitioned_mixed_flat_gb300", "csrc", "kernels.cu"), "rb") as f:
+    with open(os.path.join(ROOT, "zero_partitioned_mixed_flat_gb300", "csrc", fname), "rb") as f:
         h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def traffic_for(kernel: str, workload: str):
-    """Per-launch DRAM bytes from the committed ncu summary, only while the
-    kernel source is unchanged since the counters were taken."""
+    """Per-launch DRAM bytes (read + write) from the committed ncu summary,
+    only while the kernel's source file is unchanged since the counters were
+    taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d[workload][kernel]
-        if e.get("kernels_cu_sha256_16") != kernel_source_hash():
+        if e.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel]):
             return None
         return e.get("dram_bytes_per_launch")
     except Exception:

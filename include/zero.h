@@ -150,7 +150,7 @@ zero_status zero_plan_set_spin_limit(zero_plan *plan, int64_t polls);
  * and, over the partition, the overflow flag (any s not finite) and the
  * partial sums of grad_out^2 that feed the global norm.
  * grad_out: P floats (device).  bucket_elems: reduce in buckets of this many
- * elements (rounded up to a whole number of 32768-element norm tiles, so
+ * elements (rounded up to a whole number of 4096-element norm tiles, so
  * results are bit-identical for every bucket size); 0 = one bucket.  In
  * stage 3 buckets and tiles are counted within each unit's shard.
  * The first reduce after a step's Adam call starts a new step; every
@@ -301,7 +301,7 @@ zero_status zero_gather_layer_quantized(zero_plan *plan, int32_t unit,
  * every other call.  Asynchronous on `stream`.
  */
 #define ZERO_NOALLOC_MAX_ELEMS (8192LL * 32768LL)
-#define ZERO_NOALLOC_SCRATCH_BYTES (8192 * 8 + 256)
+#define ZERO_NOALLOC_SCRATCH_BYTES (65536 * 8 + 256)
 zero_status zero_reduce_partition_noalloc(int32_t n_ranks, zero_lp lp,
                                           const void *const *grad_slices,
                                           int64_t len, float loss_scale,

@@ -18,7 +18,7 @@ from zero_partitioned_mixed_flat_gb300.workloads import WORKLOADS, Workload
 from .zstep import Harness, same_floats
 
 pytestmark = pytest.mark.gpu
-TILE = 32768
+TILE = 4096
 
 
 def _plan(psi, n, lp, stage=1, align=8, sizes=None, units=None):

@@ -26,7 +26,7 @@
 namespace zk {
 namespace {
 
-constexpr int kReduceThreads = 256;
+constexpr int kReduceThreads = 128;
 constexpr int kVec = 8;  // lp elements per 16-byte vector
 constexpr int kTileIters = int(kTile / (kReduceThreads * kVec));
 constexpr int kBatch = 16;  // slices loaded before they are added
@@ -189,11 +189,42 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
 
 // ------------------------------------------------------------------ K2 decide
 
-struct DecideParams {
+struct ChunkSumParams {
     const double *partials;
+    double *level2;
     long long tiles_per_slot;
-    unsigned long long mask[1024 / 64];
-    int n_slots;
+    int chunks_per_slot;
+    short slots[1024];  // the step's reduced partition slots, ascending
+};
+
+constexpr int kChunkThreads = 256;
+
+// First level of the norm: block `item` sums one fixed chunk of one reduced
+// partition's tile partials (strided per thread, xor tree, warps in order).
+__global__ void __launch_bounds__(kChunkThreads)
+partial_chunk_sums(const __grid_constant__ ChunkSumParams p) {
+    __shared__ double wsum[kChunkThreads / 32];
+    const int item = blockIdx.x;
+    const int slot = p.slots[item / p.chunks_per_slot];
+    const long long t0 = (long long)(item % p.chunks_per_slot) * kPartialChunk;
+    const long long t1 = t0 + kPartialChunk < p.tiles_per_slot ? t0 + kPartialChunk : p.tiles_per_slot;
+    const double *q = p.partials + (long long)slot * p.tiles_per_slot;
+    double acc = 0.0;
+    for (long long t = t0 + threadIdx.x; t < t1; t += kChunkThreads) acc = __dadd_rn(acc, q[t]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < kChunkThreads / 32; ++w) t = __dadd_rn(t, wsum[w]);
+        p.level2[item] = t;
+    }
+}
+
+struct DecideParams {
+    const double *level2;
+    int n_items;
     double remote_sumsq;
     double global_sumsq;
     int remote_overflow;
@@ -209,12 +240,7 @@ __global__ void __launch_bounds__(kDecideThreads)
 norm_finalize_decide(const __grid_constant__ DecideParams p) {
     __shared__ double wsum[kDecideThreads / 32];
     double acc = 0.0;
-    for (int r = 0; r < p.n_slots; ++r) {
-        if (!((p.mask[r >> 6] >> (r & 63)) & 1ull)) continue;
-        const double *q = p.partials + (long long)r * p.tiles_per_slot;
-        for (long long t = threadIdx.x; t < p.tiles_per_slot; t += kDecideThreads)
-            acc = __dadd_rn(acc, q[t]);
-    }
+    for (int t = threadIdx.x; t < p.n_items; t += kDecideThreads) acc = __dadd_rn(acc, p.level2[t]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
@@ -648,10 +674,8 @@ cudaError_t reduce_impl(const void *const *slices, int n, int64_t offset, int64_
     p.len = len;
     p.inv = inv;
     p.n = n;
-    static const int occ = occupancy(reduce_unscale_stats<MAXN, BF16, ACC_LP>, kReduceThreads, 0);
-    const long long tiles = (len + kTile - 1) / kTile;
-    long long grid = (long long)sm_count() * occ;
-    if (grid > tiles) grid = tiles;
+    // one tile per CTA: the block scheduler balances the tiles over the SMs
+    const long long grid = (len + kTile - 1) / kTile;
     if (grid < 1) return cudaSuccess;
     reduce_unscale_stats<MAXN, BF16, ACC_LP><<<(unsigned)grid, kReduceThreads, 0, stream>>>(p);
     return cudaGetLastError();
@@ -729,15 +753,29 @@ cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp, 
     return reduce_dispatch<1024>(slices, n, lp, acc_lp != 0, offset, len, inv, g, partials, overflow, stream);
 }
 
-cudaError_t launch_decide(const double *partials, int64_t tiles_per_slot, const uint64_t *active_mask,
-                          int n_slots, double remote_sumsq, int remote_overflow, int use_global,
-                          double global_sumsq, float clip, float loss_scale, int growth_interval,
-                          float beta1, float beta2, StepRecord *rec, cudaStream_t stream) {
+cudaError_t launch_decide(const double *partials, double *level2, int64_t tiles_per_slot,
+                          const uint64_t *active_mask, int n_slots, double remote_sumsq, int remote_overflow,
+                          int use_global, double global_sumsq, float clip, float loss_scale,
+                          int growth_interval, float beta1, float beta2, StepRecord *rec,
+                          cudaStream_t stream) {
+    ChunkSumParams c;
+    c.partials = partials;
+    c.level2 = level2;
+    c.tiles_per_slot = tiles_per_slot;
+    c.chunks_per_slot = (int)((tiles_per_slot + kPartialChunk - 1) / kPartialChunk);
+    if (c.chunks_per_slot < 1) c.chunks_per_slot = 1;
+    int active = 0;
+    for (int r = 0; r < n_slots; ++r)
+        if ((active_mask[r >> 6] >> (r & 63)) & 1u) c.slots[active++] = (short)r;
+    const int items = active * c.chunks_per_slot;
+    if (items > 0) {
+        partial_chunk_sums<<<items, kChunkThreads, 0, stream>>>(c);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     DecideParams p;
-    p.partials = partials;
-    p.tiles_per_slot = tiles_per_slot;
-    for (int i = 0; i < 1024 / 64; ++i) p.mask[i] = active_mask[i];
-    p.n_slots = n_slots;
+    p.level2 = level2;
+    p.n_items = items;
     p.remote_sumsq = remote_sumsq;
     p.remote_overflow = remote_overflow;
     p.use_global = use_global;

@@ -63,6 +63,7 @@ struct zero_plan {
     // device scratch (allocated on first device call)
     int device = -1;
     double *d_partials = nullptr;
+    double *d_level2 = nullptr;  // first-level sums of the partials
     zk::StepRecord *d_rec = nullptr;
     // step state (host)
     Phase phase = kIdle;
@@ -141,13 +142,19 @@ zero_status ensure_device(zero_plan *p) {
         cudaGetLastError();
         return fail(ZERO_ENOMEM, "cudaMalloc of %zu partial sums failed", n_part);
     }
+    const size_t n_level2 = size_t(p->slots) *
+                            size_t(std::max<int64_t>(1, (p->tiles_per_part + zk::kPartialChunk - 1) / zk::kPartialChunk));
     e = cudaMalloc(reinterpret_cast<void **>(&p->d_rec), sizeof(zk::StepRecord));
-    if (e != cudaSuccess) {
+    cudaError_t e2 = cudaMalloc(reinterpret_cast<void **>(&p->d_level2), n_level2 * sizeof(double));
+    if (e != cudaSuccess || e2 != cudaSuccess) {
         cudaFree(p->d_partials);
+        if (e == cudaSuccess) cudaFree(p->d_rec);
+        if (e2 == cudaSuccess) cudaFree(p->d_level2);
         p->d_partials = nullptr;
         p->d_rec = nullptr;
+        p->d_level2 = nullptr;
         cudaGetLastError();
-        return fail(ZERO_ENOMEM, "cudaMalloc of the step record failed");
+        return fail(ZERO_ENOMEM, "cudaMalloc of the step record or the norm scratch failed");
     }
     zk::StepRecord init;
     std::memset(&init, 0, sizeof init);
@@ -511,7 +518,7 @@ zero_status zero_adam_step(zero_plan *p, int32_t rank, const float *grad, float 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->phase == kReducing) {
         const int r_of = p->use_global ? (p->global_overflow ? 1 : 0) : (remote_overflow ? 1 : 0);
-        cudaError_t e = zk::launch_decide(p->d_partials, p->tiles_per_part, p->active, p->slots,
+        cudaError_t e = zk::launch_decide(p->d_partials, p->d_level2, p->tiles_per_part, p->active, p->slots,
                                           remote_sumsq, r_of, p->use_global ? 1 : 0,
                                           p->global_sumsq, clip, loss_scale, p->growth_interval,
                                           beta1, beta2, p->d_rec, s);
@@ -663,6 +670,7 @@ void zero_plan_destroy(zero_plan *p) {
         cudaSetDevice(p->device);
         cudaDeviceSynchronize();
         cudaFree(p->d_partials);
+        cudaFree(p->d_level2);
         cudaFree(p->d_rec);
         cudaSetDevice(cur);
     }

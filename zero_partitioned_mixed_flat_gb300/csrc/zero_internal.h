@@ -9,8 +9,13 @@ namespace zk {
 
 // Elements per norm tile.  Each tile's sum of squares is one fp64 partial,
 // computed by one CTA in a fixed order, so the global norm is the same for
-// every grid size and every bucket size (buckets are whole tiles).
-constexpr int64_t kTile = 32768;
+// every grid size and every bucket size (buckets are whole tiles).  Small
+// enough that one stage-3 unit shard spans several hundred tiles (one CTA
+// each), so a per-unit reduce fills the GPU.
+constexpr int64_t kTile = 4096;
+// Partials summed per first-level block of the norm (fixed, so the summation
+// tree of the norm is a function of the partition only).
+constexpr int64_t kPartialChunk = 4096;
 
 // Per-plan device record of the step decision and the optimizer step state.
 struct StepRecord {
@@ -40,7 +45,8 @@ cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp,
                           double *partials, unsigned *overflow,
                           cudaStream_t stream);
 
-cudaError_t launch_decide(const double *partials, int64_t tiles_per_slot,
+// level2: scratch for n_slots * ceil(tiles_per_slot / kPartialChunk) doubles
+cudaError_t launch_decide(const double *partials, double *level2, int64_t tiles_per_slot,
                           const uint64_t *active_mask, int n_slots,
                           double remote_sumsq, int remote_overflow,
                           int use_global, double global_sumsq, float clip,

@@ -234,14 +234,23 @@ class Run:
                     self.plan.gather(u, self.gather_shards, self.gather_out, stream)
             for u in units:
                 out.append(("gather", gb * int(self.plan.unit_padded[u]), 1, lambda u=u: gather(u)))
+            # backward: a unit's gradients join the reduce bucket once its
+            # backward gather is done; a full bucket (or the last unit) is
+            # reduce-scattered at once (bucket 0: every unit on its own)
+            pending = []
             for u in units[::-1]:
                 out.append(("gather", gb * int(self.plan.unit_padded[u]), 1, lambda u=u: gather(u)))
-                for r in self.ranks:
-                    out.append(("reduce", red_b * self.plan.shard_len(u), 1,
-                                lambda u=u, r=r: self.plan.reduce_unit(r, u, lists[r], self.g[r],
-                                                                       self.S, stream)))
+                pending.append(u)
+                elems = sum(self.plan.shard_len(v) for v in pending)
+                if not w.bucket_elems or elems >= w.bucket_elems or u == 0:
+                    first, cnt = min(pending), len(pending)
+                    for r in self.ranks:
+                        out.append(("reduce", red_b * elems, -(-cnt // 64),
+                                    lambda first=first, cnt=cnt, r=r: self.plan.reduce_units(
+                                        r, first, cnt, lists[r], self.g[r], self.S, stream)))
+                    pending = []
         else:
-            launches = self.buckets * (self.plan.n_units if w.stage == 3 else 1)
+            launches = self.buckets if w.stage != 3 else -(-self.plan.n_units // 64)
             for r in self.ranks:
                 out.append(("reduce", red_b * P, launches,
                             lambda r=r: self.plan.reduce(r, lists[r], self.g[r], self.S,

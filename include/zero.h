@@ -162,17 +162,19 @@ zero_status zero_reduce_partition(zero_plan *plan, int32_t rank,
                                   float *grad_out, float loss_scale,
                                   int64_t bucket_elems, void *stream);
 
-/* Stage 3: reduce only unit `unit`'s shard of rank `rank`'s partition ("10.6
- * ZeRO 与 FSDP" §10.6.4 backward step 4: each layer's gradients are
- * reduce-scattered as soon as the layer's backward is done, in reverse layer
- * order).  Same arguments and arithmetic as zero_reduce_partition (the
- * slices and grad_out are whole-partition buffers; only the unit's range is
- * read and written); the unit joins the current step like a partition.  The
- * norm's tiles restart at every unit, so reducing the units one by one, in
- * any order, gives exactly the bits of one zero_reduce_partition call. */
-zero_status zero_reduce_unit(zero_plan *plan, int32_t rank, int32_t unit,
-                             const void *const *grad_slices, float *grad_out,
-                             float loss_scale, void *stream);
+/* Stage 3: reduce only units [first_unit, first_unit + n_units) of rank
+ * `rank`'s partition ("10.6 ZeRO 与 FSDP" §10.6.4 backward step 4: each
+ * layer's gradients are reduce-scattered once its backward is done, in
+ * reverse layer order; "年糕切片" §2.2 reduce_bucket_size: a bucket collects
+ * several layers before it is reduced).  Same arguments and arithmetic as
+ * zero_reduce_partition (the slices and grad_out are whole-partition
+ * buffers; only the units' range is read and written), in one kernel launch
+ * per 64 units; the units join the current step like a partition.  The
+ * norm's tiles restart at every unit, so reducing the units in any grouping
+ * and order gives exactly the bits of one zero_reduce_partition call. */
+zero_status zero_reduce_units(zero_plan *plan, int32_t rank, int32_t first_unit,
+                              int32_t n_units, const void *const *grad_slices,
+                              float *grad_out, float loss_scale, void *stream);
 
 /* Local result of the reduces of the current step: sum of squares (fp64)
  * and overflow flag, for exchanging with other real ranks (pass the others'

@@ -373,20 +373,27 @@ def test_stage3_unit_by_unit_reduce_equals_partition_reduce(zlib, lp):
     n = 4
     sizes, units = [70_000, 5, 33_000, 100_000, 7, TILE * 2], [0, 0, 1, 2, 3, 4]
     res = []
-    for mode in ("partition", "units"):
+    for mode in ("partition", "units", "pairs", "buckets"):
         plan = _plan(-1, n, lp, stage=3, align=8, sizes=sizes, units=units)
         P = plan.part_len
         sl = [synth.grad_slice(P, lp, 1e-2, 1.0, 4, 1, j, 1, dev) for j in range(n)]
         g = torch.full((P,), float("nan"), dtype=torch.float32, device=dev)
         if mode == "partition":
             plan.reduce(1, sl, g, 1.0)
-        else:
+        elif mode == "units":
             for u in reversed(range(plan.n_units)):
-                plan.reduce_unit(1, u, sl, g, 1.0)
+                plan.reduce_units(1, u, 1, sl, g, 1.0)
+        elif mode == "pairs":
+            plan.reduce_units(1, 3, 2, sl, g, 1.0)
+            plan.reduce_units(1, 1, 2, sl, g, 1.0)
+            plan.reduce_units(1, 0, 1, sl, g, 1.0)
+        else:
+            plan.reduce(1, sl, g, 1.0, bucket_elems=3 * TILE + 5)
         res.append((g.cpu().numpy(), plan.stats(), [synth.to_numpy_codes(t) for t in sl]))
         plan.close()
-    assert same_floats(res[0][0], res[1][0])
-    assert res[0][1] == res[1][1]
+    for other in res[1:]:
+        assert same_floats(res[0][0], other[0])
+        assert res[0][1] == other[1]
     og, oss, oof = oracle.reduce(res[0][2], lp, 1.0)
     assert same_floats(res[0][0], og) and oof == res[0][1][1]
     assert abs(res[0][1][0] - oss) <= 1e-9 * oss
@@ -403,7 +410,7 @@ def test_partly_reduced_partition_counts_only_its_part(zlib):
     plan.reduce(0, sl, g, 1.0)                       # step 1: everything
     w = torch.zeros(P, device=dev); m = torch.zeros(P, device=dev); v = torch.zeros(P, device=dev)
     plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 0.0)
-    plan.reduce_unit(0, 1, sl, g, 1.0)              # step 2: unit 1 only
+    plan.reduce_units(0, 1, 1, sl, g, 1.0)          # step 2: unit 1 only
     ss, _ = plan.stats()
     off = plan.unit_shard_offset(1)
     _, oss, _ = oracle.reduce([synth.to_numpy_codes(t[off:]) for t in sl], 0, 1.0)

@@ -33,7 +33,7 @@ SIGNATURES = {
     "zero_plan_set_spin_limit": (_i32, [_vp, _i64]),
     "zero_plan_set_reduce_precision": (_i32, [_vp, _i32]),
     "zero_reduce_partition": (_i32, [_vp, _i32, _vp, _vp, _f32, _i64, _vp]),
-    "zero_reduce_unit": (_i32, [_vp, _i32, _i32, _vp, _vp, _f32, _vp]),
+    "zero_reduce_units": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _f32, _vp]),
     "zero_partition_stats": (_i32, [_vp, _vp, _vp, _vp]),
     "zero_step_set_global_stats": (_i32, [_vp, _f64, _i32]),
     "zero_adam_step": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32,
@@ -181,10 +181,11 @@ def zero_reduce_partition(plan: int, rank: int, grad_slices: Sequence, grad_out,
                                         _stream(stream)), "zero_reduce_partition")
 
 
-def zero_reduce_unit(plan: int, rank: int, unit: int, grad_slices: Sequence, grad_out,
-                     loss_scale: float, stream=None):
-    _check(load().zero_reduce_unit(plan, rank, unit, C.cast(_ptr_array(grad_slices), _vp),
-                                   _ptr(grad_out), loss_scale, _stream(stream)), "zero_reduce_unit")
+def zero_reduce_units(plan: int, rank: int, first_unit: int, n_units: int, grad_slices: Sequence,
+                      grad_out, loss_scale: float, stream=None):
+    _check(load().zero_reduce_units(plan, rank, first_unit, n_units,
+                                    C.cast(_ptr_array(grad_slices), _vp), _ptr(grad_out), loss_scale,
+                                    _stream(stream)), "zero_reduce_units")
 
 
 def zero_partition_stats(plan: int, stream=None):

@@ -30,6 +30,7 @@ constexpr int kReduceThreads = 128;
 constexpr int kVec = 8;  // lp elements per 16-byte vector
 constexpr int kTileIters = int(kTile / (kReduceThreads * kVec));
 constexpr int kBatch = 16;  // slices loaded before they are added
+constexpr int kMaxSegments = kMaxReduceSegments;  // tile runs per reduce launch
 constexpr int kGatherStages = 3;
 constexpr unsigned kGatherChunk = 32768;  // bytes per bulk copy
 constexpr long long kDrainPolls = 1ll << 21;
@@ -92,13 +93,17 @@ __device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float x) {
 
 template <int MAXN>
 struct ReduceParams {
-    const uint4 *src[MAXN];  // slice j at the bucket start
-    float4 *g;               // output at the bucket start
-    double *partials;        // partial of the bucket's first tile
+    const uint4 *src[MAXN];  // slice j at the partition start
+    float4 *g;               // output at the partition start
+    double *partials;        // the partition's tile partials
     unsigned *overflow;
-    long long len;           // elements in the bucket (multiple of 8)
-    float inv;               // float(1 / (S * N))
+    long long seg_off[kMaxSegments];    // first element of each segment (multiple of 8)
+    long long seg_end[kMaxSegments];    // one past its last element (multiple of 8)
+    long long seg_pbase[kMaxSegments];  // partial index of its first tile
+    int seg_cta0[kMaxSegments + 1];     // first CTA of each segment; [n_seg] = grid
+    float inv;                          // float(1 / (S * N))
     int n;
+    int n_seg;
 };
 
 // round a float to the lp type and back (nearest, ties to even)
@@ -123,21 +128,25 @@ template <int MAXN, bool BF16, bool ACC_LP>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
     __shared__ double warp_sq[kReduceThreads / 32];
-    const long long n_vec = p.len / kVec;
-    const long long n_tiles = (p.len + kTile - 1) / kTile;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     bool bad = false;
-
-    for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    // this CTA's tile: tile t of segment seg
+    int seg = 0;
+    while (seg + 1 < p.n_seg && (int)blockIdx.x >= p.seg_cta0[seg + 1]) ++seg;
+    const long long t = (long long)blockIdx.x - p.seg_cta0[seg];
+    const long long e0 = p.seg_off[seg] + t * kTile;
+    const long long e1 = e0 + kTile < p.seg_end[seg] ? e0 + kTile : p.seg_end[seg];
+    const long long v_end = e1 / kVec;
+    {
         // per-thread sum of squares as an unevaluated float pair (hi + lo):
         // compensated, so the tile sum is accurate to ~1e-13 relative and the
         // clip coefficient derived from it matches a sequential fp64 sum
         float sq_hi = 0.0f, sq_lo = 0.0f;
-        const long long v0 = tile * (kTile / kVec);
+        const long long v0 = e0 / kVec;
 #pragma unroll 1
         for (int it = 0; it < kTileIters; ++it) {
             const long long vi = v0 + (long long)it * kReduceThreads + threadIdx.x;
-            if (vi >= n_vec) break;
+            if (vi >= v_end) break;
             float s[8];
             unpack8<BF16>(ld_stream(p.src[0] + vi), s);
             for (int j0 = 1; j0 < p.n; j0 += kBatch) {
@@ -177,12 +186,11 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
         if (lane == 0) warp_sq[warp] = sq;
         __syncthreads();
         if (threadIdx.x == 0) {
-            double t = 0.0;
+            double tsum = 0.0;
 #pragma unroll
-            for (int w = 0; w < kReduceThreads / 32; ++w) t = __dadd_rn(t, warp_sq[w]);
-            p.partials[tile] = t;
+            for (int w = 0; w < kReduceThreads / 32; ++w) tsum = __dadd_rn(tsum, warp_sq[w]);
+            p.partials[p.seg_pbase[seg] + t] = tsum;
         }
-        __syncthreads();
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.overflow, 1u);
 }
@@ -662,22 +670,31 @@ int occupancy(K kernel, int threads, size_t smem) {
 }
 
 template <int MAXN, bool BF16, bool ACC_LP>
-cudaError_t reduce_impl(const void *const *slices, int n, int64_t offset, int64_t len, float inv,
-                        float *g, double *partials, unsigned *overflow, cudaStream_t stream) {
+cudaError_t reduce_impl(const void *const *slices, int n, const ReduceSegment *segs, int n_segs,
+                        float inv, float *g, double *partials, unsigned *overflow, cudaStream_t stream) {
+    if (n_segs < 1 || n_segs > kMaxSegments) return cudaErrorInvalidValue;
     ReduceParams<MAXN> p;
-    for (int j = 0; j < n; ++j)
-        p.src[j] = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(slices[j]) + offset);
+    for (int j = 0; j < n; ++j) p.src[j] = static_cast<const uint4 *>(slices[j]);
     for (int j = n; j < MAXN; ++j) p.src[j] = nullptr;
-    p.g = reinterpret_cast<float4 *>(g + offset);
+    p.g = reinterpret_cast<float4 *>(g);
     p.partials = partials;
     p.overflow = overflow;
-    p.len = len;
+    long long ctas = 0;
+    for (int i = 0; i < n_segs; ++i) {
+        p.seg_off[i] = segs[i].off;
+        p.seg_end[i] = segs[i].off + segs[i].len;
+        p.seg_pbase[i] = segs[i].pbase;
+        p.seg_cta0[i] = (int)ctas;
+        ctas += (segs[i].len + kTile - 1) / kTile;  // one tile per CTA
+    }
+    for (int i = n_segs; i < kMaxSegments; ++i) p.seg_off[i] = p.seg_end[i] = p.seg_pbase[i] = 0;
+    p.seg_cta0[n_segs] = (int)ctas;
     p.inv = inv;
     p.n = n;
-    // one tile per CTA: the block scheduler balances the tiles over the SMs
-    const long long grid = (len + kTile - 1) / kTile;
-    if (grid < 1) return cudaSuccess;
-    reduce_unscale_stats<MAXN, BF16, ACC_LP><<<(unsigned)grid, kReduceThreads, 0, stream>>>(p);
+    p.n_seg = n_segs;
+    if (ctas < 1) return cudaSuccess;
+    if (ctas > 0x7fffffffll) return cudaErrorInvalidValue;
+    reduce_unscale_stats<MAXN, BF16, ACC_LP><<<(unsigned)ctas, kReduceThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -735,22 +752,22 @@ int sm_count() {
 }
 
 template <int MAXN>
-cudaError_t reduce_dispatch(const void *const *slices, int n, int lp, bool acc_lp, int64_t offset,
-                            int64_t len, float inv, float *g, double *partials, unsigned *overflow,
+cudaError_t reduce_dispatch(const void *const *slices, int n, int lp, bool acc_lp, const ReduceSegment *segs,
+                            int n_segs, float inv, float *g, double *partials, unsigned *overflow,
                             cudaStream_t stream) {
     if (lp)
-        return acc_lp ? reduce_impl<MAXN, true, true>(slices, n, offset, len, inv, g, partials, overflow, stream)
-                      : reduce_impl<MAXN, true, false>(slices, n, offset, len, inv, g, partials, overflow, stream);
-    return acc_lp ? reduce_impl<MAXN, false, true>(slices, n, offset, len, inv, g, partials, overflow, stream)
-                  : reduce_impl<MAXN, false, false>(slices, n, offset, len, inv, g, partials, overflow, stream);
+        return acc_lp ? reduce_impl<MAXN, true, true>(slices, n, segs, n_segs, inv, g, partials, overflow, stream)
+                      : reduce_impl<MAXN, true, false>(slices, n, segs, n_segs, inv, g, partials, overflow, stream);
+    return acc_lp ? reduce_impl<MAXN, false, true>(slices, n, segs, n_segs, inv, g, partials, overflow, stream)
+                  : reduce_impl<MAXN, false, false>(slices, n, segs, n_segs, inv, g, partials, overflow, stream);
 }
 
-cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp, int64_t offset,
-                          int64_t len, float inv, float *g, double *partials, unsigned *overflow,
+cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp, const ReduceSegment *segs,
+                          int n_segs, float inv, float *g, double *partials, unsigned *overflow,
                           cudaStream_t stream) {
     if (n <= 64)
-        return reduce_dispatch<64>(slices, n, lp, acc_lp != 0, offset, len, inv, g, partials, overflow, stream);
-    return reduce_dispatch<1024>(slices, n, lp, acc_lp != 0, offset, len, inv, g, partials, overflow, stream);
+        return reduce_dispatch<64>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow, stream);
+    return reduce_dispatch<1024>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow, stream);
 }
 
 cudaError_t launch_decide(const double *partials, double *level2, int64_t tiles_per_slot,

@@ -408,23 +408,44 @@ zero_status begin_reduce(zero_plan *p, int32_t rank, const void *const *grad_sli
     return ZERO_OK;
 }
 
-// Reduce unit u's range of the partition (the whole partition when there is
-// one unit), in buckets of whole norm tiles counted from the unit's start.
-zero_status reduce_unit_range(zero_plan *p, int32_t slot, int32_t u, const void *const *src, float *grad_out,
-                              float loss_scale, int64_t bucket_elems, cudaStream_t s) {
-    const int64_t shard = p->shard_len(u);
-    const int64_t base = p->unit_part_off[size_t(u)];
+// Reduce units [first, first + count) of the partition (one unit unless stage
+// 3).  Each unit is cut into pieces of whole norm tiles counted from the unit's
+// start (bucket_elems rounded up to tiles; 0 = the whole unit); consecutive
+// pieces share one kernel launch while their total stays within one bucket
+// (any number when bucket_elems is 0), up to the kernel's segment limit.  The
+// grouping only decides launches: every tile's partial is the same.
+zero_status reduce_units(zero_plan *p, int32_t slot, int32_t first, int32_t count, const void *const *src,
+                         float *grad_out, float loss_scale, int64_t bucket_elems, cudaStream_t s) {
     const float inv = float(1.0 / (double(loss_scale) * double(p->n_ranks)));
-    double *partials = p->d_partials + int64_t(slot) * p->tiles_per_part + p->unit_tile_base[size_t(u)];
-    int64_t bucket = bucket_elems == 0 ? shard : round_up(bucket_elems, zk::kTile);
-    if (bucket <= 0) bucket = shard;
-    for (int64_t b0 = 0; b0 < shard; b0 += bucket) {
-        const int64_t len = std::min(bucket, shard - b0);
-        cudaError_t e = zk::launch_reduce(src, p->n_ranks, p->lp, p->reduce_lp_accum, base + b0, len, inv,
-                                          grad_out, partials + b0 / zk::kTile, &p->d_rec->overflow, s);
+    double *partials = p->d_partials + int64_t(slot) * p->tiles_per_part;
+    const int64_t piece = bucket_elems == 0 ? 0 : round_up(bucket_elems, zk::kTile);
+    std::vector<zk::ReduceSegment> segs;
+    int64_t launch_elems = 0;
+    auto flush = [&]() -> zero_status {
+        if (segs.empty()) return ZERO_OK;
+        cudaError_t e = zk::launch_reduce(src, p->n_ranks, p->lp, p->reduce_lp_accum, segs.data(),
+                                          int(segs.size()), inv, grad_out, partials, &p->d_rec->overflow, s);
+        segs.clear();
+        launch_elems = 0;
         if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
+        return ZERO_OK;
+    };
+    for (int32_t u = first; u < first + count; ++u) {
+        const int64_t shard = p->shard_len(u);
+        const int64_t base = p->unit_part_off[size_t(u)];
+        const int64_t step = piece == 0 ? std::max<int64_t>(shard, 1) : piece;
+        for (int64_t b0 = 0; b0 < shard; b0 += step) {
+            const int64_t len = std::min(step, shard - b0);
+            if (!segs.empty() && ((piece > 0 && launch_elems + len > piece) ||
+                                  int(segs.size()) == zk::kMaxReduceSegments)) {
+                zero_status st = flush();
+                if (st != ZERO_OK) return st;
+            }
+            segs.push_back({base + b0, len, p->unit_tile_base[size_t(u)] + b0 / zk::kTile});
+            launch_elems += len;
+        }
     }
-    return ZERO_OK;
+    return flush();
 }
 
 }  // namespace
@@ -441,25 +462,24 @@ zero_status zero_reduce_partition(zero_plan *p, int32_t rank, const void *const 
     if (st != ZERO_OK) return st;
     const int32_t slot = p->stage == 0 ? 0 : rank;
     p->active[slot >> 6] |= uint64_t(1) << (slot & 63);
-    for (int32_t u = 0; u < p->n_units(); ++u) {
-        st = reduce_unit_range(p, slot, u, src.data(), grad_out, loss_scale, bucket_elems, s);
-        if (st != ZERO_OK) return st;
-    }
-    return ZERO_OK;
+    return reduce_units(p, slot, 0, p->n_units(), src.data(), grad_out, loss_scale, bucket_elems, s);
 }
 
-zero_status zero_reduce_unit(zero_plan *p, int32_t rank, int32_t unit, const void *const *grad_slices,
-                             float *grad_out, float loss_scale, void *stream) {
+zero_status zero_reduce_units(zero_plan *p, int32_t rank, int32_t first_unit, int32_t n_units,
+                              const void *const *grad_slices, float *grad_out, float loss_scale,
+                              void *stream) {
     if (!p) return fail(ZERO_EINVAL, "plan is NULL");
-    if (p->stage != 3) return fail(ZERO_EINVAL, "zero_reduce_unit needs a stage-3 plan");
-    if (unit < 0 || unit >= p->n_units()) return fail(ZERO_EINVAL, "unit %d outside [0, %d)", unit, p->n_units());
+    if (p->stage != 3) return fail(ZERO_EINVAL, "zero_reduce_units needs a stage-3 plan");
+    if (first_unit < 0 || n_units < 1 || first_unit + n_units > p->n_units())
+        return fail(ZERO_EINVAL, "units [%d, %d) outside [0, %d)", first_unit, first_unit + n_units,
+                    p->n_units());
     std::vector<const void *> src;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     zero_status st = begin_reduce(p, rank, grad_slices, grad_out, loss_scale, 0, s, &src);
     if (st != ZERO_OK) return st;
     const int32_t slot = rank;
     p->active[slot >> 6] |= uint64_t(1) << (slot & 63);
-    return reduce_unit_range(p, slot, unit, src.data(), grad_out, loss_scale, 0, s);
+    return reduce_units(p, slot, first_unit, n_units, src.data(), grad_out, loss_scale, 0, s);
 }
 
 zero_status zero_partition_stats(zero_plan *p, double *sumsq, int32_t *overflow, void *stream) {

@@ -37,13 +37,20 @@ int sm_count();
 // message for zero_last_error() on the calling thread
 void set_last_error(const char *msg);
 
-// Reduce elements [offset, offset + len) of the slices into g[offset ...);
-// partials receives the sums of squares of the bucket's tiles (tile t of the
-// bucket -> partials[t]); overflow is OR-ed.
+// One run of whole norm tiles for the reduce kernel: elements [off, off + len)
+// of the partition (off and len multiples of 8; the run starts a tile), whose
+// first tile's partial sum goes to partials[pbase].
+struct ReduceSegment {
+    int64_t off, len, pbase;
+};
+constexpr int kMaxReduceSegments = 64;
+
+// Reduce the segments (at most kMaxReduceSegments) of the N slices -- pointers
+// to the partition start -- into g (partition start), one launch; partials is
+// the partition's partial array; overflow is OR-ed.
 cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp,
-                          int64_t offset, int64_t len, float inv, float *g,
-                          double *partials, unsigned *overflow,
-                          cudaStream_t stream);
+                          const ReduceSegment *segs, int n_segs, float inv, float *g,
+                          double *partials, unsigned *overflow, cudaStream_t stream);
 
 // level2: scratch for n_slots * ceil(tiles_per_slot / kPartialChunk) doubles
 cudaError_t launch_decide(const double *partials, double *level2, int64_t tiles_per_slot,

@@ -58,8 +58,9 @@ class ZeroPlan:
         A.zero_reduce_partition(self.handle, rank, grad_slices, grad_out, loss_scale,
                                 bucket_elems, stream)
 
-    def reduce_unit(self, rank, unit, grad_slices, grad_out, loss_scale, stream=None):
-        A.zero_reduce_unit(self.handle, rank, unit, grad_slices, grad_out, loss_scale, stream)
+    def reduce_units(self, rank, first_unit, n_units, grad_slices, grad_out, loss_scale, stream=None):
+        A.zero_reduce_units(self.handle, rank, first_unit, n_units, grad_slices, grad_out, loss_scale,
+                            stream)
 
     def stats(self, stream=None):
         return A.zero_partition_stats(self.handle, stream)

@@ -99,12 +99,13 @@ def _make():
     w["7.5b-zero3"] = Workload(
         name="7.5b-zero3", sizes=s, unit_of_tensor=u, n_ranks=64, stage=3, lp=0,
         ranks=[0], steps=4, loss_scale=65536.0, growth_interval=1000,
-        grads_times_scale=True, gather=True,
-        notes="7.5B, 33 units (rest + 32 d=4096 blocks), N=64 rank 0, fp16, gathers")
+        grads_times_scale=True, gather=True, bucket_elems=500_000_000,
+        notes="7.5B, 33 units (rest + 32 d=4096 blocks), N=64 rank 0, fp16, gathers, "
+              "reduce buckets of 5e8 elements")
     w["7.5b-zero3-q8"] = Workload(
         name="7.5b-zero3-q8", sizes=s, unit_of_tensor=u, n_ranks=64, stage=3, lp=0,
         ranks=[0], steps=4, loss_scale=65536.0, growth_interval=1000,
-        grads_times_scale=True, gather=True, gather_quantized=True,
+        grads_times_scale=True, gather=True, gather_quantized=True, bucket_elems=500_000_000,
         notes="7.5b-zero3 with ZeRO++-style int8 block-quantized gathers")
     w["13b-zero2"] = Workload(
         name="13b-zero2", sizes=[13_000_000_000], n_ranks=16, stage=2, lp=1,

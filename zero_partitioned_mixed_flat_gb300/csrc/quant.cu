@@ -64,45 +64,54 @@ __device__ __forceinline__ void from_lp4(uint2 raw, float v[4]) {
     }
 }
 
-// One warp per 128-element block, kQuantUnroll blocks per warp per pass: lane
-// l holds elements 4l..4l+3 of each block.  scale = amax / 127 (float
+// A half-warp per 128-element block (a warp takes a pair of blocks per 16-byte
+// load; kQuantUnroll pairs per pass): lane l holds elements 8(l mod 16) ..
+// 8(l mod 16) + 7 of block 2*pair + l/16.  scale = amax / 127 (float
 // division), code = nearest-even integer of x / scale, clamped to +-127.
 template <bool BF16>
 __global__ void __launch_bounds__(kQuantThreads)
-quantize_shard_blocks(const uint2 *__restrict__ x, uint32_t *__restrict__ q, float *__restrict__ scales,
+quantize_shard_blocks(const uint4 *__restrict__ x, uint2 *__restrict__ q, float *__restrict__ scales,
                       long long n_blocks) {
     const int lane = threadIdx.x & 31;
+    const long long n_pairs = (n_blocks + 1) / 2;
     const long long warps = (long long)gridDim.x * (kQuantThreads / 32);
     const long long w0 = (long long)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
-    for (long long base = w0; base < n_blocks; base += warps * kQuantUnroll) {
-        uint2 raw[kQuantUnroll];
+    for (long long base = w0; base < n_pairs; base += warps * kQuantUnroll) {
+        uint4 raw[kQuantUnroll];
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
-            const long long b = base + u * warps;
-            raw[u] = b < n_blocks ? __ldcs(x + b * 32 + lane) : make_uint2(0u, 0u);
+            const long long b = 2 * (base + u * warps) + (lane >> 4);
+            raw[u] = b < n_blocks ? __ldcs(x + b * 16 + (lane & 15)) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
-            const long long b = base + u * warps;
-            if (b >= n_blocks) break;  // uniform across the warp
-            float v[4];
-            from_lp4<BF16>(raw[u], v);
-            float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+            const long long pair = base + u * warps;
+            if (pair >= n_pairs) break;  // uniform across the warp
+            const long long b = 2 * pair + (lane >> 4);
+            float v[8];
+            from_lp4<BF16>(make_uint2(raw[u].x, raw[u].y), v);
+            from_lp4<BF16>(make_uint2(raw[u].z, raw[u].w), v + 4);
+            float amax = 0.0f;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1)  // within each half-warp
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
             const float scale = __fdiv_rn(amax, 127.0f);
-            uint32_t packed = 0;
+            uint32_t packed[2] = {0u, 0u};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < 8; ++k) {
                 int c = 0;
                 if (scale > 0.0f) {
                     c = __float2int_rn(__fdiv_rn(v[k], scale));
                     c = c > 127 ? 127 : (c < -127 ? -127 : c);
                 }
-                packed |= (uint32_t)(c & 0xff) << (8 * k);
+                packed[k >> 2] |= (uint32_t)(c & 0xff) << (8 * (k & 3));
             }
-            __stcs(q + b * 32 + lane, packed);
-            if (lane == 0) scales[b] = scale;
+            if (b < n_blocks) {
+                __stcs(q + b * 16 + (lane & 15), make_uint2(packed[0], packed[1]));
+                if ((lane & 15) == 0) scales[b] = scale;
+            }
         }
     }
 }
@@ -113,33 +122,35 @@ struct DequantGatherParams {
     const float *scales[MAXN];  // rank j's scales at this unit's first block
     uint4 *out;                 // 8 lp per uint4
     long long vec_per_shard;    // shard_len / 16
-    long long n_items;          // n * vec_per_shard
 };
 
-// out[j * shard + k] = lp(code_j[k] * scale_j[k / 128]); a thread takes
-// kQuantUnroll items of 16 codes (one load each, all issued before any use).
+// out[j * shard + k] = lp(code_j[k] * scale_j[k / 128]).  blockIdx.y is the
+// rank j; along x a thread takes kQuantUnroll items of 16 codes (one load
+// each, all issued before any use).
 template <int MAXN, bool BF16>
 __global__ void __launch_bounds__(kQuantThreads)
 gather_dequant(const __grid_constant__ DequantGatherParams<MAXN> p) {
+    const int j = blockIdx.y;
+    const uint4 *codes = p.codes[j];
+    const float *scales = p.scales[j];
+    uint4 *out = p.out + 2 * (long long)j * p.vec_per_shard;
     const long long stride = (long long)gridDim.x * kQuantThreads;
-    for (long long i0 = (long long)blockIdx.x * kQuantThreads + threadIdx.x; i0 < p.n_items;
-         i0 += stride * kQuantUnroll) {
+    for (long long k0 = (long long)blockIdx.x * kQuantThreads + threadIdx.x; k0 < p.vec_per_shard;
+         k0 += stride * kQuantUnroll) {
         uint4 c[kQuantUnroll];
         float sc[kQuantUnroll];
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
-            const long long i = i0 + u * stride;
-            if (i < p.n_items) {
-                const long long j = i / p.vec_per_shard;
-                const long long k16 = i - j * p.vec_per_shard;
-                c[u] = ld_stream16(p.codes[j] + k16);
-                sc[u] = __ldg(p.scales[j] + (k16 >> 3));  // 16 codes lie in one 128-block
+            const long long k = k0 + u * stride;
+            if (k < p.vec_per_shard) {
+                c[u] = ld_stream16(codes + k);
+                sc[u] = __ldg(scales + (k >> 3));  // 16 codes lie in one 128-block
             }
         }
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
-            const long long i = i0 + u * stride;
-            if (i >= p.n_items) break;
+            const long long k = k0 + u * stride;
+            if (k >= p.vec_per_shard) break;
             const uint32_t w[4] = {c[u].x ^ 0x80808080u, c[u].y ^ 0x80808080u,
                                    c[u].z ^ 0x80808080u, c[u].w ^ 0x80808080u};
             uint32_t o[8];
@@ -147,12 +158,12 @@ gather_dequant(const __grid_constant__ DequantGatherParams<MAXN> p) {
             for (int t = 0; t < 4; ++t) {
                 float y[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) y[k] = __fmul_rn(code_to_float(w[t], k), sc[u]);
+                for (int q = 0; q < 4; ++q) y[q] = __fmul_rn(code_to_float(w[t], q), sc[u]);
                 o[2 * t] = to_lp2_packed<BF16>(y[0], y[1]);
                 o[2 * t + 1] = to_lp2_packed<BF16>(y[2], y[3]);
             }
-            __stcs(p.out + 2 * i, make_uint4(o[0], o[1], o[2], o[3]));
-            __stcs(p.out + 2 * i + 1, make_uint4(o[4], o[5], o[6], o[7]));
+            __stcs(out + 2 * k, make_uint4(o[0], o[1], o[2], o[3]));
+            __stcs(out + 2 * k + 1, make_uint4(o[4], o[5], o[6], o[7]));
         }
     }
 }
@@ -178,13 +189,15 @@ cudaError_t dequant_gather_impl(const int8_t *const *codes, const float *const *
     }
     p.out = static_cast<uint4 *>(out);
     p.vec_per_shard = shard_len / 16;
-    p.n_items = p.vec_per_shard * n;
-    if (p.n_items == 0) return cudaSuccess;
+    if (p.vec_per_shard == 0 || n == 0) return cudaSuccess;
     static const int occ = blocks_per_sm(gather_dequant<MAXN, BF16>);
-    long long grid = (long long)sm_count() * occ;
-    const long long need = (p.n_items + kQuantThreads * kQuantUnroll - 1) / (kQuantThreads * kQuantUnroll);
-    if (grid > need) grid = need;
-    gather_dequant<MAXN, BF16><<<(unsigned)grid, kQuantThreads, 0, stream>>>(p);
+    // about two waves of CTAs over all ranks
+    const long long per_rank_need = (p.vec_per_shard + kQuantThreads * kQuantUnroll - 1) /
+                                    (kQuantThreads * kQuantUnroll);
+    long long gx = (2LL * sm_count() * occ + n - 1) / n;
+    if (gx > per_rank_need) gx = per_rank_need;
+    if (gx < 1) gx = 1;
+    gather_dequant<MAXN, BF16><<<dim3((unsigned)gx, (unsigned)n), kQuantThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -194,11 +207,11 @@ cudaError_t quantize_impl(const void *shard, int64_t len, int8_t *codes, float *
     if (blocks == 0) return cudaSuccess;
     static const int occ = blocks_per_sm(quantize_shard_blocks<BF16>);
     long long grid = (long long)sm_count() * occ;
-    const long long per_cta = (kQuantThreads / 32) * kQuantUnroll;
+    const long long per_cta = (kQuantThreads / 32) * kQuantUnroll * 2;
     const long long need = (blocks + per_cta - 1) / per_cta;
     if (grid > need) grid = need;
     quantize_shard_blocks<BF16><<<(unsigned)grid, kQuantThreads, 0, stream>>>(
-        static_cast<const uint2 *>(shard), reinterpret_cast<uint32_t *>(codes), scales, blocks);
+        static_cast<const uint4 *>(shard), reinterpret_cast<uint2 *>(codes), scales, blocks);
     return cudaGetLastError();
 }
 

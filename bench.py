@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="stage 3: issue every gather on one stream (no prefetch)")
     ap.add_argument("--quantized-gather", action="store_true",
                     help="stage-3 workloads: int8 block-quantized gathers")
     return ap.parse_args()
@@ -195,6 +197,7 @@ class Run:
             self.gather_shards = others[:r0] + [self.shard[r0]] + others[r0:]
             biggest = max(self.plan.shard_len(u) for u in range(self.plan.n_units)) * w.n_ranks
             self.gather_out = torch.empty(biggest, dtype=lpd, device=dev)
+            self.gather_out2 = torch.empty(biggest, dtype=lpd, device=dev)
             if self.quantized:
                 # every rank's int8 codes + block scales (ZeRO++-style gather);
                 # the other ranks quantize their shards once here
@@ -214,53 +217,74 @@ class Run:
         else:
             self.buckets = 1 if P else 0
 
-    def calls(self, stream, slice_lists=None):
+    def calls(self, stream, slice_lists=None, side=None):
         """The step as an ordered list of (kind, algorithmic HBM bytes, kernel
-        launches, callable).  Stage 3 follows the pages' order: forward gathers
-        of every unit, then per unit in reverse order its backward gather and
-        its reduce-scatter, then the local update."""
+        launches, callable, stream).  Stage 3 follows the pages' order:
+        forward gathers of every unit, then per unit in reverse order its
+        backward gather, its gradients joining the reduce bucket and a full
+        bucket reduce-scattered, then the local update.  With a `side` stream
+        the gathers alternate between two streams and two layer buffers
+        (prefetching the next unit while the current one is gathered, "10.6
+        ZeRO 与 FSDP" §10.6.4 预取); the reduce waits for the side stream, the
+        side stream's first gather waits for the previous update.  Entries of
+        kind "wait" are those stream orderings."""
+        import torch
         w, P = self.w, self.P
         lists = slice_lists or self.slice_lists
         out = []
         red_b = 2 * w.n_ranks + 4
+        sh = int(stream.cuda_stream)
         if self.gather_shards is not None:
             units = list(range(self.plan.n_units))
             gb = self.gather_bytes_per_element()
+            bufs = [self.gather_out, self.gather_out2] if side is not None else [self.gather_out]
+            streams = [stream, side] if side is not None else [stream]
+            ev_main, ev_side = torch.cuda.Event(), torch.cuda.Event()
+            if side is not None:
+                out.append(("wait", 0, 0, lambda: (ev_main.record(stream), side.wait_event(ev_main)),
+                            None))
+            nth = [0]
 
-            def gather(u):
-                if self.quantized:
-                    self.plan.gather_quantized(u, self.codes, self.scales, self.gather_out, stream)
-                else:
-                    self.plan.gather(u, self.gather_shards, self.gather_out, stream)
+            def add_gather(u):
+                k = nth[0] % len(streams)
+                nth[0] += 1
+                st, buf = streams[k], bufs[k]
+
+                def fn(u=u, st=st, buf=buf):
+                    if self.quantized:
+                        self.plan.gather_quantized(u, self.codes, self.scales, buf, int(st.cuda_stream))
+                    else:
+                        self.plan.gather(u, self.gather_shards, buf, int(st.cuda_stream))
+                out.append(("gather", gb * int(self.plan.unit_padded[u]), 1, fn, st))
             for u in units:
-                out.append(("gather", gb * int(self.plan.unit_padded[u]), 1, lambda u=u: gather(u)))
-            # backward: a unit's gradients join the reduce bucket once its
-            # backward gather is done; a full bucket (or the last unit) is
-            # reduce-scattered at once (bucket 0: every unit on its own)
+                add_gather(u)
             pending = []
             for u in units[::-1]:
-                out.append(("gather", gb * int(self.plan.unit_padded[u]), 1, lambda u=u: gather(u)))
+                add_gather(u)
                 pending.append(u)
                 elems = sum(self.plan.shard_len(v) for v in pending)
                 if not w.bucket_elems or elems >= w.bucket_elems or u == 0:
+                    if side is not None:
+                        out.append(("wait", 0, 0, lambda: (ev_side.record(side), stream.wait_event(ev_side)),
+                                    None))
                     first, cnt = min(pending), len(pending)
                     for r in self.ranks:
                         out.append(("reduce", red_b * elems, -(-cnt // 64),
                                     lambda first=first, cnt=cnt, r=r: self.plan.reduce_units(
-                                        r, first, cnt, lists[r], self.g[r], self.S, stream)))
+                                        r, first, cnt, lists[r], self.g[r], self.S, sh), stream))
                     pending = []
         else:
             launches = self.buckets if w.stage != 3 else -(-self.plan.n_units // 64)
             for r in self.ranks:
                 out.append(("reduce", red_b * P, launches,
                             lambda r=r: self.plan.reduce(r, lists[r], self.g[r], self.S,
-                                                         w.bucket_elems, stream)))
+                                                         w.bucket_elems, sh), stream))
         for i, r in enumerate(self.ranks):
-            out.append(("adam", 30 * P, 1 + (i == 0), lambda r=r: self._adam(r, stream)))
+            out.append(("adam", 30 * P, 1 + (i == 0), lambda r=r: self._adam(r, sh), stream))
             if self.quantized:
                 out.append(("quantize", int((3 + 4 / 128) * P), 1,
                             lambda r=r: self.plan.quantize(self.shard[r], self.codes[r],
-                                                           self.scales[r], stream)))
+                                                           self.scales[r], sh), stream))
         return out
 
     def _adam(self, r, stream):
@@ -270,14 +294,16 @@ class Run:
                        w.beta2, w.eps, w.wd, int(w.adamw), self.S, w.clip, 0.0, 0, stream)
 
     def launches_per_step(self):
-        return sum(c[2] for c in self.calls(0))
+        import torch
+        return sum(c[2] for c in self.calls(torch.cuda.current_stream()))
 
     def gather_bytes_per_element(self):
         # lp gather: 2 B in + 2 B out; quantized: 1 B code + 4/128 B scale in, 2 B out
         return (3 + 4 / 128) if self.quantized else 4
 
     def bytes_per_step(self):
-        return int(sum(c[1] for c in self.calls(0)))
+        import torch
+        return int(sum(c[1] for c in self.calls(torch.cuda.current_stream())))
 
 
 def dist_setup(n_gpus):
@@ -408,22 +434,30 @@ def main():
     stream = torch.cuda.current_stream()
     sh = int(stream.cuda_stream)
 
-    calls = run.calls(sh)
-    kinds = sorted({c[0] for c in calls})
+    side = torch.cuda.Stream() if (run.gather_shards is not None and not args.no_overlap) else None
+    calls = run.calls(stream, side=side)
+    timed_calls = [c for c in calls if c[0] != "wait"]
+    kinds = sorted({c[0] for c in timed_calls})
 
     def step(evs=None):
-        if evs is not None:
-            evs[0].record(stream)
-        for i, c in enumerate(calls):
+        i = 0
+        for c in calls:
+            if c[0] == "wait":
+                c[3]()
+                continue
+            if evs is not None:
+                evs[i][0].record(c[4])
             c[3]()
             if evs is not None:
-                evs[i + 1].record(stream)
+                evs[i][1].record(c[4])
+            i += 1
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in timed_calls] for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(enabled=not args.no_clocks)
@@ -451,11 +485,11 @@ def main():
     # per kind: time per step (sum of its calls), bytes per step, launches per step
     t_kind = {k: 0.0 for k in kinds}
     for e in evs:
-        for i, c in enumerate(calls):
-            t_kind[c[0]] += e[i].elapsed_time(e[i + 1])
+        for i, c in enumerate(timed_calls):
+            t_kind[c[0]] += e[i][0].elapsed_time(e[i][1])
     t_kind = {k: v / K for k, v in t_kind.items()}
-    b_kind = {k: sum(c[1] for c in calls if c[0] == k) for k in kinds}
-    n_kind = {k: sum(1 for c in calls if c[0] == k) for k in kinds}
+    b_kind = {k: sum(c[1] for c in timed_calls if c[0] == k) for k in kinds}
+    n_kind = {k: sum(1 for c in timed_calls if c[0] == k) for k in kinds}
     ms_per_step = total_ms / K
     elems = run.P * len(run.ranks)
     value = elems * ws / (ms_per_step / 1e3)
@@ -483,7 +517,7 @@ def main():
     # ---- end to end through the ABI, host buffers, copies inside the timed region
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(run, args.e2e_steps, stream, sh, ws, dist, dev)
+        e2e = measure_e2e(run, args.e2e_steps, stream, side, ws, dist, dev)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -498,6 +532,8 @@ def main():
                            "lp": ["fp16", "bf16"][w.lp], "part_len": run.P,
                            "partitions_per_gpu": len(run.ranks),
                            "bucket_elems": w.bucket_elems,
+                           "gather_prefetch_streams": 2 if side is not None else (
+                               1 if run.gather_shards is not None else 0),
                            "l2": "inputs larger than L2 (%.1f GB touched per step vs 129 MB L2)"
                                  % (run.bytes_per_step() / 1e9),
                            "parallelism": "dp%d simulated on each GPU (ranks as device buffers)"
@@ -527,7 +563,7 @@ def host_mem_available():
     return None
 
 
-def measure_e2e(run, steps, stream, sh, ws, dist, dev):
+def measure_e2e(run, steps, stream, side, ws, dist, dev):
     """Same metric through the public API with the step's gradient slices in
     pinned host memory, timed end to end on the host clock, every step ending
     with a synchronising device->host read of the step result.
@@ -557,8 +593,8 @@ def measure_e2e(run, steps, stream, sh, ws, dist, dev):
     h2d = sum(int(t.numel()) * t.element_size() for t in host.values())
     host_lists = {r: [host[r][j] for j in range(run.w.n_ranks)] for r in run.ranks}
 
-    staged_calls = run.calls(sh)
-    direct_calls = run.calls(sh, slice_lists=host_lists)
+    staged_calls = run.calls(stream, side=side)
+    direct_calls = run.calls(stream, slice_lists=host_lists, side=side)
 
     def staged():
         for r in run.ranks:

@@ -7,7 +7,8 @@
 // lp while it concatenates the ranks' shards.  Per layer element the gather
 // moves 1 B + 4/128 B in and 2 B out, against 2 B in and 2 B out for the lp
 // gather.  Both kernels are plain streaming kernels; each thread keeps several
-// independent 16-byte (or 8-byte) loads in flight before it computes.
+// independent loads in flight before it computes, and every warp load and
+// store is one contiguous run.
 #include "zero_internal.h"
 
 #include <cuda_bf16.h>
@@ -18,14 +19,6 @@ namespace {
 
 constexpr int kQuantThreads = 256;
 constexpr int kQuantUnroll = 4;   // blocks per warp (quantize) / items per thread (gather)
-
-__device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
 
 // two floats -> two lp values in one packed conversion (each rounded to
 // nearest, ties to even, as a separate conversion would)
@@ -118,52 +111,51 @@ quantize_shard_blocks(const uint4 *__restrict__ x, uint2 *__restrict__ q, float 
 
 template <int MAXN>
 struct DequantGatherParams {
-    const uint4 *codes[MAXN];   // rank j's codes at this unit's offset (16 per uint4)
+    const uint2 *codes[MAXN];   // rank j's codes at this unit's offset (8 per uint2)
     const float *scales[MAXN];  // rank j's scales at this unit's first block
     uint4 *out;                 // 8 lp per uint4
-    long long vec_per_shard;    // shard_len / 16
+    long long vec_per_shard;    // shard_len / 8
 };
 
 // out[j * shard + k] = lp(code_j[k] * scale_j[k / 128]).  blockIdx.y is the
-// rank j; along x a thread takes kQuantUnroll items of 16 codes (one load
-// each, all issued before any use).
+// rank j; along x a thread takes kQuantUnroll items of 8 codes (one 8-byte
+// load each, all issued before any use) and writes each item's 8 lp values
+// with one 16-byte store, so a warp's loads and stores are contiguous runs.
 template <int MAXN, bool BF16>
 __global__ void __launch_bounds__(kQuantThreads)
 gather_dequant(const __grid_constant__ DequantGatherParams<MAXN> p) {
     const int j = blockIdx.y;
-    const uint4 *codes = p.codes[j];
+    const uint2 *codes = p.codes[j];
     const float *scales = p.scales[j];
-    uint4 *out = p.out + 2 * (long long)j * p.vec_per_shard;
+    uint4 *out = p.out + (long long)j * p.vec_per_shard;
     const long long stride = (long long)gridDim.x * kQuantThreads;
     for (long long k0 = (long long)blockIdx.x * kQuantThreads + threadIdx.x; k0 < p.vec_per_shard;
          k0 += stride * kQuantUnroll) {
-        uint4 c[kQuantUnroll];
+        uint2 c[kQuantUnroll];
         float sc[kQuantUnroll];
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
             const long long k = k0 + u * stride;
             if (k < p.vec_per_shard) {
-                c[u] = ld_stream16(codes + k);
-                sc[u] = __ldg(scales + (k >> 3));  // 16 codes lie in one 128-block
+                c[u] = __ldcs(codes + k);
+                sc[u] = __ldg(scales + (k >> 4));  // 8 codes lie in one 128-block
             }
         }
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
             const long long k = k0 + u * stride;
             if (k >= p.vec_per_shard) break;
-            const uint32_t w[4] = {c[u].x ^ 0x80808080u, c[u].y ^ 0x80808080u,
-                                   c[u].z ^ 0x80808080u, c[u].w ^ 0x80808080u};
-            uint32_t o[8];
+            const uint32_t w[2] = {c[u].x ^ 0x80808080u, c[u].y ^ 0x80808080u};
+            uint32_t o[4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
+            for (int t = 0; t < 2; ++t) {
                 float y[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) y[q] = __fmul_rn(code_to_float(w[t], q), sc[u]);
                 o[2 * t] = to_lp2_packed<BF16>(y[0], y[1]);
                 o[2 * t + 1] = to_lp2_packed<BF16>(y[2], y[3]);
             }
-            __stcs(out + 2 * k, make_uint4(o[0], o[1], o[2], o[3]));
-            __stcs(out + 2 * k + 1, make_uint4(o[4], o[5], o[6], o[7]));
+            __stcs(out + k, make_uint4(o[0], o[1], o[2], o[3]));
         }
     }
 }
@@ -180,7 +172,7 @@ cudaError_t dequant_gather_impl(const int8_t *const *codes, const float *const *
                                 int64_t offset, int64_t shard_len, void *out, cudaStream_t stream) {
     DequantGatherParams<MAXN> p;
     for (int j = 0; j < n; ++j) {
-        p.codes[j] = reinterpret_cast<const uint4 *>(codes[j] + offset);
+        p.codes[j] = reinterpret_cast<const uint2 *>(codes[j] + offset);
         p.scales[j] = scales[j] + offset / 128;
     }
     for (int j = n; j < MAXN; ++j) {
@@ -188,7 +180,7 @@ cudaError_t dequant_gather_impl(const int8_t *const *codes, const float *const *
         p.scales[j] = nullptr;
     }
     p.out = static_cast<uint4 *>(out);
-    p.vec_per_shard = shard_len / 16;
+    p.vec_per_shard = shard_len / 8;
     if (p.vec_per_shard == 0 || n == 0) return cudaSuccess;
     static const int occ = blocks_per_sm(gather_dequant<MAXN, BF16>);
     // about two waves of CTAs over all ranks

@@ -483,10 +483,23 @@ def main():
     if res["skipped"]:
         log("warning: a timed step was skipped (overflow)")
     # per kind: time per step (sum of its calls), bytes per step, launches per step
+    # time per kind and step = the union of its calls' intervals (calls of one
+    # kind may overlap when gathers are prefetched on the second stream)
     t_kind = {k: 0.0 for k in kinds}
     for e in evs:
+        spans = {k: [] for k in kinds}
         for i, c in enumerate(timed_calls):
-            t_kind[c[0]] += e[i][0].elapsed_time(e[i][1])
+            spans[c[0]].append((start.elapsed_time(e[i][0]), start.elapsed_time(e[i][1])))
+        for k, iv in spans.items():
+            iv.sort()
+            cur0, cur1 = iv[0]
+            for a, b_ in iv[1:]:
+                if a > cur1:
+                    t_kind[k] += cur1 - cur0
+                    cur0, cur1 = a, b_
+                else:
+                    cur1 = max(cur1, b_)
+            t_kind[k] += cur1 - cur0
     t_kind = {k: v / K for k, v in t_kind.items()}
     b_kind = {k: sum(c[1] for c in timed_calls if c[0] == k) for k in kinds}
     n_kind = {k: sum(1 for c in timed_calls if c[0] == k) for k in kinds}

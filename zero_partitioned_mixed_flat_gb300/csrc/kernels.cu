@@ -34,7 +34,7 @@ constexpr int kMaxSegments = kMaxReduceSegments;  // tile runs per reduce launch
 constexpr int kGatherStages = 3;
 constexpr unsigned kGatherChunk = 32768;  // bytes per bulk copy
 constexpr long long kDrainPolls = 1ll << 21;
-static_assert(kTile % (kReduceThreads * kVec) == 0, "tile must be whole iterations");
+static_assert(kTile % (2 * kReduceThreads * kVec) == 0, "tile must be whole iterations");
 
 // ---------------------------------------------------------------- memory ops
 
@@ -124,10 +124,16 @@ __device__ __forceinline__ void round_lp_pair(float &a, float &b) {
 // value is added (reduce in the low-precision dtype).  The float add of two lp
 // values followed by that rounding equals the correctly rounded lp sum (24
 // float bits >= 2p + 2, so the double rounding is innocuous).
-template <int MAXN, bool BF16, bool ACC_LP>
+// VPT: vectors (of 8 elements) per thread per iteration; 2 for small N so a
+// thread still keeps 16 loads in flight.  Each warp's 1 KB of float output per
+// vector round goes through shared memory so that it leaves as two contiguous
+// 512-byte stores instead of 32 lanes writing 32-byte strided halves.
+template <int MAXN, bool BF16, bool ACC_LP, int VPT>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
+    constexpr int BATCH = kBatch / VPT;
     __shared__ double warp_sq[kReduceThreads / 32];
+    __shared__ float4 stage[kReduceThreads / 32][64];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     bool bad = false;
     // this CTA's tile: tile t of segment seg
@@ -144,39 +150,67 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
         float sq_hi = 0.0f, sq_lo = 0.0f;
         const long long v0 = e0 / kVec;
 #pragma unroll 1
-        for (int it = 0; it < kTileIters; ++it) {
-            const long long vi = v0 + (long long)it * kReduceThreads + threadIdx.x;
-            if (vi >= v_end) break;
-            float s[8];
-            unpack8<BF16>(ld_stream(p.src[0] + vi), s);
-            for (int j0 = 1; j0 < p.n; j0 += kBatch) {
-                uint4 q[kBatch];
+        for (int it = 0; it < kTileIters / VPT; ++it) {
+            const long long vb = v0 + (long long)it * VPT * kReduceThreads + warp * 32;
+            if (vb >= v_end) break;  // the whole warp is past the end
+            long long vi[VPT];
+            bool ok[VPT];
 #pragma unroll
-                for (int b = 0; b < kBatch; ++b)
-                    if (j0 + b < p.n) q[b] = ld_stream(p.src[j0 + b] + vi);
+            for (int v = 0; v < VPT; ++v) {
+                vi[v] = vb + (long long)v * kReduceThreads + lane;
+                ok[v] = vi[v] < v_end;
+            }
+            float s[VPT][8];
 #pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    if (j0 + b < p.n) {
-                        float x[8];
-                        unpack8<BF16>(q[b], x);
+            for (int v = 0; v < VPT; ++v) {
+                const uint4 z = ok[v] ? ld_stream(p.src[0] + vi[v]) : make_uint4(0u, 0u, 0u, 0u);
+                unpack8<BF16>(z, s[v]);
+            }
+            for (int j0 = 1; j0 < p.n; j0 += BATCH) {
+                uint4 q[VPT][BATCH];
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], x[k]);
-                        if constexpr (ACC_LP) {
+                for (int v = 0; v < VPT; ++v)
 #pragma unroll
-                            for (int k = 0; k < 8; k += 2) round_lp_pair<BF16>(s[k], s[k + 1]);
+                    for (int b = 0; b < BATCH; ++b)
+                        if (j0 + b < p.n && ok[v]) q[v][b] = ld_stream(p.src[j0 + b] + vi[v]);
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) {
+#pragma unroll
+                    for (int b = 0; b < BATCH; ++b) {
+                        if (j0 + b < p.n && ok[v]) {
+                            float x[8];
+                            unpack8<BF16>(q[v][b], x);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) s[v][k] = __fadd_rn(s[v][k], x[k]);
+                            if constexpr (ACC_LP) {
+#pragma unroll
+                                for (int k = 0; k < 8; k += 2) round_lp_pair<BF16>(s[v][k], s[v][k + 1]);
+                            }
                         }
                     }
                 }
             }
-            float o[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                bad |= !isfinite(s[k]);
-                o[k] = __fmul_rn(s[k], p.inv);
-                two_sum_acc(sq_hi, sq_lo, __fmul_rn(o[k], o[k]));
+            for (int v = 0; v < VPT; ++v) {
+                float o[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    bad |= !isfinite(s[v][k]);  // zero for lanes past the end
+                    o[k] = __fmul_rn(s[v][k], p.inv);
+                    two_sum_acc(sq_hi, sq_lo, __fmul_rn(o[k], o[k]));
+                }
+                // lane l's vector -> stage[2l, 2l+1]; then lane l stores float4 l
+                // and 32 + l of the warp's contiguous 1 KB run
+                stage[warp][2 * lane] = make_float4(o[0], o[1], o[2], o[3]);
+                stage[warp][2 * lane + 1] = make_float4(o[4], o[5], o[6], o[7]);
+                __syncwarp();
+                const float4 lo = stage[warp][lane];
+                const float4 hi = stage[warp][32 + lane];
+                __syncwarp();
+                const long long wv = vb + (long long)v * kReduceThreads;  // the warp's first vector
+                if (wv + (lane >> 1) < v_end) st_stream_f4(p.g + 2 * wv + lane, lo);
+                if (wv + 16 + (lane >> 1) < v_end) st_stream_f4(p.g + 2 * wv + 32 + lane, hi);
             }
-            st_stream_f4(p.g + 2 * vi, make_float4(o[0], o[1], o[2], o[3]));
-            st_stream_f4(p.g + 2 * vi + 1, make_float4(o[4], o[5], o[6], o[7]));
         }
         // fixed-shape fp64 tree: lanes (xor butterfly), then warps in order
         double sq = __dadd_rn((double)sq_hi, (double)sq_lo);
@@ -669,7 +703,7 @@ int occupancy(K kernel, int threads, size_t smem) {
     return blocks < 1 ? 1 : blocks;
 }
 
-template <int MAXN, bool BF16, bool ACC_LP>
+template <int MAXN, bool BF16, bool ACC_LP, int VPT>
 cudaError_t reduce_impl(const void *const *slices, int n, const ReduceSegment *segs, int n_segs,
                         float inv, float *g, double *partials, unsigned *overflow, cudaStream_t stream) {
     if (n_segs < 1 || n_segs > kMaxSegments) return cudaErrorInvalidValue;
@@ -694,7 +728,7 @@ cudaError_t reduce_impl(const void *const *slices, int n, const ReduceSegment *s
     p.n_seg = n_segs;
     if (ctas < 1) return cudaSuccess;
     if (ctas > 0x7fffffffll) return cudaErrorInvalidValue;
-    reduce_unscale_stats<MAXN, BF16, ACC_LP><<<(unsigned)ctas, kReduceThreads, 0, stream>>>(p);
+    reduce_unscale_stats<MAXN, BF16, ACC_LP, VPT><<<(unsigned)ctas, kReduceThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -751,23 +785,25 @@ int sm_count() {
     return g_dev[dev].sms;
 }
 
-template <int MAXN>
+template <int MAXN, int VPT>
 cudaError_t reduce_dispatch(const void *const *slices, int n, int lp, bool acc_lp, const ReduceSegment *segs,
                             int n_segs, float inv, float *g, double *partials, unsigned *overflow,
                             cudaStream_t stream) {
     if (lp)
-        return acc_lp ? reduce_impl<MAXN, true, true>(slices, n, segs, n_segs, inv, g, partials, overflow, stream)
-                      : reduce_impl<MAXN, true, false>(slices, n, segs, n_segs, inv, g, partials, overflow, stream);
-    return acc_lp ? reduce_impl<MAXN, false, true>(slices, n, segs, n_segs, inv, g, partials, overflow, stream)
-                  : reduce_impl<MAXN, false, false>(slices, n, segs, n_segs, inv, g, partials, overflow, stream);
+        return acc_lp ? reduce_impl<MAXN, true, true, VPT>(slices, n, segs, n_segs, inv, g, partials, overflow, stream)
+                      : reduce_impl<MAXN, true, false, VPT>(slices, n, segs, n_segs, inv, g, partials, overflow, stream);
+    return acc_lp ? reduce_impl<MAXN, false, true, VPT>(slices, n, segs, n_segs, inv, g, partials, overflow, stream)
+                  : reduce_impl<MAXN, false, false, VPT>(slices, n, segs, n_segs, inv, g, partials, overflow, stream);
 }
 
 cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp, const ReduceSegment *segs,
                           int n_segs, float inv, float *g, double *partials, unsigned *overflow,
                           cudaStream_t stream) {
+    if (n <= kBatch / 2)
+        return reduce_dispatch<64, 2>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow, stream);
     if (n <= 64)
-        return reduce_dispatch<64>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow, stream);
-    return reduce_dispatch<1024>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow, stream);
+        return reduce_dispatch<64, 1>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow, stream);
+    return reduce_dispatch<1024, 1>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow, stream);
 }
 
 cudaError_t launch_decide(const double *partials, double *level2, int64_t tiles_per_slot,

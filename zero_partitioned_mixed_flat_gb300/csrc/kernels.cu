@@ -4,7 +4,7 @@
 //                          partition, unscale, overflow flag, per-tile sum of
 //                          squares ("10.6 ZeRO 与 FSDP" §10.6.1 Reduce-Scatter,
 //                          §10.6.2 Step 2).
-// K2 norm_finalize_decide  global norm, clip coefficient, skip and loss-scale
+// K2 norm_decide           global norm, clip coefficient, skip and loss-scale
 //                          decision, step counter ("年糕切片" §4.2-§4.3).
 // K3 adam_fused_cast       Adam/AdamW on fp32 master/m/v + lp cast into the
 //                          all-gather destination (§10.6.2 Steps 3-4); a
@@ -231,42 +231,13 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
 
 // ------------------------------------------------------------------ K2 decide
 
-struct ChunkSumParams {
+struct DecideParams {
     const double *partials;
     double *level2;
+    unsigned *arrivals;  // 0 at launch; the last block resets it
     long long tiles_per_slot;
     int chunks_per_slot;
-    short slots[1024];  // the step's reduced partition slots, ascending
-};
-
-constexpr int kChunkThreads = 256;
-
-// First level of the norm: block `item` sums one fixed chunk of one reduced
-// partition's tile partials (strided per thread, xor tree, warps in order).
-__global__ void __launch_bounds__(kChunkThreads)
-partial_chunk_sums(const __grid_constant__ ChunkSumParams p) {
-    __shared__ double wsum[kChunkThreads / 32];
-    const int item = blockIdx.x;
-    const int slot = p.slots[item / p.chunks_per_slot];
-    const long long t0 = (long long)(item % p.chunks_per_slot) * kPartialChunk;
-    const long long t1 = t0 + kPartialChunk < p.tiles_per_slot ? t0 + kPartialChunk : p.tiles_per_slot;
-    const double *q = p.partials + (long long)slot * p.tiles_per_slot;
-    double acc = 0.0;
-    for (long long t = t0 + threadIdx.x; t < t1; t += kChunkThreads) acc = __dadd_rn(acc, q[t]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
-    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = acc;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int w = 0; w < kChunkThreads / 32; ++w) t = __dadd_rn(t, wsum[w]);
-        p.level2[item] = t;
-    }
-}
-
-struct DecideParams {
-    const double *level2;
-    int n_items;
+    int n_items;         // reduced slots x chunks per slot (>= 1)
     double remote_sumsq;
     double global_sumsq;
     int remote_overflow;
@@ -274,25 +245,57 @@ struct DecideParams {
     float clip, loss_scale, beta1, beta2;
     int growth_interval;
     StepRecord *rec;
+    short slots[1024];   // the step's reduced partition slots, ascending
 };
 
-constexpr int kDecideThreads = 1024;
+constexpr int kDecideThreads = 256;
 
-__global__ void __launch_bounds__(kDecideThreads)
-norm_finalize_decide(const __grid_constant__ DecideParams p) {
-    __shared__ double wsum[kDecideThreads / 32];
-    double acc = 0.0;
-    for (int t = threadIdx.x; t < p.n_items; t += kDecideThreads) acc = __dadd_rn(acc, p.level2[t]);
+__device__ __forceinline__ double block_sum_fixed(double acc, double *wsum) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+    for (int off = 16; off > 0; off >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
     if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = acc;
     __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kDecideThreads / 32; ++w) t = __dadd_rn(t, wsum[w]);
+    return t;  // valid in thread 0
+}
+
+// The norm in two fixed-order fp64 levels and the step decision, in one
+// launch: block `item` sums one fixed chunk of one reduced partition's tile
+// partials; the last block to arrive (counted after a fence) sums those
+// chunk sums in item order and decides.  The order of every addition depends
+// only on the partition sizes, never on which block finishes first.
+__global__ void __launch_bounds__(kDecideThreads)
+norm_decide(const __grid_constant__ DecideParams p) {
+    __shared__ double wsum[kDecideThreads / 32];
+    __shared__ bool last;
+    {
+        const int item = blockIdx.x;
+        const int slot = p.slots[item / p.chunks_per_slot];
+        const long long t0 = (long long)(item % p.chunks_per_slot) * kPartialChunk;
+        const long long t1 = t0 + kPartialChunk < p.tiles_per_slot ? t0 + kPartialChunk : p.tiles_per_slot;
+        const double *q = p.partials + (long long)slot * p.tiles_per_slot;
+        double acc = 0.0;
+        for (long long t = t0 + threadIdx.x; t < t1; t += kDecideThreads) acc = __dadd_rn(acc, q[t]);
+        const double chunk = block_sum_fixed(acc, wsum);
+        if (threadIdx.x == 0) {
+            p.level2[item] = chunk;
+            __threadfence();
+            last = atomicAdd(p.arrivals, 1u) == gridDim.x - 1;
+        }
+        __syncthreads();
+    }
+    if (!last) return;
+    __threadfence();
+    double acc = 0.0;
+    for (int t = threadIdx.x; t < p.n_items; t += kDecideThreads) acc = __dadd_rn(acc, __ldcg(p.level2 + t));
+    __syncthreads();  // wsum is reused
+    double sumsq = block_sum_fixed(acc, wsum);
     if (threadIdx.x != 0) return;
+    *p.arrivals = 0u;
 
     StepRecord *rec = p.rec;
-    double sumsq = 0.0;
-    for (int w = 0; w < kDecideThreads / 32; ++w) sumsq = __dadd_rn(sumsq, wsum[w]);
     sumsq = p.use_global ? p.global_sumsq : __dadd_rn(sumsq, p.remote_sumsq);
     const double norm = sqrt(sumsq);
     const int skip = (rec->overflow != 0u) || (p.remote_overflow != 0);
@@ -806,29 +809,23 @@ cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp, 
     return reduce_dispatch<1024, 1>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow, stream);
 }
 
-cudaError_t launch_decide(const double *partials, double *level2, int64_t tiles_per_slot,
+cudaError_t launch_decide(const double *partials, double *level2, unsigned *arrivals, int64_t tiles_per_slot,
                           const uint64_t *active_mask, int n_slots, double remote_sumsq, int remote_overflow,
                           int use_global, double global_sumsq, float clip, float loss_scale,
                           int growth_interval, float beta1, float beta2, StepRecord *rec,
                           cudaStream_t stream) {
-    ChunkSumParams c;
-    c.partials = partials;
-    c.level2 = level2;
-    c.tiles_per_slot = tiles_per_slot;
-    c.chunks_per_slot = (int)((tiles_per_slot + kPartialChunk - 1) / kPartialChunk);
-    if (c.chunks_per_slot < 1) c.chunks_per_slot = 1;
+    DecideParams p;
+    p.partials = partials;
+    p.level2 = level2;
+    p.arrivals = arrivals;
+    p.tiles_per_slot = tiles_per_slot;
+    p.chunks_per_slot = (int)((tiles_per_slot + kPartialChunk - 1) / kPartialChunk);
+    if (p.chunks_per_slot < 1) p.chunks_per_slot = 1;
     int active = 0;
     for (int r = 0; r < n_slots; ++r)
-        if ((active_mask[r >> 6] >> (r & 63)) & 1u) c.slots[active++] = (short)r;
-    const int items = active * c.chunks_per_slot;
-    if (items > 0) {
-        partial_chunk_sums<<<items, kChunkThreads, 0, stream>>>(c);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    DecideParams p;
-    p.level2 = level2;
-    p.n_items = items;
+        if ((active_mask[r >> 6] >> (r & 63)) & 1u) p.slots[active++] = (short)r;
+    if (active == 0) return cudaErrorInvalidValue;
+    p.n_items = active * p.chunks_per_slot;
     p.remote_sumsq = remote_sumsq;
     p.remote_overflow = remote_overflow;
     p.use_global = use_global;
@@ -839,7 +836,7 @@ cudaError_t launch_decide(const double *partials, double *level2, int64_t tiles_
     p.beta2 = beta2;
     p.growth_interval = growth_interval;
     p.rec = rec;
-    norm_finalize_decide<<<1, kDecideThreads, 0, stream>>>(p);
+    norm_decide<<<p.n_items, kDecideThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

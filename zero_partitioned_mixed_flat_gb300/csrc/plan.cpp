@@ -537,8 +537,12 @@ zero_status zero_adam_step(zero_plan *p, int32_t rank, const float *grad, float 
     if (st != ZERO_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->phase == kReducing) {
+        bool any = false;
+        for (uint64_t w : p->active) any = any || w != 0;
+        if (!any) return fail(ZERO_ESTATE, "no partition was reduced in the current step");
         const int r_of = p->use_global ? (p->global_overflow ? 1 : 0) : (remote_overflow ? 1 : 0);
-        cudaError_t e = zk::launch_decide(p->d_partials, p->d_level2, p->tiles_per_part, p->active, p->slots,
+        cudaError_t e = zk::launch_decide(p->d_partials, p->d_level2, &p->d_rec->arrivals, p->tiles_per_part,
+                                          p->active, p->slots,
                                           remote_sumsq, r_of, p->use_global ? 1 : 0,
                                           p->global_sumsq, clip, loss_scale, p->growth_interval,
                                           beta1, beta2, p->d_rec, s);

@@ -29,7 +29,8 @@ struct StepRecord {
     int good_steps;       // consecutive non-skipped steps since the last growth
     unsigned overflow;    // set by the reduce kernel when a sum is not finite
     int error;            // set when a bounded device wait gives up
-    int pad_[2];
+    unsigned arrivals;    // blocks of the norm kernel done (0 between launches)
+    int pad_;
 };
 
 int sm_count();
@@ -53,7 +54,8 @@ cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp,
                           double *partials, unsigned *overflow, cudaStream_t stream);
 
 // level2: scratch for n_slots * ceil(tiles_per_slot / kPartialChunk) doubles
-cudaError_t launch_decide(const double *partials, double *level2, int64_t tiles_per_slot,
+cudaError_t launch_decide(const double *partials, double *level2, unsigned *arrivals,
+                          int64_t tiles_per_slot,
                           const uint64_t *active_mask, int n_slots,
                           double remote_sumsq, int remote_overflow,
                           int use_global, double global_sumsq, float clip,

@@ -333,6 +333,59 @@ def test_quantize_and_dequant_gather(zlib, n, lp):
     _quant_case(n, [5000, 128, 40_000, 3, 70_000], [0, 0, 1, 2, 2], lp)
 
 
+def _boundary_blocks(lp, rng, n_blocks):
+    """lp codes of n_blocks 128-element blocks whose quotients x / scale sit on
+    or next to half-integers (ties to even and both neighbours), with block
+    maxima from tiny to huge (bf16) so that every scale range is exercised."""
+    out = np.empty((n_blocks, 128), np.uint16)
+    big = 60000.0 if lp == 0 else 1e36
+    tiny = 1e-4 if lp == 0 else 1e-36
+    for b in range(n_blocks):
+        kind = b % 4
+        if kind == 0:
+            amax = np.float32(127.0)                 # scale exactly 1
+        elif kind == 1:
+            amax = np.float32(10.0 ** rng.uniform(-3, 3))
+        elif kind == 2:
+            amax = np.float32(big * rng.uniform(0.5, 1.0))
+        else:
+            amax = np.float32(tiny * rng.uniform(1.0, 2.0))
+        amax_c = oracle.float_to_lp(np.array([amax], np.float32), lp)[0]
+        amax = oracle.lp_to_float(np.array([amax_c], np.uint16), lp)[0]
+        scale = np.float32(amax / np.float32(127.0))
+        k = rng.integers(-127, 127, 127).astype(np.float32) + np.float32(0.5)
+        x = oracle.float_to_lp((k * scale).astype(np.float32), lp).astype(np.int32)
+        x += rng.integers(-1, 2, 127)                # the tie's code or a neighbour
+        x = np.clip(x, 0, 0xFFFF).astype(np.uint16)
+        xf = oracle.lp_to_float(x, lp)
+        x[~(np.abs(xf) <= amax)] = amax_c           # keep |x| <= amax (and finite)
+        out[b, 0] = amax_c
+        out[b, 1:] = x
+    return out.reshape(-1)
+
+
+@pytest.mark.parametrize("lp", [0, 1])
+def test_quantize_rounding_boundaries(zlib, lp):
+    # quotients on and next to half-integers: the codes must be those of the
+    # correctly rounded quotient, ties to even
+    rng = np.random.default_rng(11 + lp)
+    n = 2
+    plan = _plan(-1, n, lp, stage=3, align=128, sizes=[n * 128 * 256], units=[0])
+    P = plan.part_len
+    dev = torch.device("cuda")
+    for j in range(n):
+        host = _boundary_blocks(lp, rng, P // 128)
+        shard = torch.from_numpy(host.view(np.int16)).to(dev).view(synth.LP_DTYPES[lp])
+        codes = torch.empty(P, dtype=torch.int8, device=dev)
+        scales = torch.empty(P // 128, dtype=torch.float32, device=dev)
+        plan.quantize(shard, codes, scales)
+        torch.cuda.synchronize()
+        oq, osc = oracle.quantize_blocks(host, lp, 128)
+        assert np.array_equal(scales.cpu().numpy().view(np.uint32), osc.view(np.uint32))
+        assert np.array_equal(codes.cpu().numpy(), oq)
+    plan.close()
+
+
 def test_quantized_gather_rejects_small_align(zlib):
     plan = _plan(-1, 2, 0, stage=3, align=8, sizes=[64, 64], units=[0, 1])
     buf = torch.zeros(1024, dtype=torch.float16, device="cuda")

@@ -29,12 +29,17 @@ namespace {
 constexpr int kReduceThreads = 128;
 constexpr int kVec = 8;  // lp elements per 16-byte vector
 constexpr int kTileIters = int(kTile / (kReduceThreads * kVec));
-constexpr int kBatch = 16;  // slices loaded before they are added
+constexpr int kBatch = 16;  // loads (slices x vectors) a thread issues before it adds
+// vectors of 8 elements a thread takes from each slice per round: 4 makes a
+// warp's load from one slice one contiguous 2 KB run and covers a 4096-element
+// tile in one round (faster than 1 or 2 at N = 8, 16 and 64 on GB300)
+constexpr int kReduceVpt = 4;
 constexpr int kMaxSegments = kMaxReduceSegments;  // tile runs per reduce launch
 constexpr int kGatherStages = 3;
 constexpr unsigned kGatherChunk = 32768;  // bytes per bulk copy
 constexpr long long kDrainPolls = 1ll << 21;
-static_assert(kTile % (2 * kReduceThreads * kVec) == 0, "tile must be whole iterations");
+static_assert(kTile % (kReduceVpt * kReduceThreads * kVec) == 0, "tile must be whole rounds");
+static_assert(kBatch % kReduceVpt == 0, "a batch holds whole slices");
 
 // ---------------------------------------------------------------- memory ops
 
@@ -124,10 +129,11 @@ __device__ __forceinline__ void round_lp_pair(float &a, float &b) {
 // value is added (reduce in the low-precision dtype).  The float add of two lp
 // values followed by that rounding equals the correctly rounded lp sum (24
 // float bits >= 2p + 2, so the double rounding is innocuous).
-// VPT: vectors (of 8 elements) per thread per iteration; 2 for small N so a
-// thread still keeps 16 loads in flight.  Each warp's 1 KB of float output per
-// vector round goes through shared memory so that it leaves as two contiguous
-// 512-byte stores instead of 32 lanes writing 32-byte strided halves.
+// VPT: vectors (of 8 elements) per thread per round, kBatch / VPT slices per
+// batch of loads, so a thread keeps kBatch loads in flight.  Each warp's 1 KB
+// of float output per vector goes through shared memory so that it leaves as
+// two contiguous 512-byte stores instead of 32 lanes writing 32-byte strided
+// halves.
 template <int MAXN, bool BF16, bool ACC_LP, int VPT>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
@@ -802,11 +808,11 @@ cudaError_t reduce_dispatch(const void *const *slices, int n, int lp, bool acc_l
 cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp, const ReduceSegment *segs,
                           int n_segs, float inv, float *g, double *partials, unsigned *overflow,
                           cudaStream_t stream) {
-    if (n <= kBatch / 2)
-        return reduce_dispatch<64, 2>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow, stream);
     if (n <= 64)
-        return reduce_dispatch<64, 1>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow, stream);
-    return reduce_dispatch<1024, 1>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow, stream);
+        return reduce_dispatch<64, kReduceVpt>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow,
+                                               stream);
+    return reduce_dispatch<1024, kReduceVpt>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow,
+                                             stream);
 }
 
 cudaError_t launch_decide(const double *partials, double *level2, unsigned *arrivals, int64_t tiles_per_slot,

@@ -41,6 +41,54 @@ __device__ __forceinline__ float code_to_float(uint32_t biased, int k) {
     return __fsub_rn(__uint_as_float(bits), 8388736.0f);
 }
 
+// The code of x: the nearest-even integer of the correctly rounded quotient
+// x / scale, clamped to +-127, as a byte (the division, for the rare elements
+// that the fast path below leaves to it).
+__device__ __forceinline__ uint32_t code_by_division(float x, float scale) {
+    if (!(scale > 0.0f)) return 0u;
+    int c = __float2int_rn(__fdiv_rn(x, scale));
+    c = c > 127 ? 127 : (c < -127 ? -127 : c);
+    return (uint32_t)c & 0xffu;
+}
+
+// Adding 1.5 * 2^23 to a float q with |q| < 2^22 leaves the nearest-even
+// integer k of q in the low mantissa bits (the adder rounds to nearest even,
+// and 1.5 * 2^23 is even), so the low byte of the sum is k as a signed byte
+// and subtracting the constant back gives k exactly.
+constexpr float kRoundMagic = 12582912.0f;
+
+// 8 codes of one thread's elements, packed 4 per word (byte k = element k).
+// Fast path: q = x * RN(1/scale) lies within 2^-23 |x/scale| of the exact
+// quotient and RN(x / scale) within 2^-24 |x/scale|; with |x/scale| <= 127
+// both lie within 2.3e-5 of it, so when every q is farther than 2^-13 from a
+// half-integer, rounding q gives the codes of the correctly rounded quotients
+// (and |q| < 127.5 needs no clamp).  Otherwise (rare: ties, a NaN element), and
+// for a zero, subnormal-small, huge or non-finite scale, every element is
+// divided.
+__device__ __forceinline__ void quant_codes8(const float v[8], float scale, uint32_t packed[2]) {
+    bool divide = !(scale >= 0x1p-100f && scale <= 0x1p+100f);
+    if (!divide) {
+        const float rcp = __frcp_rn(scale);
+        uint32_t t[8];
+        bool near = false;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float q = __fmul_rn(v[k], rcp);
+            const float r = __fadd_rn(q, kRoundMagic);
+            near |= !(fabsf(__fsub_rn(q, __fsub_rn(r, kRoundMagic))) < 0.5f - 0x1p-13f);
+            t[k] = __float_as_uint(r);
+        }
+        packed[0] = __byte_perm(__byte_perm(t[0], t[1], 0x0040u), __byte_perm(t[2], t[3], 0x0040u), 0x5410u);
+        packed[1] = __byte_perm(__byte_perm(t[4], t[5], 0x0040u), __byte_perm(t[6], t[7], 0x0040u), 0x5410u);
+        divide = near;
+    }
+    if (divide) {
+        packed[0] = packed[1] = 0u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) packed[k >> 2] |= code_by_division(v[k], scale) << (8 * (k & 3));
+    }
+}
+
 template <bool BF16>
 __device__ __forceinline__ void from_lp4(uint2 raw, float v[4]) {
     const uint32_t w[2] = {raw.x, raw.y};
@@ -60,7 +108,8 @@ __device__ __forceinline__ void from_lp4(uint2 raw, float v[4]) {
 // A half-warp per 128-element block (a warp takes a pair of blocks per 16-byte
 // load; kQuantUnroll pairs per pass): lane l holds elements 8(l mod 16) ..
 // 8(l mod 16) + 7 of block 2*pair + l/16.  scale = amax / 127 (float
-// division), code = nearest-even integer of x / scale, clamped to +-127.
+// division), code = nearest-even integer of x / scale (the correctly rounded
+// float quotient, see quant_codes8), clamped to +-127.
 template <bool BF16>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_shard_blocks(const uint4 *__restrict__ x, uint2 *__restrict__ q, float *__restrict__ scales,
@@ -91,16 +140,8 @@ quantize_shard_blocks(const uint4 *__restrict__ x, uint2 *__restrict__ q, float 
             for (int off = 8; off > 0; off >>= 1)  // within each half-warp
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
             const float scale = __fdiv_rn(amax, 127.0f);
-            uint32_t packed[2] = {0u, 0u};
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                int c = 0;
-                if (scale > 0.0f) {
-                    c = __float2int_rn(__fdiv_rn(v[k], scale));
-                    c = c > 127 ? 127 : (c < -127 ? -127 : c);
-                }
-                packed[k >> 2] |= (uint32_t)(c & 0xff) << (8 * (k & 3));
-            }
+            uint32_t packed[2];
+            quant_codes8(v, scale, packed);
             if (b < n_blocks) {
                 __stcs(q + b * 16 + (lane & 15), make_uint2(packed[0], packed[1]));
                 if ((lane & 15) == 0) scales[b] = scale;

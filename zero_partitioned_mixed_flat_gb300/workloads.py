@@ -125,6 +125,11 @@ def _make():
         lp=0, ranks=[0], steps=4, loss_scale=65536.0, growth_interval=1000,
         grads_times_scale=True, gather=True,
         notes="7.5b-zero3 kernels on 3 units (64M rest + two d=1024 blocks)")
+    w["profile-zero3-q8"] = Workload(
+        name="profile-zero3-q8", sizes=[1 << 28], unit_of_tensor=[0], n_ranks=4, stage=3,
+        lp=0, ranks=[0], steps=4, loss_scale=65536.0, growth_interval=1000,
+        grads_times_scale=True, gather=True, gather_quantized=True,
+        notes="quantize and dequantizing-gather kernels on one 2^28 unit, N=4 (P = 2^26)")
     return w
 
 

@@ -223,6 +223,26 @@ zero_status zero_adam_step(zero_plan *plan, int32_t rank, const float *grad,
                            float clip, double remote_sumsq,
                            int32_t remote_overflow, void *stream);
 
+/* Optimizer sub-groups ("10.6 ZeRO 与 FSDP" §10.6.6, the ds_config key
+ * sub_group_size: the flat partition is stepped a sub-group of elements at a
+ * time).  zero_adam_step restricted to partition elements [begin, begin +
+ * len): the same decision (taken by the first call of the step, range or
+ * whole), the same per-element arithmetic, so stepping a partition in
+ * sub-groups, in any order and grouping, gives exactly the bits of one
+ * zero_adam_step call.  grad, master, m, v and param_out are the same
+ * whole-partition (or whole-layout) pointers as for zero_adam_step; only the
+ * range is read and written.  begin and len must be multiples of 8
+ * (ZERO_EALIGN otherwise) with begin + len <= P (ZERO_EINVAL otherwise);
+ * len = 0 only takes the decision if it is still due.  Each element must be
+ * stepped once per step: the library does not track which ranges were done. */
+zero_status zero_adam_step_range(zero_plan *plan, int32_t rank, int64_t begin,
+                                 int64_t len, const float *grad, float *master,
+                                 float *m, float *v, void *param_out, float lr,
+                                 float beta1, float beta2, float eps, float wd,
+                                 int32_t adamw, float loss_scale, float clip,
+                                 double remote_sumsq, int32_t remote_overflow,
+                                 void *stream);
+
 /* Decision of the last decided step: global norm, skipped flag, loss scale
  * for the next step, and the step counter t.  Any pointer may be NULL.
  * Synchronises the device.  Returns ZERO_ETIMEOUT (and clears it) if a

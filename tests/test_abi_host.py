@@ -142,6 +142,17 @@ def test_step_calls_validate_before_touching_the_device(lib):
             Z.zero_adam_step(plan, 0, buf, buf + 8, buf, buf, buf, 1e-3, .9, .999, 1e-8, 0.,
                              1, 1.0, 1.0, stream=0)
         assert e.value.code == Z.ZERO_EALIGN
+        for begin, length, code in [(-8, 8, Z.ZERO_EINVAL), (0, 520, Z.ZERO_EINVAL),
+                                    (512, 8, Z.ZERO_EINVAL), (4, 8, Z.ZERO_EALIGN),
+                                    (0, 12, Z.ZERO_EALIGN)]:   # P = 512
+            with pytest.raises(Z.ZeroError) as e:
+                Z.zero_adam_step_range(plan, 0, begin, length, buf, buf, buf, buf, buf, 1e-3, .9,
+                                       .999, 1e-8, 0., 1, 1.0, 1.0, stream=0)
+            assert e.value.code == code, (begin, length)
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_adam_step_range(plan, 0, 8, 8, buf, buf, buf, buf, buf, 1e-3, .9, .999, 1e-8,
+                                   0., 1, 1.0, 1.0, stream=0)
+        assert e.value.code == Z.ZERO_ESTATE                     # Adam before any reduce
         with pytest.raises(Z.ZeroError) as e:
             Z.zero_gather_layer(plan, 0, [buf, buf], buf, stream=0)
         assert e.value.code == Z.ZERO_EINVAL                     # not a stage-3 plan

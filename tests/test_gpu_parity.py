@@ -147,6 +147,25 @@ def test_tiny_variants(zlib, kw):
     h.close()
 
 
+@pytest.mark.parametrize("sub_group", [8, 40_000, 1 << 20])
+def test_adam_in_sub_groups(zlib, sub_group):
+    # the optimizer step taken a sub-group at a time (sub_group_size) against
+    # the oracle, and bit for bit against the whole-partition call
+    w = _tiny(n_ranks=3, ranks=[0, 1, 2], sizes=[100_000, 7, 33_333], clip=0.05)
+    a = Harness(w, sub_group=sub_group)
+    b = Harness(w)
+    for _ in range(2):
+        a.step()
+        b.step()
+        for r in a.ranks:
+            for t in ("master", "m", "v"):
+                assert torch.equal(getattr(a.st[r], t), getattr(b.st[r], t)), (r, t)
+        assert torch.equal(a.param, b.param)
+        assert a.plan.result() == b.plan.result()
+    a.close()
+    b.close()
+
+
 def test_overflow_skips_and_halves_scale(zlib):
     w = _tiny(growth_interval=1000, inject_inf_step=2, loss_scale=65536.0, steps=3)
     h = Harness(w)

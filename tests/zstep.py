@@ -89,8 +89,9 @@ class Harness:
 
     def __init__(self, w: Workload, ranks=None, full: bool = True, n_sample: int = 1 << 20,
                  threads: int = 8, chunk: int = 1 << 22, device="cuda", bucket=None,
-                 stage=None):
+                 stage=None, sub_group: int = 0):
         self.w = w
+        self.sub_group = sub_group  # > 0: Adam in sub-groups of this many elements
         self.dev = torch.device(device)
         self.full = full
         self.threads = threads
@@ -168,8 +169,15 @@ class Harness:
         for r in self.ranks:
             s = self.st[r]
             out = s.shard if self.stage == 3 else self.param
-            self.plan.adam(r, s.g, s.master, s.m, s.v, out, w.lr, w.beta1, w.beta2, w.eps, w.wd,
-                           int(w.adamw), self.S, w.clip)
+            if not self.sub_group:
+                self.plan.adam(r, s.g, s.master, s.m, s.v, out, w.lr, w.beta1, w.beta2, w.eps,
+                               w.wd, int(w.adamw), self.S, w.clip)
+                continue
+            # sub-groups in reverse order, the last one ragged
+            for b in reversed(range(0, self.P, self.sub_group)):
+                n = min(self.sub_group, self.P - b)
+                self.plan.adam_range(r, b, n, s.g, s.master, s.m, s.v, out, w.lr, w.beta1,
+                                     w.beta2, w.eps, w.wd, int(w.adamw), self.S, w.clip)
         return self.plan.result()
 
     # ---------------------------------------------------------- oracle

@@ -38,6 +38,8 @@ SIGNATURES = {
     "zero_step_set_global_stats": (_i32, [_vp, _f64, _i32]),
     "zero_adam_step": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32,
                               _f32, _i32, _f32, _f32, _f64, _i32, _vp]),
+    "zero_adam_step_range": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _f32, _f32,
+                                    _f32, _f32, _f32, _i32, _f32, _f32, _f64, _i32, _vp]),
     "zero_step_result": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "zero_plan_check": (_i32, [_vp]),
     "zero_gather_layer": (_i32, [_vp, _i32, _vp, _vp, _vp]),
@@ -208,6 +210,16 @@ def zero_adam_step(plan: int, rank: int, grad, master, m, v, param_out, lr: floa
                                  _ptr(param_out), lr, beta1, beta2, eps, wd, int(adamw),
                                  loss_scale, clip, remote_sumsq, int(remote_overflow),
                                  _stream(stream)), "zero_adam_step")
+
+
+def zero_adam_step_range(plan: int, rank: int, begin: int, length: int, grad, master, m, v,
+                         param_out, lr: float, beta1: float, beta2: float, eps: float, wd: float,
+                         adamw: int, loss_scale: float, clip: float, remote_sumsq: float = 0.0,
+                         remote_overflow: int = 0, stream=None):
+    _check(load().zero_adam_step_range(plan, rank, begin, length, _ptr(grad), _ptr(master), _ptr(m),
+                                       _ptr(v), _ptr(param_out), lr, beta1, beta2, eps, wd,
+                                       int(adamw), loss_scale, clip, remote_sumsq,
+                                       int(remote_overflow), _stream(stream)), "zero_adam_step_range")
 
 
 def zero_step_result(plan: int) -> dict:

@@ -519,11 +519,17 @@ zero_status zero_step_set_global_stats(zero_plan *p, double global_sumsq, int32_
     return ZERO_OK;
 }
 
-zero_status zero_adam_step(zero_plan *p, int32_t rank, const float *grad, float *master, float *m,
-                           float *v, void *param_out, float lr, float beta1, float beta2, float eps,
-                           float wd, int32_t adamw, float loss_scale, float clip,
-                           double remote_sumsq, int32_t remote_overflow, void *stream) {
-    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+}  // extern "C"
+
+namespace {
+
+// The decision (first call of a step) and the Adam launch over partition
+// elements [begin, begin + len) of rank `rank`; shared by zero_adam_step
+// (the whole partition) and zero_adam_step_range (one sub-group).
+zero_status adam_impl(zero_plan *p, int32_t rank, int64_t begin, int64_t len, const float *grad,
+                      float *master, float *m, float *v, void *param_out, float lr, float beta1,
+                      float beta2, float eps, float wd, int32_t adamw, float loss_scale, float clip,
+                      double remote_sumsq, int32_t remote_overflow, void *stream) {
     zero_status st = check_rank(p, rank);
     if (st != ZERO_OK) return st;
     if (p->part > 0 && (!grad || !master || !m || !v)) return fail(ZERO_EINVAL, "NULL state pointer");
@@ -549,19 +555,48 @@ zero_status zero_adam_step(zero_plan *p, int32_t rank, const float *grad, float 
         if (e != cudaSuccess) return cuda_fail(e, "decide kernel launch");
         p->phase = kDecided;
     }
+    if (len == 0) return ZERO_OK;
     const float omb1 = 1.0f - beta1;
     const float omb2 = 1.0f - beta2;
     const float decay = float(1.0 - double(lr) * double(wd));
     void *param = nullptr;
     if (param_out) {
-        const int64_t off = (p->stage == 3) ? 0 : int64_t(rank) * p->part;
+        const int64_t off = ((p->stage == 3) ? 0 : int64_t(rank) * p->part) + begin;
         param = static_cast<uint16_t *>(param_out) + off;
     }
-    cudaError_t e = zk::launch_adam(grad, master, m, v, param, p->lp, p->part, p->d_rec,
-                                    &p->d_rec->error, lr, beta1, beta2, omb1, omb2, eps, wd, decay,
-                                    adamw ? 1 : 0, s);
+    cudaError_t e = zk::launch_adam(grad + begin, master + begin, m + begin, v + begin, param, p->lp, len,
+                                    p->d_rec, &p->d_rec->error, lr, beta1, beta2, omb1, omb2, eps, wd,
+                                    decay, adamw ? 1 : 0, s);
     if (e != cudaSuccess) return cuda_fail(e, "adam kernel launch");
     return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+zero_status zero_adam_step(zero_plan *p, int32_t rank, const float *grad, float *master, float *m,
+                           float *v, void *param_out, float lr, float beta1, float beta2, float eps,
+                           float wd, int32_t adamw, float loss_scale, float clip,
+                           double remote_sumsq, int32_t remote_overflow, void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    return adam_impl(p, rank, 0, p->part, grad, master, m, v, param_out, lr, beta1, beta2, eps, wd,
+                     adamw, loss_scale, clip, remote_sumsq, remote_overflow, stream);
+}
+
+zero_status zero_adam_step_range(zero_plan *p, int32_t rank, int64_t begin, int64_t len,
+                                 const float *grad, float *master, float *m, float *v,
+                                 void *param_out, float lr, float beta1, float beta2, float eps,
+                                 float wd, int32_t adamw, float loss_scale, float clip,
+                                 double remote_sumsq, int32_t remote_overflow, void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (begin < 0 || len < 0 || begin > p->part || len > p->part - begin)
+        return fail(ZERO_EINVAL, "range [%lld, %lld + %lld) outside the partition of %lld elements",
+                    (long long)begin, (long long)begin, (long long)len, (long long)p->part);
+    if (begin % 8 != 0 || len % 8 != 0)
+        return fail(ZERO_EALIGN, "sub-group begin and length must be multiples of 8 elements");
+    return adam_impl(p, rank, begin, len, grad, master, m, v, param_out, lr, beta1, beta2, eps, wd,
+                     adamw, loss_scale, clip, remote_sumsq, remote_overflow, stream);
 }
 
 zero_status zero_step_result(zero_plan *p, double *norm, int32_t *skipped, float *new_loss_scale,

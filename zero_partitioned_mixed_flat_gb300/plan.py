@@ -73,6 +73,13 @@ class ZeroPlan:
         A.zero_adam_step(self.handle, rank, grad, master, m, v, param_out, lr, beta1, beta2,
                          eps, wd, adamw, loss_scale, clip, remote_sumsq, remote_overflow, stream)
 
+    def adam_range(self, rank, begin, length, grad, master, m, v, param_out, lr, beta1, beta2,
+                   eps, wd, adamw, loss_scale, clip, remote_sumsq=0.0, remote_overflow=0,
+                   stream=None):
+        A.zero_adam_step_range(self.handle, rank, begin, length, grad, master, m, v, param_out,
+                               lr, beta1, beta2, eps, wd, adamw, loss_scale, clip, remote_sumsq,
+                               remote_overflow, stream)
+
     def result(self):
         return A.zero_step_result(self.handle)
 

@@ -16,6 +16,7 @@
 // Everything here is bandwidth-bound streaming: no tensor cores.  All float
 // arithmetic of the step uses explicit round-to-nearest intrinsics so that no
 // multiply-add is fused and the op order is the one the ABI documents.
+#include "launch.h"
 #include "zero_internal.h"
 
 #include <cuda_bf16.h>
@@ -137,6 +138,7 @@ __device__ __forceinline__ void round_lp_pair(float &a, float &b) {
 template <int MAXN, bool BF16, bool ACC_LP, int VPT>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
+    pdl_enter();
     constexpr int BATCH = kBatch / VPT;
     __shared__ double warp_sq[kReduceThreads / 32];
     __shared__ float4 stage[kReduceThreads / 32][64];
@@ -274,6 +276,7 @@ __device__ __forceinline__ double block_sum_fixed(double acc, double *wsum) {
 // only on the partition sizes, never on which block finishes first.
 __global__ void __launch_bounds__(kDecideThreads)
 norm_decide(const __grid_constant__ DecideParams p) {
+    pdl_enter();
     __shared__ double wsum[kDecideThreads / 32];
     __shared__ bool last;
     {
@@ -490,6 +493,7 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[kAdamInStages];
     __shared__ __align__(8) uint64_t empty[kAdamInStages];
+    pdl_enter();
     const StepRecord *rec = p.rec;
     if (rec->skip) return;
     const long long n_tiles = (p.len + kAdamTile - 1) / kAdamTile;
@@ -631,6 +635,7 @@ __global__ void __launch_bounds__(32)
 gather_layer_tma(const __grid_constant__ GatherParams<MAXN> p) {
     extern __shared__ __align__(128) unsigned char stage_buf[];
     __shared__ __align__(8) uint64_t bar[kGatherStages];
+    pdl_enter();
     if (threadIdx.x != 0) return;  // one thread drives the copy engine
     if (blockIdx.x >= p.n_chunks) return;
     const long long count = (p.n_chunks - blockIdx.x + gridDim.x - 1) / gridDim.x;
@@ -737,8 +742,8 @@ cudaError_t reduce_impl(const void *const *slices, int n, const ReduceSegment *s
     p.n_seg = n_segs;
     if (ctas < 1) return cudaSuccess;
     if (ctas > 0x7fffffffll) return cudaErrorInvalidValue;
-    reduce_unscale_stats<MAXN, BF16, ACC_LP, VPT><<<(unsigned)ctas, kReduceThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(reduce_unscale_stats<MAXN, BF16, ACC_LP, VPT>, dim3((unsigned)ctas), dim3(kReduceThreads),
+                      0, stream, p);
 }
 
 template <bool BF16>
@@ -751,8 +756,8 @@ cudaError_t adam_tma_impl(const AdamTmaParams &p, cudaStream_t stream) {
     long long grid = (long long)sm_count() * occ;
     if (grid > tiles) grid = tiles;
     if (grid < 1) return cudaSuccess;
-    adam_fused_cast<BF16><<<(unsigned)grid, kAdamTmaThreads, kAdamTmaSmem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(adam_fused_cast<BF16>, dim3((unsigned)grid), dim3(kAdamTmaThreads), kAdamTmaSmem, stream,
+                      p);
 }
 
 template <int MAXN>
@@ -776,8 +781,7 @@ cudaError_t gather_impl(const void *const *shards, int n, int64_t src_off, int64
     static const int occ = occupancy(gather_layer_tma<MAXN>, 32, smem);
     long long grid = (long long)sm_count() * occ;
     if (grid > p.n_chunks) grid = p.n_chunks;
-    gather_layer_tma<MAXN><<<(unsigned)grid, 32, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(gather_layer_tma<MAXN>, dim3((unsigned)grid), dim3(32), smem, stream, p);
 }
 
 }  // namespace
@@ -842,8 +846,7 @@ cudaError_t launch_decide(const double *partials, double *level2, unsigned *arri
     p.beta2 = beta2;
     p.growth_interval = growth_interval;
     p.rec = rec;
-    norm_decide<<<p.n_items, kDecideThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(norm_decide, dim3((unsigned)p.n_items), dim3(kDecideThreads), 0, stream, p);
 }
 
 cudaError_t launch_adam(const float *g, float *master, float *m, float *v, void *param, int lp,

@@ -9,6 +9,7 @@
 // gather.  Both kernels are plain streaming kernels; each thread keeps several
 // independent loads in flight before it computes, and every warp load and
 // store is one contiguous run.
+#include "launch.h"
 #include "zero_internal.h"
 
 #include <cuda_bf16.h>
@@ -114,6 +115,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_shard_blocks(const uint4 *__restrict__ x, uint2 *__restrict__ q, float *__restrict__ scales,
                       long long n_blocks) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const long long n_pairs = (n_blocks + 1) / 2;
     const long long warps = (long long)gridDim.x * (kQuantThreads / 32);
@@ -165,6 +167,7 @@ struct DequantGatherParams {
 template <int MAXN, bool BF16>
 __global__ void __launch_bounds__(kQuantThreads)
 gather_dequant(const __grid_constant__ DequantGatherParams<MAXN> p) {
+    pdl_enter();
     const int j = blockIdx.y;
     const uint2 *codes = p.codes[j];
     const float *scales = p.scales[j];
@@ -230,8 +233,8 @@ cudaError_t dequant_gather_impl(const int8_t *const *codes, const float *const *
     long long gx = (2LL * sm_count() * occ + n - 1) / n;
     if (gx > per_rank_need) gx = per_rank_need;
     if (gx < 1) gx = 1;
-    gather_dequant<MAXN, BF16><<<dim3((unsigned)gx, (unsigned)n), kQuantThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(gather_dequant<MAXN, BF16>, dim3((unsigned)gx, (unsigned)n), dim3(kQuantThreads), 0, stream,
+                      p);
 }
 
 template <bool BF16>
@@ -243,9 +246,8 @@ cudaError_t quantize_impl(const void *shard, int64_t len, int8_t *codes, float *
     const long long per_cta = (kQuantThreads / 32) * kQuantUnroll * 2;
     const long long need = (blocks + per_cta - 1) / per_cta;
     if (grid > need) grid = need;
-    quantize_shard_blocks<BF16><<<(unsigned)grid, kQuantThreads, 0, stream>>>(
-        static_cast<const uint4 *>(shard), reinterpret_cast<uint2 *>(codes), scales, blocks);
-    return cudaGetLastError();
+    return launch_pdl(quantize_shard_blocks<BF16>, dim3((unsigned)grid), dim3(kQuantThreads), 0, stream,
+                      static_cast<const uint4 *>(shard), reinterpret_cast<uint2 *>(codes), scales, blocks);
 }
 
 }  // namespace

@@ -325,37 +325,89 @@ def dist_setup(n_gpus):
     return 1, 0, 0, None
 
 
+def host_threads():
+    return max(1, min(os.cpu_count() or 1, 64))
+
+
+class OracleSample:
+    """The oracle as it stands over a sample of one partition, split into T
+    contiguous chunks run on T host threads (the oracle's C calls release the
+    GIL): per step every chunk is reduced, the chunks' sums of squares are
+    added in chunk order for the one decision, then every chunk is updated."""
+
+    def __init__(self, w, slices, master, loss_scale, threads):
+        import numpy as np
+        from concurrent.futures import ThreadPoolExecutor
+        self.w, self.S = w, loss_scale
+        M = slices[0].size
+        T = max(1, min(threads, M // 4096))
+        bounds = [(M * i // T) // 8 * 8 for i in range(T)] + [M]
+        self.chunks = [(bounds[i], bounds[i + 1]) for i in range(T) if bounds[i + 1] > bounds[i]]
+        self.slices = slices
+        self.master = master
+        self.m = np.zeros(M, np.float32)
+        self.v = np.zeros(M, np.float32)
+        self.g = np.empty(M, np.float32)
+        self.step_no = self.good = 0
+        self.pool = ThreadPoolExecutor(len(self.chunks))
+        self.threads = len(self.chunks)
+
+    def step(self):
+        import oracle
+        w = self.w
+
+        def red(c):
+            c0, c1 = c
+            _, ss, of = oracle.reduce([s[c0:c1] for s in self.slices], w.lp, self.S,
+                                      out=self.g[c0:c1])
+            return ss, of
+        parts = list(self.pool.map(red, self.chunks))
+        ss, of = 0.0, 0
+        for p_ss, p_of in parts:
+            ss += p_ss
+            of |= p_of
+        d = oracle.decide(ss, of, w.clip, self.S, self.step_no, self.good, w.growth_interval,
+                          w.beta1, w.beta2)
+
+        def upd(c):
+            c0, c1 = c
+            oracle.adam(self.g[c0:c1], self.master[c0:c1], self.m[c0:c1], self.v[c0:c1], w.lp,
+                        d["coef"], d["skip"], w.lr, w.beta1, w.beta2, w.eps, w.wd, int(w.adamw),
+                        d["bc1"], d["bc2"])
+        list(self.pool.map(upd, self.chunks))
+        self.step_no, self.good = d["step"], d["good_steps"]
+
+    def close(self):
+        self.pool.shutdown()
+
+
 def cpu_baseline(run, seconds):
-    """The oracle as it stands, single-threaded, on a bounded sample of the
-    same workload: the first M elements of the first simulated partition."""
-    import numpy as np
-    import oracle
+    """The oracle as it stands on a bounded sample of the same workload (the
+    first M elements of the first simulated partition, all N slices), on all
+    host cores."""
     from zero_partitioned_mixed_flat_gb300 import synth
     w = run.w
     r = run.ranks[0]
-    M = min(run.P, 1 << 21)
+    T = host_threads()
+    # up to 2^20 elements per thread, at most 512 MB of slices on the host
+    M = min(run.P, T << 20, (256 << 20) // w.n_ranks)
+    M -= M % 8
     if M == 0:
         return None
     sl = [synth.to_numpy_codes(run.slices[r][j, :M]) for j in range(w.n_ranks)]
-    master0 = run.master[r][:M].cpu().numpy().copy()
-    m = np.zeros(M, np.float32)
-    v = np.zeros(M, np.float32)
-    master = master0.copy()
+    o = OracleSample(w, sl, run.master[r][:M].cpu().numpy().copy(), run.S, T)
     reps, t0 = 0, time.perf_counter()
-    step, good = 0, 0
     while True:
-        g, ss, of = oracle.reduce(sl, w.lp, run.S)
-        d = oracle.decide(ss, of, w.clip, run.S, step, good, w.growth_interval, w.beta1, w.beta2)
-        oracle.adam(g, master, m, v, w.lp, d["coef"], d["skip"], w.lr, w.beta1, w.beta2, w.eps,
-                    w.wd, int(w.adamw), d["bc1"], d["bc2"])
-        step, good = d["step"], d["good_steps"]
+        o.step()
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds or el >= 30.0:
             break
-    return {"value": M * reps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+    o.close()
+    return {"value": M * reps / el, "unit": UNIT, "cores": o.threads, "kind": "oracle",
             "sample": "first %d elements of partition %d (all %d slices): reduce + decide + "
-                      "Adam, %d repetitions, %.1f s, single thread" % (M, r, w.n_ranks, reps, el)}
+                      "Adam, %d repetitions, %.1f s, %d host threads over contiguous chunks"
+                      % (M, r, w.n_ranks, reps, el, o.threads)}
 
 
 def run_reference(args):
@@ -370,7 +422,9 @@ def run_reference(args):
     w = WORKLOADS[args.workload]
     lay = oracle.layout(w.sizes, w.n_ranks, w.align, w.stage, w.unit_of_tensor)
     P = lay["part_len"]
-    M = min(P, 1 << 20)
+    T = host_threads()
+    M = min(P, T << 20, (256 << 20) // w.n_ranks)
+    M -= M % 8
     rng = np.random.default_rng(0)
     scale = w.loss_scale if w.grads_times_scale else 1.0
     vals = (rng.standard_normal((w.n_ranks, M)) * w.grad_std * scale).astype(np.float32)
@@ -379,35 +433,25 @@ def run_reference(args):
     else:
         sl = list(oracle.float_to_lp(vals, 1).reshape(w.n_ranks, M))
     master = (rng.standard_normal(M) * w.master_std).astype(np.float32)
-    m = np.zeros(M, np.float32)
-    v = np.zeros(M, np.float32)
-    step = good = 0
-
-    def one():
-        nonlocal step, good
-        g, ss, of = oracle.reduce(sl, w.lp, w.loss_scale)
-        d = oracle.decide(ss, of, w.clip, w.loss_scale, step, good, w.growth_interval,
-                          w.beta1, w.beta2)
-        oracle.adam(g, master, m, v, w.lp, d["coef"], d["skip"], w.lr, w.beta1, w.beta2, w.eps,
-                    w.wd, int(w.adamw), d["bc1"], d["bc2"])
-        step, good = d["step"], d["good_steps"]
-
+    o = OracleSample(w, sl, master, w.loss_scale, T)
     for _ in range(args.warmup):
-        one()
+        o.step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        one()
+        o.step()
     el = time.perf_counter() - t0
+    o.close()
     value = M * args.steps / el
     sample = ("%d of the %d elements of one partition, all %d slices, per step "
-              "(reduce + decide + Adam), single thread" % (M, P, w.n_ranks))
+              "(reduce + decide + Adam), %d host threads over contiguous chunks"
+              % (M, P, w.n_ranks, o.threads))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "sample_elements": M, "part_len": P,
                        "n_ranks": w.n_ranks, "stage": w.stage},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": o.threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}

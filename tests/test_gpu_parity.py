@@ -15,7 +15,7 @@ import zero_partitioned_mixed_flat_gb300 as Z
 from zero_partitioned_mixed_flat_gb300 import synth
 from zero_partitioned_mixed_flat_gb300.workloads import WORKLOADS, Workload
 
-from .zstep import Harness, same_floats
+from .zstep import Harness, max_rel_err, same_floats
 
 pytestmark = pytest.mark.gpu
 TILE = 4096
@@ -202,6 +202,39 @@ def test_nan_and_remote_terms(zlib):
     plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0)
     r = plan.result()
     assert r["skipped"] == 1 and torch.equal(before, w)
+    plan.close()
+
+
+@pytest.mark.parametrize("skips", [0, 3, 9])
+def test_bias_corrections_after_unread_skips(zlib, skips):
+    # the decision takes 1 - beta^t from a host table around the counter the
+    # host expects; skipped steps that were never read back move the device
+    # counter off that guess (9 skips: outside the table, computed on the
+    # device).  Every case must match the oracle's step at t = 501.
+    dev = torch.device("cuda")
+    n, part, b1, b2 = 2, 2 * TILE + 40, 0.9, 0.999
+    plan = _plan(n * part, n, 0)
+    plan.set_state(500)
+    sl = [synth.grad_slice(part, 0, 1e-2, 1.0, 4, 1, j, 0, dev) for j in range(n)]
+    g = torch.empty(part, device=dev)
+    w0 = synth.master_init(part, 0.02, 4, 0, dev)
+    w, m, v = w0.clone(), torch.full((part,), 1e-3, device=dev), torch.full((part,), 1e-6, device=dev)
+    m0, v0 = m.cpu().numpy().copy(), v.cpu().numpy().copy()
+    for _ in range(skips):   # remote overflow: skipped, counter unchanged, nothing read back
+        plan.reduce(0, sl, g, 1.0)
+        plan.adam(0, g, w, m, v, None, 1e-3, b1, b2, 1e-8, 0.01, 1, 1.0, 1.0, 0.0, 1)
+    plan.reduce(0, sl, g, 1.0)
+    plan.adam(0, g, w, m, v, None, 1e-3, b1, b2, 1e-8, 0.01, 1, 1.0, 1.0)
+    r = plan.result()
+    assert r["step"] == 501 and r["skipped"] == 0
+    host = [synth.to_numpy_codes(t) for t in sl]
+    og, oss, oof = oracle.reduce(host, 0, 1.0)
+    d = oracle.decide(oss, oof, 1.0, 1.0, 500, 0, 0, np.float32(b1), np.float32(b2))
+    ow, om, ov = w0.cpu().numpy().copy(), m0, v0
+    oracle.adam(og, ow, om, ov, 0, d["coef"], d["skip"], np.float32(1e-3), np.float32(b1),
+                np.float32(b2), np.float32(1e-8), np.float32(0.01), 1, d["bc1"], d["bc2"])
+    for got, exp in ((w, ow), (m, om), (v, ov)):
+        assert max_rel_err(got.cpu().numpy(), exp) <= 1e-6
     plan.close()
 
 

@@ -165,7 +165,19 @@ class Harness:
         w = self.w
         for r in self.ranks:
             s = self.st[r]
-            self.plan.reduce(r, s.slices, s.g, self.S, self.bucket)
+            if self.stage == 3 and w.gather:
+                # the benchmark's stage-3 schedule: units in reverse order, a
+                # bucket reduce-scattered once it holds bucket_elems (or at unit 0)
+                pending = []
+                for u in reversed(range(self.plan.n_units)):
+                    pending.append(u)
+                    elems = sum(self.plan.shard_len(v) for v in pending)
+                    if not self.bucket or elems >= self.bucket or u == 0:
+                        self.plan.reduce_units(r, min(pending), len(pending), s.slices, s.g,
+                                               self.S)
+                        pending = []
+            else:
+                self.plan.reduce(r, s.slices, s.g, self.S, self.bucket)
         for r in self.ranks:
             s = self.st[r]
             out = s.shard if self.stage == 3 else self.param

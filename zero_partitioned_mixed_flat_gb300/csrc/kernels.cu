@@ -253,6 +253,8 @@ struct DecideParams {
     float clip, loss_scale, beta1, beta2;
     int growth_interval;
     StepRecord *rec;
+    long long bc_t0;             // bc*_tab[i] is for step counter bc_t0 - i
+    float bc1_tab[kBcTable], bc2_tab[kBcTable];
     short slots[1024];   // the step's reduced partition slots, ascending
 };
 
@@ -278,15 +280,42 @@ __global__ void __launch_bounds__(kDecideThreads)
 norm_decide(const __grid_constant__ DecideParams p) {
     pdl_enter();
     __shared__ double wsum[kDecideThreads / 32];
+    __shared__ float bias_corr[2];
     __shared__ bool last;
+    StepRecord *rec = p.rec;
     {
         const int item = blockIdx.x;
         const int slot = p.slots[item / p.chunks_per_slot];
         const long long t0 = (long long)(item % p.chunks_per_slot) * kPartialChunk;
         const long long t1 = t0 + kPartialChunk < p.tiles_per_slot ? t0 + kPartialChunk : p.tiles_per_slot;
         const double *q = p.partials + (long long)slot * p.tiles_per_slot;
+        // every load first, then the adds in index order (a missing term adds 0)
+        constexpr int kPer = (int)(kPartialChunk / kDecideThreads);
+        double x[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const long long t = t0 + threadIdx.x + (long long)i * kDecideThreads;
+            x[i] = t < t1 ? q[t] : 0.0;
+        }
+        // bias corrections for t + 1 (the step counter if the step is not
+        // skipped): from the host's table when it holds that counter, else two
+        // lanes compute them in fp64 while the loads are in flight.  The record
+        // is written only by the last block, after every block has arrived, so
+        // every block reads the step's old t.
+        if (threadIdx.x == 32 || threadIdx.x == 64) {
+            const int b = threadIdx.x == 64;
+            const long long tn = rec->step + 1;
+            const long long i = p.bc_t0 - tn;
+            if (i >= 0 && i < kBcTable) {
+                bias_corr[b] = b ? p.bc2_tab[i] : p.bc1_tab[i];
+            } else {
+                const double beta = b ? (double)p.beta2 : (double)p.beta1;
+                bias_corr[b] = __double2float_rn(__dsub_rn(1.0, pow(beta, (double)tn)));
+            }
+        }
         double acc = 0.0;
-        for (long long t = t0 + threadIdx.x; t < t1; t += kDecideThreads) acc = __dadd_rn(acc, q[t]);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) acc = __dadd_rn(acc, x[i]);
         const double chunk = block_sum_fixed(acc, wsum);
         if (threadIdx.x == 0) {
             p.level2[item] = chunk;
@@ -304,7 +333,6 @@ norm_decide(const __grid_constant__ DecideParams p) {
     if (threadIdx.x != 0) return;
     *p.arrivals = 0u;
 
-    StepRecord *rec = p.rec;
     sumsq = p.use_global ? p.global_sumsq : __dadd_rn(sumsq, p.remote_sumsq);
     const double norm = sqrt(sumsq);
     const int skip = (rec->overflow != 0u) || (p.remote_overflow != 0);
@@ -334,8 +362,10 @@ norm_decide(const __grid_constant__ DecideParams p) {
     rec->loss_scale = s;
     rec->good_steps = good;
     rec->step = t;
-    rec->bc1 = __double2float_rn(__dsub_rn(1.0, pow((double)p.beta1, (double)t)));
-    rec->bc2 = __double2float_rn(__dsub_rn(1.0, pow((double)p.beta2, (double)t)));
+    if (!skip) {  // a skipped step keeps the previous corrections (Adam does not run)
+        rec->bc1 = bias_corr[0];
+        rec->bc2 = bias_corr[1];
+    }
 }
 
 // ------------------------------------------------- TMA / mbarrier primitives
@@ -819,7 +849,8 @@ cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp, 
                                              stream);
 }
 
-cudaError_t launch_decide(const double *partials, double *level2, unsigned *arrivals, int64_t tiles_per_slot,
+cudaError_t launch_decide(const double *partials, double *level2, unsigned *arrivals, int64_t bc_t0,
+                          const float *bc1_tab, const float *bc2_tab, int64_t tiles_per_slot,
                           const uint64_t *active_mask, int n_slots, double remote_sumsq, int remote_overflow,
                           int use_global, double global_sumsq, float clip, float loss_scale,
                           int growth_interval, float beta1, float beta2, StepRecord *rec,
@@ -846,6 +877,11 @@ cudaError_t launch_decide(const double *partials, double *level2, unsigned *arri
     p.beta2 = beta2;
     p.growth_interval = growth_interval;
     p.rec = rec;
+    p.bc_t0 = bc_t0;
+    for (int i = 0; i < kBcTable; ++i) {
+        p.bc1_tab[i] = bc1_tab[i];
+        p.bc2_tab[i] = bc2_tab[i];
+    }
     return launch_pdl(norm_decide, dim3((unsigned)p.n_items), dim3(kDecideThreads), 0, stream, p);
 }
 

@@ -71,6 +71,9 @@ struct zero_plan {
     int32_t growth_interval = 1000;
     int32_t reduce_lp_accum = 0;  // 1: partial sums rounded to the lp type
     int64_t spin_limit = kDefaultSpinLimit;
+    // the device step counter as far as the host can tell without reading it:
+    // the last value read back or set, plus one per decision launched since
+    int64_t t_hint = 0;
     bool use_global = false;  // zero_step_set_global_stats was called this step
     double global_sumsq = 0.0;
     int32_t global_overflow = 0;
@@ -361,6 +364,7 @@ zero_status zero_plan_set_state(zero_plan *p, int64_t step, int32_t good_steps) 
     rec.good_steps = good_steps;
     e = cudaMemcpy(p->d_rec, &rec, sizeof rec, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step record)");
+    p->t_hint = step;
     return ZERO_OK;
 }
 
@@ -547,13 +551,24 @@ zero_status adam_impl(zero_plan *p, int32_t rank, int64_t begin, int64_t len, co
         for (uint64_t w : p->active) any = any || w != 0;
         if (!any) return fail(ZERO_ESTATE, "no partition was reduced in the current step");
         const int r_of = p->use_global ? (p->global_overflow ? 1 : 0) : (remote_overflow ? 1 : 0);
-        cudaError_t e = zk::launch_decide(p->d_partials, p->d_level2, &p->d_rec->arrivals, p->tiles_per_part,
-                                          p->active, p->slots,
+        // bias corrections, computed as the oracle does, for the counters
+        // t_hint + 1 down to t_hint + 2 - kBcTable (t_hint + 1 unless earlier
+        // steps were skipped since the counter was last read back)
+        const int64_t bc_t0 = p->t_hint + 1;
+        float bc1[zk::kBcTable], bc2[zk::kBcTable];
+        for (int i = 0; i < zk::kBcTable; ++i) {
+            const int64_t t = bc_t0 - i;
+            bc1[i] = t > 0 ? float(1.0 - std::pow(double(beta1), double(t))) : 0.0f;
+            bc2[i] = t > 0 ? float(1.0 - std::pow(double(beta2), double(t))) : 0.0f;
+        }
+        cudaError_t e = zk::launch_decide(p->d_partials, p->d_level2, &p->d_rec->arrivals, bc_t0, bc1, bc2,
+                                          p->tiles_per_part, p->active, p->slots,
                                           remote_sumsq, r_of, p->use_global ? 1 : 0,
                                           p->global_sumsq, clip, loss_scale, p->growth_interval,
                                           beta1, beta2, p->d_rec, s);
         if (e != cudaSuccess) return cuda_fail(e, "decide kernel launch");
         p->phase = kDecided;
+        p->t_hint += 1;
     }
     if (len == 0) return ZERO_OK;
     const float omb1 = 1.0f - beta1;
@@ -609,6 +624,7 @@ zero_status zero_step_result(zero_plan *p, double *norm, int32_t *skipped, float
     zk::StepRecord rec;
     e = cudaMemcpy(&rec, p->d_rec, sizeof rec, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step record)");
+    p->t_hint = rec.step;
     if (norm) *norm = rec.norm;
     if (skipped) *skipped = rec.skip;
     if (new_loss_scale) *new_loss_scale = rec.loss_scale;

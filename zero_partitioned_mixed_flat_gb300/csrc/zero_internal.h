@@ -53,8 +53,14 @@ cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp,
                           const ReduceSegment *segs, int n_segs, float inv, float *g,
                           double *partials, unsigned *overflow, cudaStream_t stream);
 
+// Bias corrections computed on the host for the step counters the decision
+// is likely to reach: entry i is for t = bc_t0 - i (1 - beta^t in fp64, then
+// rounded to float).  A counter outside the table is computed on the device.
+constexpr int kBcTable = 8;
+
 // level2: scratch for n_slots * ceil(tiles_per_slot / kPartialChunk) doubles
 cudaError_t launch_decide(const double *partials, double *level2, unsigned *arrivals,
+                          int64_t bc_t0, const float *bc1_tab, const float *bc2_tab,
                           int64_t tiles_per_slot,
                           const uint64_t *active_mask, int n_slots,
                           double remote_sumsq, int remote_overflow,

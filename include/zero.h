@@ -269,6 +269,24 @@ zero_status zero_gather_layer(zero_plan *plan, int32_t unit,
                               void *stream);
 
 /* ----------------------------------------------------------------------
+ * Stage-1/2 parameter all-gather after the update ("10.6 ZeRO 与 FSDP"
+ * §10.6.2 Step 4: every rank's updated partition is all-gathered into the
+ * full parameter layout), in buckets ("从'年糕切片'理解ZeRO" §4.2, the
+ * ds_config key allgather_bucket_size).
+ * partitions: N device pointers, partitions[j] = rank j's P updated lp
+ * parameters (e.g. its range of its own full-layout buffer: out may be one
+ * of them, partitions[j] == out + j*P gathers in place).  out: the Ψ_p-element
+ * full layout (device):  out[j*P + k] = partitions[j][k],  k < P.
+ * bucket_elems <= 0: one launch; else launches of N runs of
+ * max(8, floor(bucket_elems / N / 8) * 8) elements each (one bucket of about
+ * bucket_elems elements), in partition order.  Same TMA bulk copies and
+ * bounded waits as zero_gather_layer.  Stage-1/2 plans only (ZERO_EINVAL);
+ * pointers must be 16-byte aligned (ZERO_EALIGN).  Asynchronous on stream.
+ */
+zero_status zero_allgather_params(zero_plan *plan, const void *const *partitions,
+                                  void *out, int64_t bucket_elems, void *stream);
+
+/* ----------------------------------------------------------------------
  * Quantized stage-3 gather ("ZeRO-1/2/3 vs DDP" note, ZeRO++: the
  * all-gathered parameters are quantized to cut the traffic).  Stage-3 plans
  * whose align is a multiple of ZERO_QUANT_BLOCK.

@@ -156,6 +156,12 @@ def test_step_calls_validate_before_touching_the_device(lib):
         with pytest.raises(Z.ZeroError) as e:
             Z.zero_gather_layer(plan, 0, [buf, buf], buf, stream=0)
         assert e.value.code == Z.ZERO_EINVAL                     # not a stage-3 plan
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_allgather_params(plan, [buf, buf + 8], buf, 0, stream=0)
+        assert e.value.code == Z.ZERO_EALIGN                     # misaligned partition
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_allgather_params(plan, [buf, None], buf, 0, stream=0)
+        assert e.value.code == Z.ZERO_EINVAL                     # NULL partition
         with pytest.raises(Z.ZeroError):
             Z.zero_plan_fragments(plan, 5)
         assert "rank" in Z.zero_last_error()
@@ -169,5 +175,8 @@ def test_step_calls_validate_before_touching_the_device(lib):
         with pytest.raises(Z.ZeroError) as e:
             Z.zero_gather_layer(p3, 0, [1 << 20, (1 << 20) + 8], 1 << 20, stream=0)
         assert e.value.code == Z.ZERO_EALIGN
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_allgather_params(p3, [1 << 20, 1 << 20], 1 << 20, 0, stream=0)
+        assert e.value.code == Z.ZERO_EINVAL                     # stage 3: layer gathers
     finally:
         Z.zero_plan_destroy(p3)

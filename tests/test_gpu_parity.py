@@ -320,6 +320,30 @@ def test_gather_wait_timeout_is_reported_and_recoverable(zlib):
     plan2.close()
 
 
+@pytest.mark.parametrize("n,lp,bucket", [(2, 0, 0), (3, 1, 4096), (8, 0, 1000), (64, 1, 200_000),
+                                         (5, 0, 8)])
+def test_allgather_params_buckets(zlib, n, lp, bucket):
+    # stage-1/2 step-end all-gather of the updated partitions into the full
+    # layout, in buckets (allgather_bucket_size): a concatenation, bit for bit
+    dev = torch.device("cuda")
+    P = 2 * TILE + 8 * (n + 1)
+    plan = _plan(n * P, n, lp, stage=2)
+    assert plan.part_len == P
+    parts = [synth.lp_shard(P, lp, 0.02, 6, j, dev) for j in range(n)]
+    out = torch.full((n * P,), 7, dtype=synth.LP_DTYPES[lp], device=dev)
+    plan.allgather(parts, out, bucket)
+    plan.check()
+    exp = oracle.gather([synth.to_numpy_codes(t) for t in parts])
+    assert np.array_equal(synth.to_numpy_codes(out), exp)
+    # in place: each rank's source is its own range of the output
+    full = torch.full((n * P,), 5, dtype=synth.LP_DTYPES[lp], device=dev)
+    full[:P].copy_(parts[0])
+    plan.allgather([full[:P]] + parts[1:], full, bucket)
+    plan.check()
+    assert np.array_equal(synth.to_numpy_codes(full), exp)
+    plan.close()
+
+
 def test_global_stats_replace_the_local_sum(zlib):
     # multi-rank use: the caller's global totals decide the step exactly
     dev = torch.device("cuda")

@@ -8,7 +8,8 @@ used for device memory and streams.
 from ._abi import (  # noqa: F401
     LIB_PATH, SIGNATURES, STATUS_NAMES, ZERO_BF16, ZERO_EALIGN, ZERO_ECUDA, ZERO_EINVAL,
     ZERO_ENOMEM, ZERO_ESTATE, ZERO_ETIMEOUT, ZERO_FP16, ZERO_MAX_RANKS, ZERO_OK, ZeroError,
-    load, zero_adam_step, zero_adam_step_range, zero_gather_layer, zero_last_error,
+    load, zero_adam_step, zero_adam_step_range, zero_allgather_params, zero_gather_layer,
+    zero_last_error,
     zero_memory_report, zero_partition_stats, zero_plan_check, zero_plan_create,
     zero_plan_destroy, zero_plan_fragments, zero_plan_query, zero_plan_set_loss_scaler,
     zero_plan_set_spin_limit, zero_plan_set_state, zero_plan_set_reduce_precision,

@@ -43,6 +43,7 @@ SIGNATURES = {
     "zero_step_result": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "zero_plan_check": (_i32, [_vp]),
     "zero_gather_layer": (_i32, [_vp, _i32, _vp, _vp, _vp]),
+    "zero_allgather_params": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "zero_quantize_shard": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "zero_gather_layer_quantized": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     "zero_reduce_partition_noalloc": (_i32, [_i32, _i32, _vp, _i64, _f32, _vp, _vp, _vp, _vp]),
@@ -237,6 +238,13 @@ def zero_plan_check(plan: int):
 def zero_gather_layer(plan: int, unit: int, shards: Sequence, out, stream=None):
     _check(load().zero_gather_layer(plan, unit, C.cast(_ptr_array(shards), _vp), _ptr(out),
                                     _stream(stream)), "zero_gather_layer")
+
+
+def zero_allgather_params(plan: int, partitions: Sequence, out, bucket_elems: int = 0,
+                          stream=None):
+    _check(load().zero_allgather_params(plan, C.cast(_ptr_array(partitions), _vp), _ptr(out),
+                                        int(bucket_elems), _stream(stream)),
+           "zero_allgather_params")
 
 
 ZERO_QUANT_BLOCK = 128

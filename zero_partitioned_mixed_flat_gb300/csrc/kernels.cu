@@ -651,7 +651,8 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
 template <int MAXN>
 struct GatherParams {
     const char *src[MAXN];  // shard j at this unit's offset
-    char *dst;
+    char *dst;              // rank j's bytes go to dst + j * dst_stride
+    long long dst_stride;
     long long shard_bytes;
     long long chunks_per_shard;
     long long n_chunks;
@@ -680,7 +681,7 @@ gather_layer_tma(const __grid_constant__ GatherParams<MAXN> p) {
         const long long rem = p.shard_bytes - off;
         bytes = rem < (long long)kGatherChunk ? (uint32_t)rem : kGatherChunk;
         src = p.src[j] + off;
-        dst = p.dst + j * p.shard_bytes + off;
+        dst = p.dst + j * p.dst_stride + off;
     };
     auto issue = [&](long long k) {
         const char *src;
@@ -792,11 +793,12 @@ cudaError_t adam_tma_impl(const AdamTmaParams &p, cudaStream_t stream) {
 
 template <int MAXN>
 cudaError_t gather_impl(const void *const *shards, int n, int64_t src_off, int64_t shard_bytes,
-                        void *out, int64_t spin_limit, int *error, cudaStream_t stream) {
+                        void *out, int64_t dst_stride, int64_t spin_limit, int *error, cudaStream_t stream) {
     GatherParams<MAXN> p;
     for (int j = 0; j < n; ++j) p.src[j] = static_cast<const char *>(shards[j]) + src_off;
     for (int j = n; j < MAXN; ++j) p.src[j] = nullptr;
     p.dst = static_cast<char *>(out);
+    p.dst_stride = dst_stride;
     p.shard_bytes = shard_bytes;
     p.chunks_per_shard = (shard_bytes + kGatherChunk - 1) / kGatherChunk;
     p.n_chunks = p.chunks_per_shard * n;
@@ -911,11 +913,13 @@ cudaError_t launch_adam(const float *g, float *master, float *m, float *v, void 
 }
 
 cudaError_t launch_gather(const void *const *shards, int n, int64_t src_offset_bytes,
-                          int64_t shard_bytes, void *out, int64_t spin_limit, int *error,
-                          cudaStream_t stream) {
+                          int64_t shard_bytes, void *out, int64_t dst_stride_bytes, int64_t spin_limit,
+                          int *error, cudaStream_t stream) {
     if (n <= 64)
-        return gather_impl<64>(shards, n, src_offset_bytes, shard_bytes, out, spin_limit, error, stream);
-    return gather_impl<1024>(shards, n, src_offset_bytes, shard_bytes, out, spin_limit, error, stream);
+        return gather_impl<64>(shards, n, src_offset_bytes, shard_bytes, out, dst_stride_bytes, spin_limit,
+                               error, stream);
+    return gather_impl<1024>(shards, n, src_offset_bytes, shard_bytes, out, dst_stride_bytes, spin_limit,
+                             error, stream);
 }
 
 }  // namespace zk

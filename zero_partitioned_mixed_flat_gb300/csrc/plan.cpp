@@ -658,9 +658,37 @@ zero_status zero_gather_layer(zero_plan *p, int32_t unit, const void *const *sha
     if (st != ZERO_OK) return st;
     int64_t off = 0;  // the unit's shard offset inside each rank's partition
     for (int32_t u = 0; u < unit; ++u) off += p->shard_len(u);
-    cudaError_t e = zk::launch_gather(shards, p->n_ranks, off * 2, shard * 2, out, p->spin_limit,
+    cudaError_t e = zk::launch_gather(shards, p->n_ranks, off * 2, shard * 2, out, shard * 2, p->spin_limit,
                                       &p->d_rec->error, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+    return ZERO_OK;
+}
+
+zero_status zero_allgather_params(zero_plan *p, const void *const *partitions, void *out,
+                                  int64_t bucket_elems, void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (p->stage != 1 && p->stage != 2) return fail(ZERO_EINVAL, "zero_allgather_params needs a stage-1 or 2 plan");
+    if (!partitions || (!out && p->part > 0)) return fail(ZERO_EINVAL, "NULL partitions or output");
+    for (int32_t j = 0; j < p->n_ranks; ++j) {
+        if (!partitions[j] && p->part > 0) return fail(ZERO_EINVAL, "partitions[%d] is NULL", j);
+        if (!aligned16(partitions[j])) return fail(ZERO_EALIGN, "partitions[%d] is not 16-byte aligned", j);
+    }
+    if (!aligned16(out)) return fail(ZERO_EALIGN, "out is not 16-byte aligned");
+    zero_status st = ensure_device(p);
+    if (st != ZERO_OK) return st;
+    // per-rank run of one bucket: bucket_elems / N, a multiple of 8, at least 8
+    int64_t run = p->part;
+    if (bucket_elems > 0) {
+        run = bucket_elems / p->n_ranks / 8 * 8;
+        if (run < 8) run = 8;
+    }
+    for (int64_t k0 = 0; k0 < p->part; k0 += run) {
+        const int64_t len = std::min(run, p->part - k0);
+        cudaError_t e = zk::launch_gather(partitions, p->n_ranks, k0 * 2, len * 2,
+                                          static_cast<uint16_t *>(out) + k0, p->part * 2, p->spin_limit,
+                                          &p->d_rec->error, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+    }
     return ZERO_OK;
 }
 

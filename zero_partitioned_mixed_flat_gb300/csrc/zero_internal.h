@@ -74,9 +74,10 @@ cudaError_t launch_adam(const float *g, float *master, float *m, float *v,
                         float beta2, float omb1, float omb2, float eps,
                         float wd, float decay, int adamw, cudaStream_t stream);
 
+// out + j * dst_stride_bytes + [0, shard_bytes) <- shards[j] + src_offset_bytes + [0, shard_bytes)
 cudaError_t launch_gather(const void *const *shards, int n, int64_t src_offset_bytes,
-                          int64_t shard_bytes, void *out, int64_t spin_limit,
-                          int *error, cudaStream_t stream);
+                          int64_t shard_bytes, void *out, int64_t dst_stride_bytes,
+                          int64_t spin_limit, int *error, cudaStream_t stream);
 
 // quantized all-gather (block = 128 elements): shard -> int8 codes + scales;
 // codes/scales of N ranks at a unit's offset -> lp layer buffer

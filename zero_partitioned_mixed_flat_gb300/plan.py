@@ -89,6 +89,9 @@ class ZeroPlan:
     def gather(self, unit, shards, out, stream=None):
         A.zero_gather_layer(self.handle, unit, shards, out, stream)
 
+    def allgather(self, partitions, out, bucket_elems=0, stream=None):
+        A.zero_allgather_params(self.handle, partitions, out, bucket_elems, stream)
+
     def quantize(self, shard, codes, scales, stream=None):
         A.zero_quantize_shard(self.handle, shard, codes, scales, stream)
 

@@ -28,7 +28,11 @@
  *    except the ones documented as synchronising.
  *  - Errors are returned as zero_status codes; nothing is thrown.
  *    zero_last_error() gives a message for the last failure on the calling
- *    thread.  On an error, no device work has been enqueued by that call.
+ *    thread.  On an argument or state error, no device work has been
+ *    enqueued by that call (a call that launches several kernels and meets a
+ *    CUDA launch failure part-way may have enqueued the earlier ones).
+ *  - A plan holds host-side step state: calls on one plan must not run
+ *    concurrently from several host threads; different plans are independent.
  *  - Low-precision ("lp") values are IEEE binary16 (ZERO_FP16) or bfloat16
  *    (ZERO_BF16), chosen per plan.
  */

@@ -45,7 +45,7 @@ def _reduce_case(zlib, n, part, lp, scale, bucket=0, rank=0, seed=0, acc_lp=Fals
     return g, ss
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 5, 16, 17, 64, 65, 130])
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 16, 17, 64, 65, 130, Z.ZERO_MAX_RANKS])
 @pytest.mark.parametrize("lp", [0, 1])
 def test_reduce_ragged_and_wide(zlib, n, lp):
     # 3 whole norm tiles plus a ragged tail of 136 elements
@@ -145,6 +145,41 @@ def test_tiny_variants(zlib, kw):
     for _ in range(2):
         h.step()
     h.close()
+
+
+def test_all_ranks_of_a_maximal_plan_in_one_step(zlib):
+    # N = ZERO_MAX_RANKS partitions reduced on one plan: one decision over all
+    # 1024 partitions' partials, then every partition updated with it
+    n, part, lr, b1, b2, eps, wd = Z.ZERO_MAX_RANKS, 16, 1e-3, 0.9, 0.999, 1e-8, 0.01
+    dev = torch.device("cuda")
+    plan = _plan(n * part, n, 0)
+    assert plan.part_len == part
+    big = synth.grad_slice(n * n * part, 0, 1e-2, 1.0, 5, 1, 0, 0, dev).view(n, n, part)
+    base, row = big.data_ptr(), part * 2        # slice j of rank r: big[r, j]
+    g = torch.empty((n, part), dtype=torch.float32, device=dev)
+    w0 = synth.master_init(n * part, 0.02, 5, 0, dev).view(n, part)
+    w, m, v = w0.clone(), torch.zeros_like(w0), torch.zeros_like(w0)
+    for r in range(n):
+        plan.reduce(r, [base + (r * n + j) * row for j in range(n)], g[r], 1.0)
+    for r in range(n):
+        plan.adam(r, g[r], w[r], m[r], v[r], None, lr, b1, b2, eps, wd, 1, 1.0, 0.05)
+    res = plan.result()
+    host = synth.to_numpy_codes(big.reshape(-1)).reshape(n, n, part)
+    og = np.empty((n, part), np.float32)
+    ss = 0.0
+    for r in range(n):
+        og[r], r_ss, r_of = oracle.reduce(list(host[r]), 0, 1.0)
+        ss += r_ss
+        assert r_of == 0
+    assert same_floats(g.cpu().numpy(), og)
+    d = oracle.decide(ss, 0, np.float32(0.05), 1.0, 0, 0, 1000, np.float32(b1), np.float32(b2))
+    assert abs(res["norm"] - d["norm"]) <= 1e-5 * d["norm"] and res["step"] == 1
+    ow, om, ov = w0.cpu().numpy().reshape(-1).copy(), np.zeros(n * part, np.float32), np.zeros(n * part, np.float32)
+    oracle.adam(og.reshape(-1), ow, om, ov, 0, d["coef"], d["skip"], np.float32(lr), np.float32(b1),
+                np.float32(b2), np.float32(eps), np.float32(wd), 1, d["bc1"], d["bc2"])
+    for got, exp in ((w, ow), (m, om), (v, ov)):
+        assert max_rel_err(got.cpu().numpy().reshape(-1), exp) <= 1e-6
+    plan.close()
 
 
 @pytest.mark.parametrize("sub_group", [8, 40_000, 1 << 20])
@@ -285,7 +320,7 @@ def _gather_case(n, sizes, units, lp=0, align=8, spin=None):
     return plan, outs
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 64, 65])
+@pytest.mark.parametrize("n", [1, 2, 3, 64, 65, Z.ZERO_MAX_RANKS])
 def test_gather_units(zlib, n):
     sizes = [1000, 24, 4096 * 9 + 8, 5, 16384 * 3, 100_000]
     units = [0, 0, 1, 2, 2, 3]
@@ -403,7 +438,7 @@ def _quant_case(n, sizes, units, lp):
     plan.close()
 
 
-@pytest.mark.parametrize("n", [2, 3, 64, 65])
+@pytest.mark.parametrize("n", [2, 3, 64, 65, Z.ZERO_MAX_RANKS])
 @pytest.mark.parametrize("lp", [0, 1])
 def test_quantize_and_dequant_gather(zlib, n, lp):
     _quant_case(n, [5000, 128, 40_000, 3, 70_000], [0, 0, 1, 2, 2], lp)

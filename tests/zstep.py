@@ -185,7 +185,10 @@ class Harness:
                 self.plan.adam(r, s.g, s.master, s.m, s.v, out, w.lr, w.beta1, w.beta2, w.eps,
                                w.wd, int(w.adamw), self.S, w.clip)
                 continue
+            # an empty range first (it only takes the decision), then the
             # sub-groups in reverse order, the last one ragged
+            self.plan.adam_range(r, 0, 0, s.g, s.master, s.m, s.v, out, w.lr, w.beta1, w.beta2,
+                                 w.eps, w.wd, int(w.adamw), self.S, w.clip)
             for b in reversed(range(0, self.P, self.sub_group)):
                 n = min(self.sub_group, self.P - b)
                 self.plan.adam_range(r, b, n, s.g, s.master, s.m, s.v, out, w.lr, w.beta1,

@@ -285,18 +285,34 @@ class Run:
                             lambda r=r: self.plan.reduce(r, lists[r], self.g[r], self.S,
                                                          w.bucket_elems, sh), stream))
         for i, r in enumerate(self.ranks):
-            out.append(("adam", 30 * P, 1 + (i == 0), lambda r=r: self._adam(r, sh), stream))
+            if i == 0:
+                # the step's one decision (norm of every reduced partition,
+                # clip, skip, loss scale, t) as its own call: an empty Adam range
+                out.append(("decide", 8 * self.tiles_per_part() * len(self.ranks), 1,
+                            lambda r=r: self._adam(r, sh, decide_only=True), stream))
+            out.append(("adam", 30 * P, 1, lambda r=r: self._adam(r, sh), stream))
             if self.quantized:
                 out.append(("quantize", int((3 + 4 / 128) * P), 1,
                             lambda r=r: self.plan.quantize(self.shard[r], self.codes[r],
                                                            self.scales[r], sh), stream))
         return out
 
-    def _adam(self, r, stream):
+    def _adam(self, r, stream, decide_only=False):
         w = self.w
         out = self.shard[r] if w.stage == 3 else self.param
+        if decide_only:
+            self.plan.adam_range(r, 0, 0, self.g[r], self.master[r], self.m[r], self.v[r], out,
+                                 w.lr, w.beta1, w.beta2, w.eps, w.wd, int(w.adamw), self.S, w.clip,
+                                 0.0, 0, stream)
+            return
         self.plan.adam(r, self.g[r], self.master[r], self.m[r], self.v[r], out, w.lr, w.beta1,
                        w.beta2, w.eps, w.wd, int(w.adamw), self.S, w.clip, 0.0, 0, stream)
+
+    def tiles_per_part(self):
+        """Norm tiles (4096 elements) of one partition: per unit shard in stage 3."""
+        if self.w.stage == 3:
+            return sum(-(-self.plan.shard_len(u) // 4096) for u in range(self.plan.n_units))
+        return -(-self.P // 4096)
 
     def launches_per_step(self):
         import torch
@@ -615,7 +631,7 @@ def main():
     b = bytes_per_element(w.n_ranks)
     # dominant kernel = the one with the largest share of the step
     dom = max(t_kind, key=t_kind.get)
-    kname = {"reduce": "reduce_unscale_stats", "adam": "adam_fused_cast",
+    kname = {"reduce": "reduce_unscale_stats", "adam": "adam_fused_cast", "decide": "norm_decide",
              "gather": "gather_dequant" if run.quantized else "gather_layer_tma",
              "quantize": "quantize_shard_blocks"}[dom]
     achieved = b_kind[dom] / (t_kind[dom] / 1e3) / 1e9

@@ -260,14 +260,29 @@ struct DecideParams {
 
 constexpr int kDecideThreads = 256;
 
-__device__ __forceinline__ double block_sum_fixed(double acc, double *wsum) {
+// fp64 adds are slow on this part (a 64-cycle latency, under 2 per cycle per
+// SM), so every fixed-order sum here is a tree, never a long chain.
+__device__ __forceinline__ double warp_sum_fixed(double acc) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+    return acc;  // lane 0's value is the one used
+}
+
+__device__ __forceinline__ double block_sum_fixed(double acc, double *wsum) {
+    acc = warp_sum_fixed(acc);
     if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = acc;
     __syncthreads();
     double t = 0.0;
-    if (threadIdx.x == 0)
-        for (int w = 0; w < kDecideThreads / 32; ++w) t = __dadd_rn(t, wsum[w]);
+    if (threadIdx.x == 0) {  // pairwise over the warps
+        double w[kDecideThreads / 32];
+#pragma unroll
+        for (int i = 0; i < kDecideThreads / 32; ++i) w[i] = wsum[i];
+#pragma unroll
+        for (int h = kDecideThreads / 64; h >= 1; h >>= 1)
+#pragma unroll
+            for (int i = 0; i < h; ++i) w[i] = __dadd_rn(w[i], w[i + h]);
+        t = w[0];
+    }
     return t;  // valid in thread 0
 }
 
@@ -289,8 +304,10 @@ norm_decide(const __grid_constant__ DecideParams p) {
         const long long t0 = (long long)(item % p.chunks_per_slot) * kPartialChunk;
         const long long t1 = t0 + kPartialChunk < p.tiles_per_slot ? t0 + kPartialChunk : p.tiles_per_slot;
         const double *q = p.partials + (long long)slot * p.tiles_per_slot;
-        // every load first, then the adds in index order (a missing term adds 0)
+        // every load first, then a pairwise tree (a missing term adds 0)
         constexpr int kPer = (int)(kPartialChunk / kDecideThreads);
+        static_assert((kPer & (kPer - 1)) == 0 && ((kDecideThreads / 32) & (kDecideThreads / 32 - 1)) == 0,
+                      "pairwise trees need powers of two");
         double x[kPer];
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
@@ -313,10 +330,11 @@ norm_decide(const __grid_constant__ DecideParams p) {
                 bias_corr[b] = __double2float_rn(__dsub_rn(1.0, pow(beta, (double)tn)));
             }
         }
-        double acc = 0.0;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) acc = __dadd_rn(acc, x[i]);
-        const double chunk = block_sum_fixed(acc, wsum);
+        for (int h = kPer / 2; h >= 1; h >>= 1)  // pairwise within the thread
+#pragma unroll
+            for (int i = 0; i < h; ++i) x[i] = __dadd_rn(x[i], x[i + h]);
+        const double chunk = block_sum_fixed(x[0], wsum);
         if (threadIdx.x == 0) {
             p.level2[item] = chunk;
             __threadfence();
@@ -326,10 +344,16 @@ norm_decide(const __grid_constant__ DecideParams p) {
     }
     if (!last) return;
     __threadfence();
-    double acc = 0.0;
-    for (int t = threadIdx.x; t < p.n_items; t += kDecideThreads) acc = __dadd_rn(acc, __ldcg(p.level2 + t));
-    __syncthreads();  // wsum is reused
-    double sumsq = block_sum_fixed(acc, wsum);
+    double sumsq;
+    if (p.n_items <= 32) {  // one warp: item l in lane l, then the warp tree
+        if (threadIdx.x >= 32) return;
+        sumsq = warp_sum_fixed((int)threadIdx.x < p.n_items ? __ldcg(p.level2 + threadIdx.x) : 0.0);
+    } else {
+        double acc = 0.0;
+        for (int t = threadIdx.x; t < p.n_items; t += kDecideThreads) acc = __dadd_rn(acc, __ldcg(p.level2 + t));
+        __syncthreads();  // wsum is reused
+        sumsq = block_sum_fixed(acc, wsum);
+    }
     if (threadIdx.x != 0) return;
     *p.arrivals = 0u;
 

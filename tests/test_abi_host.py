@@ -5,6 +5,7 @@ statically), exports every entry point include/zero.h declares, and its
 partitioner and accounting agree with the independent oracle bit for bit.
 Argument validation happens before any device call, so it is tested here.
 """
+import ctypes as C
 import os
 import random
 import re
@@ -37,6 +38,40 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert sorted(Z.SIGNATURES) == names   # the binding covers exactly the ABI
+
+
+def _prototypes():
+    """name -> (return type, [parameter types]) of every function declared in
+    include/zero.h, with the C types reduced to what a call passes."""
+    text = open(os.path.join(ROOT, "include", "zero.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    protos = {}
+    for ret, name, args in re.findall(
+            r"(zero_status|void|const char \*)\s*\b(zero_[a-z_]+)\s*\(([^)]*)\)\s*;", text):
+        kinds = []
+        for a in [x.strip() for x in args.split(",") if x.strip() and x.strip() != "void"]:
+            a = re.sub(r"\[[^]]*\]", "*", a)              # array parameters are pointers
+            if "*" in a:
+                kinds.append("ptr")
+            else:
+                kinds.append(a.split()[0].replace("const", "").strip() or a.split()[1])
+        protos[name] = (ret.replace(" ", ""), kinds)
+    return protos
+
+
+_CTYPES = {"ptr": (C.c_void_p,), "int32_t": (C.c_int32,), "int64_t": (C.c_int64,),
+           "float": (C.c_float,), "double": (C.c_double,), "zero_lp": (C.c_int32,)}
+
+
+def test_binding_signatures_match_the_header():
+    protos = _prototypes()
+    assert sorted(protos) == sorted(Z.SIGNATURES)
+    for name, (ret, kinds) in protos.items():
+        cret, cargs = Z.SIGNATURES[name]
+        assert len(cargs) == len(kinds), name
+        for i, (k, c) in enumerate(zip(kinds, cargs)):
+            assert c in _CTYPES[k], (name, i, k, c)
+        assert {"zero_status": C.c_int32, "void": None, "constchar*": C.c_char_p}[ret] == cret, name
 
 
 def _cmp_layout(orc, sizes, n, align, stage, units):

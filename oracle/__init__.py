@@ -70,6 +70,14 @@ def lib():
         L.orc_dequant_gather.restype = None
         L.orc_gather.argtypes = [_i32, _vp, _i64, _vp]
         L.orc_gather.restype = None
+        L.orc_e4m3_decode_array.argtypes = [_i64, _vp, _vp]
+        L.orc_e4m3_decode_array.restype = None
+        L.orc_e4m3_encode_array.argtypes = [_i64, _vp, _vp]
+        L.orc_e4m3_encode_array.restype = None
+        L.orc_quantize_blocks_fp8.argtypes = [_i64, _vp, _i32, _i32, _vp, _vp]
+        L.orc_quantize_blocks_fp8.restype = None
+        L.orc_dequant_gather_fp8.argtypes = [_i32, _vp, _vp, _i64, _i32, _i32, _vp]
+        L.orc_dequant_gather_fp8.restype = None
         _LIB = L
     return _LIB
 
@@ -231,8 +239,42 @@ def dequant_gather(qs, scales, lp, block=128):
     return out
 
 
+def e4m3_decode(codes):
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float32)
+    lib().orc_e4m3_decode_array(c.size, _ptr(c), _ptr(out))
+    return out
+
+
+def e4m3_encode(x):
+    v = _c(x, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    lib().orc_e4m3_encode_array(v.size, _ptr(v), _ptr(out))
+    return out
+
+
+def quantize_blocks_fp8(x_codes, lp, block=128):
+    x = _c(x_codes, np.uint16)
+    assert x.size % block == 0
+    q = np.empty(x.size, np.uint8)
+    sc = np.empty(x.size // block, np.float32)
+    lib().orc_quantize_blocks_fp8(x.size, _ptr(x), lp, block, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def dequant_gather_fp8(qs, scales, lp, block=128):
+    qs = [_c(q, np.uint8) for q in qs]
+    scales = [_c(s, np.float32) for s in scales]
+    length = qs[0].size
+    out = np.empty(length * len(qs), np.uint16)
+    lib().orc_dequant_gather_fp8(len(qs), C.cast(_ptr_array(qs), _vp),
+                                 C.cast(_ptr_array(scales), _vp), length, block, lp, _ptr(out))
+    return out
+
+
 LIB_PATH = _build.LIB
 __all__ = ["lib", "lp_to_float", "float_to_lp", "layout", "partition_to_flat",
            "fragments", "memory", "reduce", "reduce_lp_accum", "decide", "quantize_blocks",
-           "dequant_gather", "adam", "gather", "LIB_PATH",
+           "dequant_gather", "e4m3_decode", "e4m3_encode", "quantize_blocks_fp8",
+           "dequant_gather_fp8", "adam", "gather", "LIB_PATH",
            "Decision"]

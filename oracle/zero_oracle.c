@@ -524,3 +524,105 @@ void orc_dequant_gather(int32_t n, const int8_t *const *q, const float *const *s
             out[(int64_t)j * shard_len + k] = orc_float_to_lp(y, lp);
         }
 }
+
+/* ------------------------------------------------------------------------
+ * fp8 (OCP E4M3) variant of the quantized all-gather.  The format follows
+ * its definition: code s.eeee.mmm is (-1)^s * m/8 * 2^-6 when eeee = 0 and
+ * (-1)^s * (1 + m/8) * 2^(eeee - 7) otherwise; eeee.mmm = 1111.111 is NaN.
+ * ---------------------------------------------------------------------- */
+float orc_e4m3_decode(uint8_t c)
+{
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    float mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexpf((float)m, -9);
+    else
+        mag = ldexpf((float)(8 + m), e - 10);
+    return s ? -mag : mag;
+}
+
+/* Nearest code, ties to even: the magnitude is rounded on the grid of its
+ * binade (step 2^(E-3) for a normal binade 2^E, E >= -6; step 2^-9 below
+ * 2^-6), then the code whose value it is is looked up among the 127
+ * non-negative finite codes. */
+uint8_t orc_e4m3_encode(float v)
+{
+    uint8_t s = signbit(v) ? 0x80 : 0x00;
+    float a, step, r;
+    int E, c;
+    if (isnan(v))
+        return 0x7f;
+    a = fabsf(v);
+    if (a >= 464.0f)          /* past the midpoint between 448 and 480: saturate */
+        return s | 0x7e;
+    if (a == 0.0f)
+        return s;
+    frexpf(a, &E);            /* a = f * 2^E, f in [0.5, 1): binade 2^(E-1) */
+    E = E - 1;
+    if (E < -6)
+        E = -6;
+    step = ldexpf(1.0f, E - 3);
+    r = nearbyintf(a / step) * step;   /* a / step is exact (power of two) */
+    for (c = 0; c < 0x7f; ++c)
+        if (orc_e4m3_decode((uint8_t)c) == r)
+            return s | (uint8_t)c;
+    return 0xff;              /* unreachable: every rounded magnitude is a code */
+}
+
+void orc_e4m3_decode_array(int64_t n, const uint8_t *c, float *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e4m3_decode(c[i]);
+}
+
+void orc_e4m3_encode_array(int64_t n, const float *v, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e4m3_encode(v[i]);
+}
+
+void orc_quantize_blocks_fp8(int64_t len, const uint16_t *x, int32_t lp, int32_t block,
+                             uint8_t *q, float *scales)
+{
+    for (int64_t b0 = 0; b0 < len; b0 += block) {
+        float amax = 0.0f, inv;
+        int e, E;
+        for (int32_t k = 0; k < block; ++k) {
+            float a = fabsf(orc_lp_to_float(x[b0 + k], lp));
+            if (a > amax)
+                amax = a;
+        }
+        if (amax == 0.0f) {
+            scales[b0 / block] = 0.0f;
+            for (int32_t k = 0; k < block; ++k)
+                q[b0 + k] = 0;
+            continue;
+        }
+        if (isinf(amax)) {
+            e = 120;
+        } else {
+            frexpf(amax, &E);     /* floor(log2 amax) = E - 1 */
+            e = E - 1 - 7;
+            if (e < -126)
+                e = -126;
+            if (e > 120)
+                e = 120;
+        }
+        scales[b0 / block] = ldexpf(1.0f, e);
+        inv = ldexpf(1.0f, -e);
+        for (int32_t k = 0; k < block; ++k)
+            q[b0 + k] = orc_e4m3_encode(orc_lp_to_float(x[b0 + k], lp) * inv);
+    }
+}
+
+void orc_dequant_gather_fp8(int32_t n, const uint8_t *const *q, const float *const *scales,
+                            int64_t shard_len, int32_t block, int32_t lp, uint16_t *out)
+{
+    for (int32_t j = 0; j < n; ++j)
+        for (int64_t k = 0; k < shard_len; ++k) {
+            float y = orc_e4m3_decode(q[j][k]) * scales[j][k / block];
+            out[(int64_t)j * shard_len + k] = orc_float_to_lp(y, lp);
+        }
+}

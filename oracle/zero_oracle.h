@@ -148,6 +148,28 @@ void orc_quantize_blocks(int64_t len, const uint16_t *x, int32_t lp, int32_t blo
 void orc_dequant_gather(int32_t n, const int8_t *const *q, const float *const *scales,
                         int64_t shard_len, int32_t block, int32_t lp, uint16_t *out);
 
+/* ---- fp8 variant of the quantized all-gather ---------------------------
+ * Codes are OCP FP8 E4M3 ("e4m3fn": 1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits; no infinities; S.1111.111 is NaN; largest finite 448;
+ * subnormals m * 2^-9).  Encoding rounds to nearest, ties to even, and
+ * saturates finite values beyond 448 (and infinities) to +-448; NaN -> 0x7f.
+ * Blocks of `block` elements share a power-of-two scale 2^e with
+ *   e = floor(log2 amax) - 7, clamped to [-126, 120]  (amax finite > 0),
+ *   e = 120 when amax is infinite,
+ * so amax / 2^e lies in [128, 256) and no finite value saturates:
+ *   code = e4m3(x * 2^-e)   (one float multiply, then the encoding)
+ *   scale = 2^e (0 and every code 0 when amax == 0)
+ * and the receiver's value is lp(decode(code) * scale).                   */
+float orc_e4m3_decode(uint8_t c);
+uint8_t orc_e4m3_encode(float v);
+void orc_e4m3_decode_array(int64_t n, const uint8_t *c, float *out);
+void orc_e4m3_encode_array(int64_t n, const float *v, uint8_t *out);
+void orc_quantize_blocks_fp8(int64_t len, const uint16_t *x, int32_t lp, int32_t block,
+                             uint8_t *q, float *scales);
+/* out[j * shard_len + k] = lp(decode(q_j[k]) * scale_j[k / block]) */
+void orc_dequant_gather_fp8(int32_t n, const uint8_t *const *q, const float *const *scales,
+                            int64_t shard_len, int32_t block, int32_t lp, uint16_t *out);
+
 #ifdef __cplusplus
 }
 #endif

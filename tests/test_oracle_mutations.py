@@ -49,6 +49,11 @@ MUTANTS = {
     "quant_truncates": ("r = nearbyintf(orc_lp_to_float(x[b0 + k], lp) / scale);",
                         "r = truncf(orc_lp_to_float(x[b0 + k], lp) / scale);"),
     "dequant_wrong_block": ("scales[j][k / block]", "scales[j][k / block / 2]"),
+    "e4m3_bias_8": ("mag = ldexpf((float)(8 + m), e - 10);", "mag = ldexpf((float)(8 + m), e - 11);"),
+    "e4m3_truncates": ("r = nearbyintf(a / step) * step;", "r = floorf(a / step) * step;"),
+    "fp8_scale_exponent_off": ("e = E - 1 - 7;", "e = E - 1 - 8;"),
+    "fp8_dequant_one_scale": ("orc_e4m3_decode(q[j][k]) * scales[j][k / block]",
+                              "orc_e4m3_decode(q[j][k]) * scales[j][0]"),
     "lp_accum_not_rounded": ("run = orc_float_to_lp(orc_lp_to_float(run, lp) +\n                                      orc_lp_to_float(slices[j][i], lp), lp);",
                              "run = orc_float_to_lp(orc_lp_to_float(run, lp), lp);"),
 }

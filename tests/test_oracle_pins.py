@@ -632,3 +632,92 @@ def test_dequant_gather_layout(orc):
     for j in range(3):
         one = orc.dequant_gather([qs[j][0]], [qs[j][1]], 0, 128)
         assert np.array_equal(out[j * 256:(j + 1) * 256], one)
+
+
+# ------------------------------------------ fp8 (E4M3) variant of the gather
+
+def test_e4m3_decode_definition_and_library(orc):
+    # the format's definition at hand-picked codes ...
+    d = orc.e4m3_decode(np.array([0x00, 0x01, 0x07, 0x08, 0x38, 0xb8, 0x7e, 0x70, 0x77, 0x80],
+                                 np.uint8))
+    assert d.tolist() == [0.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 1.0, -1.0, 448.0, 128.0, 240.0,
+                          -0.0]
+    assert math.copysign(1.0, d[-1]) == -1.0
+    assert np.isnan(orc.e4m3_decode(np.array([0x7f, 0xff], np.uint8))).all()
+    # ... and every one of the 256 codes against torch's float8_e4m3fn
+    c = np.arange(256, dtype=np.uint8)
+    d = orc.e4m3_decode(c)
+    t = torch.from_numpy(c).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(np.isnan(d), np.isnan(t))
+    assert np.array_equal(d[~np.isnan(d)], t[~np.isnan(t)])
+
+
+def test_e4m3_encode_rounds_to_nearest_even_and_saturates(orc):
+    c = np.arange(0x7f, dtype=np.uint8)
+    vals = orc.e4m3_decode(c)
+    assert np.array_equal(orc.e4m3_encode(vals), c)                    # exact values
+    assert np.array_equal(orc.e4m3_encode(-vals), c | 0x80)
+    mids = ((vals[1:].astype(np.float64) + vals[:-1]) / 2).astype(np.float32)   # exact ties
+    even = np.where((c[:-1] & 1) == 0, c[:-1], c[1:])
+    assert np.array_equal(orc.e4m3_encode(mids), even)
+    rng = np.random.default_rng(31)
+    v = np.concatenate([rng.uniform(-463, 463, 50000),
+                        rng.uniform(-1, 1, 50000) * 2.0 ** rng.integers(-14, 9, 50000)]).astype(np.float32)
+    v = np.concatenate([v, mids, -mids])
+    t = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(orc.e4m3_encode(v), t)
+    # saturation (finite and infinite), NaN, signed zero
+    big = np.array([464.0, 1e30, np.inf, -464.0, -np.inf, np.nan, -0.0], np.float32)
+    assert orc.e4m3_encode(big).tolist() == [0x7e, 0x7e, 0x7e, 0xfe, 0xfe, 0x7f, 0x80]
+
+
+def test_quantize_fp8_scale_and_error(orc):
+    rng = np.random.default_rng(32)
+    for lp in (0, 1):
+        x = (rng.standard_normal(128 * 300) * 10.0 ** rng.integers(-3, 3, 128 * 300)).astype(np.float32)
+        codes = orc.float_to_lp(x, lp)
+        xf = orc.lp_to_float(codes, lp).reshape(-1, 128).astype(np.float64)
+        q, sc = orc.quantize_blocks_fp8(codes, lp, 128)
+        amax = np.abs(xf).max(axis=1)
+        # the scale is the power of two that puts amax in [128, 256)
+        e = np.log2(sc.astype(np.float64))
+        assert np.array_equal(e, np.round(e))
+        assert np.all((amax / sc >= 128) & (amax / sc < 256))
+        # codes are the nearest-even encoding of x / scale (computed in float64:
+        # a power-of-two scaling is exact)
+        ref = torch.from_numpy((xf / sc[:, None]).astype(np.float32).reshape(-1)).to(
+            torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(q, ref)
+        # dequantized error: half an E4M3 step (2^-4 relative, 2^-10 * scale for
+        # subnormal codes), plus the lp rounding
+        y = orc.lp_to_float(orc.dequant_gather_fp8([q], [sc], lp, 128), lp).reshape(-1, 128)
+        lp_ulp = 2.0 ** (-10 if lp == 0 else -7)
+        bound = np.maximum(np.abs(xf) * 2.0 ** -4, sc[:, None] * 2.0 ** -10) + np.abs(y) * lp_ulp
+        assert np.all(np.abs(y - xf) <= bound * (1 + 1e-6))
+
+
+def test_quantize_fp8_exact_round_trip_and_zero_block(orc):
+    # values that are E4M3 codes times 2^e come back bit for bit
+    rng = np.random.default_rng(33)
+    c = rng.integers(0, 0x70, 128).astype(np.uint8) | (rng.integers(0, 2, 128) << 7).astype(np.uint8)
+    c[5] = 0x75                                            # 208: the block maximum, in [128, 256)
+    for e in (-15, -3, 0, 4, 7):     # every value stays an fp16 number
+        x = orc.e4m3_decode(c) * np.float32(2.0 ** e)
+        codes = orc.float_to_lp(x, 0)
+        assert np.array_equal(orc.lp_to_float(codes, 0), x)  # representable in fp16
+        q, sc = orc.quantize_blocks_fp8(codes, 0, 128)
+        assert sc.tolist() == [2.0 ** e]
+        assert np.array_equal(q, c)
+        assert np.array_equal(orc.dequant_gather_fp8([q], [sc], 0, 128), codes)
+    q, sc = orc.quantize_blocks_fp8(np.zeros(128, np.uint16), 0, 128)
+    assert sc.tolist() == [0.0] and not q.any()
+
+
+def test_dequant_gather_fp8_layout(orc):
+    rng = np.random.default_rng(34)
+    shards = [orc.float_to_lp(rng.standard_normal(384).astype(np.float32), 1) for _ in range(3)]
+    qs = [orc.quantize_blocks_fp8(s, 1, 128) for s in shards]
+    out = orc.dequant_gather_fp8([q for q, _ in qs], [c for _, c in qs], 1, 128)
+    for j in range(3):
+        one = orc.dequant_gather_fp8([qs[j][0]], [qs[j][1]], 1, 128)
+        assert np.array_equal(out[j * 384:(j + 1) * 384], one)

@@ -54,6 +54,8 @@ def parse_args():
                     help="stage 3: issue every gather on one stream (no prefetch)")
     ap.add_argument("--quantized-gather", action="store_true",
                     help="stage-3 workloads: int8 block-quantized gathers")
+    ap.add_argument("--quant-format", choices=["int8", "fp8"], default=None,
+                    help="code format of the quantized gather (default: the workload's)")
     return ap.parse_args()
 
 
@@ -204,8 +206,9 @@ class Run:
             self.gather_out = torch.empty(biggest, dtype=lpd, device=dev)
             self.gather_out2 = torch.empty(biggest, dtype=lpd, device=dev)
             if self.quantized:
-                # every rank's int8 codes + block scales (ZeRO++-style gather);
-                # the other ranks quantize their shards once here
+                # every rank's 1-byte codes (int8 or E4M3) + block scales
+                # (ZeRO++-style gather); the other ranks quantize their shards once here
+                self.plan.set_gather_quantization(w.quant_format)
                 self.codes = [torch.empty(P, dtype=torch.int8, device=dev) for _ in range(w.n_ranks)]
                 self.scales = [torch.empty(P // 128, dtype=torch.float32, device=dev)
                                for _ in range(w.n_ranks)]
@@ -486,9 +489,11 @@ def main():
     ws, rank, local, dist = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
-    if args.quantized_gather:
+    if args.quantized_gather or args.quant_format:
         import dataclasses
         w = dataclasses.replace(w, gather_quantized=True)
+        if args.quant_format:
+            w = dataclasses.replace(w, quant_format=int(args.quant_format == "fp8"))
     # weak scaling: every GPU owns its own partition(s) of the simulated job
     part_ranks = [(r + rank) % w.n_ranks for r in w.ranks]
     t_setup = time.perf_counter()
@@ -661,7 +666,9 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": {"workload": w.name, "psi": int(sum(w.sizes)),
+                "config": {"workload": w.name + ("-fp8" if run.quantized and w.quant_format and
+                                                  not w.name.endswith("fp8") else ""),
+                           "psi": int(sum(w.sizes)),
                            "n_ranks": w.n_ranks, "stage": w.stage,
                            "lp": ["fp16", "bf16"][w.lp], "part_len": run.P,
                            "partitions_per_gpu": len(run.ranks),

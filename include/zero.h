@@ -296,7 +296,7 @@ zero_status zero_allgather_params(zero_plan *plan, const void *const *partitions
  * whose align is a multiple of ZERO_QUANT_BLOCK.
  *
  * zero_quantize_shard: shard (P lp elements, this rank's own shard buffer)
- * -> codes (P int8) and scales (P / ZERO_QUANT_BLOCK floats), per block of
+ * -> codes (P bytes) and scales (P / ZERO_QUANT_BLOCK floats), per block of
  * ZERO_QUANT_BLOCK elements:
  *   amax = max |x|,  scale = amax / 127 (float division),
  *   code = nearest integer (ties to even) to x / scale, clamped to
@@ -308,8 +308,25 @@ zero_status zero_allgather_params(zero_plan *plan, const void *const *partitions
  * with o the unit's shard offset; the product is a float multiply rounded to
  * the lp type (nearest even).  1 B + 4/128 B read per element instead of 2 B.
  * All pointers 16-byte aligned, device memory, asynchronous on `stream`.
+ *
+ * zero_plan_set_gather_quantization selects the code format of both calls
+ * (the pages name no format; host only, default ZERO_QUANT_INT8):
+ *  - ZERO_QUANT_INT8: the int8 codes above.
+ *  - ZERO_QUANT_FP8_E4M3: each code byte is an OCP FP8 E4M3 value (bias 7,
+ *    3 mantissa bits, largest 448, no infinities); per block the scale is the
+ *    power of two 2^e with e = floor(log2 amax) - 7, clamped to [-126, 120]
+ *    (120 when amax is infinite), so amax / 2^e is in [128, 256):
+ *      code = E4M3(x * 2^-e), nearest even, finite overflow and infinities
+ *             saturated to +-448 (never reached by finite blocks);
+ *      scale = 2^e, or 0 with every code 0 when amax == 0;
+ *    and the gather writes lp(decode(code) * scale).  Relative error up to
+ *    2^-4 instead of int8's amax/254, with a wider dynamic range per block.
+ *    Codes of non-finite elements are the hardware conversion's.
  */
 #define ZERO_QUANT_BLOCK 128
+#define ZERO_QUANT_INT8 0
+#define ZERO_QUANT_FP8_E4M3 1
+zero_status zero_plan_set_gather_quantization(zero_plan *plan, int32_t format);
 zero_status zero_quantize_shard(zero_plan *plan, const void *shard, int8_t *codes,
                                 float *scales, void *stream);
 zero_status zero_gather_layer_quantized(zero_plan *plan, int32_t unit,

@@ -213,5 +213,10 @@ def test_step_calls_validate_before_touching_the_device(lib):
         with pytest.raises(Z.ZeroError) as e:
             Z.zero_allgather_params(p3, [1 << 20, 1 << 20], 1 << 20, 0, stream=0)
         assert e.value.code == Z.ZERO_EINVAL                     # stage 3: layer gathers
+        Z.zero_plan_set_gather_quantization(p3, Z.ZERO_QUANT_FP8_E4M3)
+        Z.zero_plan_set_gather_quantization(p3, Z.ZERO_QUANT_INT8)
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_plan_set_gather_quantization(p3, 2)
+        assert e.value.code == Z.ZERO_EINVAL                     # unknown code format
     finally:
         Z.zero_plan_destroy(p3)

@@ -411,9 +411,18 @@ def test_global_stats_replace_the_local_sum(zlib):
 
 # ------------------------------------------------------ quantized gather
 
-def _quant_case(n, sizes, units, lp):
+def _quant_fns(fmt):
+    """The oracle's quantizer and dequantizing gather for a code format."""
+    if fmt == Z.ZERO_QUANT_FP8_E4M3:
+        return oracle.quantize_blocks_fp8, oracle.dequant_gather_fp8, np.uint8
+    return oracle.quantize_blocks, oracle.dequant_gather, np.int8
+
+
+def _quant_case(n, sizes, units, lp, fmt=0):
     dev = torch.device("cuda")
     plan = _plan(-1, n, lp, stage=3, align=128, sizes=sizes, units=units)
+    plan.set_gather_quantization(fmt)
+    o_quant, o_dequant, code_t = _quant_fns(fmt)
     P = plan.part_len
     shards = [synth.lp_shard(P, lp, 0.02, 5, j, dev) for j in range(n)]
     shards[0][:256].zero_()                       # whole zero blocks: scale 0
@@ -424,24 +433,25 @@ def _quant_case(n, sizes, units, lp):
     torch.cuda.synchronize()
     host_q = []
     for j in range(n):
-        oq, osc = oracle.quantize_blocks(synth.to_numpy_codes(shards[j]), lp, 128)
-        assert np.array_equal(codes[j].cpu().numpy(), oq), j
+        oq, osc = o_quant(synth.to_numpy_codes(shards[j]), lp, 128)
+        assert np.array_equal(codes[j].cpu().numpy().view(code_t), oq), j
         assert np.array_equal(scales[j].cpu().numpy().view(np.uint32), osc.view(np.uint32)), j
         host_q.append((oq, osc))
     for u in range(plan.n_units):
         sl, off = plan.shard_len(u), plan.unit_shard_offset(u)
         out = torch.full((sl * n,), 3, dtype=synth.LP_DTYPES[lp], device=dev)
         plan.gather_quantized(u, codes, scales, out)
-        exp = oracle.dequant_gather([q[off:off + sl] for q, _ in host_q],
-                                    [c[off // 128:(off + sl) // 128] for _, c in host_q], lp, 128)
+        exp = o_dequant([q[off:off + sl] for q, _ in host_q],
+                        [c[off // 128:(off + sl) // 128] for _, c in host_q], lp, 128)
         assert np.array_equal(synth.to_numpy_codes(out), exp), u
     plan.close()
 
 
 @pytest.mark.parametrize("n", [2, 3, 64, 65, Z.ZERO_MAX_RANKS])
 @pytest.mark.parametrize("lp", [0, 1])
-def test_quantize_and_dequant_gather(zlib, n, lp):
-    _quant_case(n, [5000, 128, 40_000, 3, 70_000], [0, 0, 1, 2, 2], lp)
+@pytest.mark.parametrize("fmt", [Z.ZERO_QUANT_INT8, Z.ZERO_QUANT_FP8_E4M3])
+def test_quantize_and_dequant_gather(zlib, n, lp, fmt):
+    _quant_case(n, [5000, 128, 40_000, 3, 70_000], [0, 0, 1, 2, 2], lp, fmt)
 
 
 def _boundary_blocks(lp, rng, n_blocks):
@@ -494,6 +504,51 @@ def test_quantize_rounding_boundaries(zlib, lp):
         oq, osc = oracle.quantize_blocks(host, lp, 128)
         assert np.array_equal(scales.cpu().numpy().view(np.uint32), osc.view(np.uint32))
         assert np.array_equal(codes.cpu().numpy(), oq)
+    plan.close()
+
+
+def _fp8_boundary_blocks(lp, rng, n_blocks):
+    """lp codes of blocks whose scaled values sit on E4M3 rounding ties (and
+    their lp neighbours), subnormal E4M3 codes, and block maxima spanning
+    the lp range (bf16 down to float-subnormal blocks: the clamped scale)."""
+    c = np.arange(0x7f, dtype=np.uint8)
+    vals = oracle.e4m3_decode(c).astype(np.float64)
+    mids = (vals[1:] + vals[:-1]) / 2                         # every tie of the format
+    out = np.empty((n_blocks, 128), np.uint16)
+    lo, hi = (-15, 7) if lp == 0 else (-132, 120)
+    for b in range(n_blocks):
+        e = int(rng.integers(lo, hi + 1))
+        amax = float(rng.uniform(128, 256))
+        m = rng.choice(mids[mids < amax], 127) * rng.choice([-1.0, 1.0], 127)
+        x = np.concatenate([[amax], m]) * 2.0 ** e
+        codes = oracle.float_to_lp(x.astype(np.float32), lp).astype(np.int32)
+        codes[1:] += rng.integers(-1, 2, 127)                  # ties and their neighbours
+        codes = np.clip(codes, 0, 0xffff).astype(np.uint16)
+        xf = oracle.lp_to_float(codes, lp)
+        bad = ~np.isfinite(xf) | (np.abs(xf) > np.abs(xf[0]))
+        codes[bad] = codes[0]
+        out[b] = codes
+    return out.reshape(-1)
+
+
+@pytest.mark.parametrize("lp", [0, 1])
+def test_quantize_fp8_rounding_boundaries(zlib, lp):
+    rng = np.random.default_rng(41 + lp)
+    n = 2
+    plan = _plan(-1, n, lp, stage=3, align=128, sizes=[n * 128 * 256], units=[0])
+    plan.set_gather_quantization(Z.ZERO_QUANT_FP8_E4M3)
+    P = plan.part_len
+    dev = torch.device("cuda")
+    for j in range(n):
+        host = _fp8_boundary_blocks(lp, rng, P // 128)
+        shard = torch.from_numpy(host.view(np.int16)).to(dev).view(synth.LP_DTYPES[lp])
+        codes = torch.empty(P, dtype=torch.int8, device=dev)
+        scales = torch.empty(P // 128, dtype=torch.float32, device=dev)
+        plan.quantize(shard, codes, scales)
+        torch.cuda.synchronize()
+        oq, osc = oracle.quantize_blocks_fp8(host, lp, 128)
+        assert np.array_equal(scales.cpu().numpy().view(np.uint32), osc.view(np.uint32))
+        assert np.array_equal(codes.cpu().numpy().view(np.uint8), oq)
     plan.close()
 
 

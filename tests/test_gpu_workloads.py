@@ -55,10 +55,13 @@ def _windows(sl, gen):
     return [(k0, min(L, sl - k0)) for k0 in sorted(starts)]
 
 
-def _check_gathers(plan, w, shards, gen, quantized):
+def _check_gathers(plan, w, shards, gen, quantized, fmt=0):
     """Gather every unit (forward order) and compare sampled windows with the
     oracle's gather (or quantize + dequantizing gather) of the same windows."""
     n, dev = w.n_ranks, shards[0].device
+    plan.set_gather_quantization(fmt)
+    o_quant = oracle.quantize_blocks_fp8 if fmt else oracle.quantize_blocks
+    o_dequant = oracle.dequant_gather_fp8 if fmt else oracle.dequant_gather
     biggest = max(plan.shard_len(u) for u in range(plan.n_units)) * n
     out = torch.empty(biggest, dtype=synth.LP_DTYPES[w.lp], device=dev)
     if quantized:
@@ -76,8 +79,8 @@ def _check_gathers(plan, w, shards, gen, quantized):
         for k0, L in _windows(sl, gen):
             win = [synth.to_numpy_codes(t[off + k0: off + k0 + L]) for t in shards]
             if quantized:
-                qs = [oracle.quantize_blocks(x, w.lp, 128) for x in win]
-                exp = oracle.dequant_gather([q for q, _ in qs], [c for _, c in qs], w.lp, 128)
+                qs = [o_quant(x, w.lp, 128) for x in win]
+                exp = o_dequant([q for q, _ in qs], [c for _, c in qs], w.lp, 128)
             else:
                 exp = oracle.gather(win)
             got = synth.to_numpy_codes(out[:sl * n].view(n, sl)[:, k0:k0 + L])
@@ -93,6 +96,7 @@ def test_7p5b_zero3_with_gathers(zlib):
     shards = _synthetic_shards(h.plan, w, h.dev)
     _check_gathers(h.plan, w, shards, np.random.default_rng(7), quantized=False)
     _check_gathers(h.plan, w, shards, np.random.default_rng(8), quantized=True)
+    _check_gathers(h.plan, w, shards, np.random.default_rng(9), quantized=True, fmt=1)
     h.close()
 
 

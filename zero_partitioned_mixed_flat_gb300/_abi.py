@@ -20,6 +20,7 @@ STATUS_NAMES = ["ZERO_OK", "ZERO_EINVAL", "ZERO_EALIGN", "ZERO_ENOMEM", "ZERO_EC
                 "ZERO_ETIMEOUT", "ZERO_ESTATE"]
 ZERO_FP16, ZERO_BF16 = 0, 1
 ZERO_MAX_RANKS = 1024
+ZERO_QUANT_INT8, ZERO_QUANT_FP8_E4M3 = 0, 1
 
 # every exported entry point of include/zero.h, with its ctypes signature
 _i32, _i64, _f32, _f64, _vp = C.c_int32, C.c_int64, C.c_float, C.c_double, C.c_void_p
@@ -32,6 +33,7 @@ SIGNATURES = {
     "zero_plan_set_state": (_i32, [_vp, _i64, _i32]),
     "zero_plan_set_spin_limit": (_i32, [_vp, _i64]),
     "zero_plan_set_reduce_precision": (_i32, [_vp, _i32]),
+    "zero_plan_set_gather_quantization": (_i32, [_vp, _i32]),
     "zero_reduce_partition": (_i32, [_vp, _i32, _vp, _vp, _f32, _i64, _vp]),
     "zero_reduce_units": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _f32, _vp]),
     "zero_partition_stats": (_i32, [_vp, _vp, _vp, _vp]),
@@ -163,6 +165,10 @@ def zero_plan_set_spin_limit(plan: int, polls: int):
 def zero_plan_set_reduce_precision(plan: int, accumulate_in_lp: int):
     _check(load().zero_plan_set_reduce_precision(plan, int(accumulate_in_lp)),
            "zero_plan_set_reduce_precision")
+
+
+def zero_plan_set_gather_quantization(plan: int, fmt: int):
+    _check(load().zero_plan_set_gather_quantization(plan, fmt), "zero_plan_set_gather_quantization")
 
 
 def zero_plan_destroy(plan: int):

@@ -70,6 +70,7 @@ struct zero_plan {
     uint64_t active[ZERO_MAX_RANKS / 64] = {0};
     int32_t growth_interval = 1000;
     int32_t reduce_lp_accum = 0;  // 1: partial sums rounded to the lp type
+    int32_t quant_format = ZERO_QUANT_INT8;  // codes of the quantized gather
     int64_t spin_limit = kDefaultSpinLimit;
     // the device step counter as far as the host can tell without reading it:
     // the last value read back or set, plus one per decision launched since
@@ -342,6 +343,13 @@ zero_status zero_plan_set_reduce_precision(zero_plan *p, int32_t accumulate_in_l
     if (!p || (accumulate_in_lp != 0 && accumulate_in_lp != 1))
         return fail(ZERO_EINVAL, "plan is NULL or accumulate_in_lp is not 0/1");
     p->reduce_lp_accum = accumulate_in_lp;
+    return ZERO_OK;
+}
+
+zero_status zero_plan_set_gather_quantization(zero_plan *p, int32_t format) {
+    if (!p || (format != ZERO_QUANT_INT8 && format != ZERO_QUANT_FP8_E4M3))
+        return fail(ZERO_EINVAL, "plan is NULL or format is not ZERO_QUANT_INT8 / ZERO_QUANT_FP8_E4M3");
+    p->quant_format = format;
     return ZERO_OK;
 }
 
@@ -703,7 +711,8 @@ zero_status zero_quantize_shard(zero_plan *p, const void *shard, int8_t *codes, 
         return fail(ZERO_EALIGN, "shard, codes or scales is not 16-byte aligned");
     zero_status st = ensure_device(p);
     if (st != ZERO_OK) return st;
-    cudaError_t e = zk::launch_quantize(shard, p->lp, p->part, codes, scales, static_cast<cudaStream_t>(stream));
+    cudaError_t e = zk::launch_quantize(shard, p->lp, p->quant_format == ZERO_QUANT_FP8_E4M3, p->part, codes, scales,
+                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "quantize kernel launch");
     return ZERO_OK;
 }
@@ -727,7 +736,8 @@ zero_status zero_gather_layer_quantized(zero_plan *p, int32_t unit, const int8_t
     if (st != ZERO_OK) return st;
     int64_t off = 0;
     for (int32_t u = 0; u < unit; ++u) off += p->shard_len(u);
-    cudaError_t e = zk::launch_dequant_gather(codes, scales, p->n_ranks, p->lp, off, shard, out,
+    cudaError_t e = zk::launch_dequant_gather(codes, scales, p->n_ranks, p->lp,
+                                              p->quant_format == ZERO_QUANT_FP8_E4M3, off, shard, out,
                                               static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "dequantizing gather kernel launch");
     return ZERO_OK;

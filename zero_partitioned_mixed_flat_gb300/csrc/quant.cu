@@ -90,6 +90,50 @@ __device__ __forceinline__ void quant_codes8(const float v[8], float scale, uint
     }
 }
 
+// ---- fp8 (OCP E4M3) variant: a power-of-two block scale 2^e with
+// e = floor(log2 amax) - 7 clamped to [-126, 120] (120 for an infinite amax),
+// so amax / 2^e lies in [128, 256): code = E4M3(x * 2^-e), nearest even,
+// finite overflow and infinities saturated to +-448.
+
+// two floats -> two E4M3 codes, a in the low byte (one conversion instruction)
+__device__ __forceinline__ uint32_t to_e4m3x2(float a, float b) {
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// two E4M3 codes (low byte first) -> two exact floats
+__device__ __forceinline__ float2 from_e4m3x2(uint32_t two) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)two));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+
+// the block scale exponent from amax's bits (amax >= 0, not NaN)
+__device__ __forceinline__ int fp8_scale_exponent(float amax) {
+    const int biased = (int)(__float_as_uint(amax) >> 23);
+    int e = biased == 0 ? -126 : biased - 127 - 7;
+    e = e < -126 ? -126 : e;
+    return e > 120 ? 120 : e;
+}
+
+__device__ __forceinline__ void quant_codes8_fp8(const float v[8], float amax, float &scale,
+                                                 uint32_t packed[2]) {
+    if (amax == 0.0f) {  // an all-zero block: scale 0 and codes 0 (also for -0)
+        scale = 0.0f;
+        packed[0] = packed[1] = 0u;
+        return;
+    }
+    const int e = fp8_scale_exponent(amax);
+    scale = __uint_as_float((uint32_t)(e + 127) << 23);
+    const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) h[k] = to_e4m3x2(__fmul_rn(v[2 * k], inv), __fmul_rn(v[2 * k + 1], inv));
+    packed[0] = h[0] | (h[1] << 16);
+    packed[1] = h[2] | (h[3] << 16);
+}
+
 template <bool BF16>
 __device__ __forceinline__ void from_lp4(uint2 raw, float v[4]) {
     const uint32_t w[2] = {raw.x, raw.y};
@@ -110,8 +154,9 @@ __device__ __forceinline__ void from_lp4(uint2 raw, float v[4]) {
 // load; kQuantUnroll pairs per pass): lane l holds elements 8(l mod 16) ..
 // 8(l mod 16) + 7 of block 2*pair + l/16.  scale = amax / 127 (float
 // division), code = nearest-even integer of x / scale (the correctly rounded
-// float quotient, see quant_codes8), clamped to +-127.
-template <bool BF16>
+// float quotient, see quant_codes8), clamped to +-127.  FP8: the E4M3 codes
+// and power-of-two scale of quant_codes8_fp8 instead.
+template <bool BF16, bool FP8>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_shard_blocks(const uint4 *__restrict__ x, uint2 *__restrict__ q, float *__restrict__ scales,
                       long long n_blocks) {
@@ -141,9 +186,14 @@ quantize_shard_blocks(const uint4 *__restrict__ x, uint2 *__restrict__ q, float 
 #pragma unroll
             for (int off = 8; off > 0; off >>= 1)  // within each half-warp
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-            const float scale = __fdiv_rn(amax, 127.0f);
+            float scale;
             uint32_t packed[2];
-            quant_codes8(v, scale, packed);
+            if constexpr (FP8) {
+                quant_codes8_fp8(v, amax, scale, packed);
+            } else {
+                scale = __fdiv_rn(amax, 127.0f);
+                quant_codes8(v, scale, packed);
+            }
             if (b < n_blocks) {
                 __stcs(q + b * 16 + (lane & 15), make_uint2(packed[0], packed[1]));
                 if ((lane & 15) == 0) scales[b] = scale;
@@ -164,7 +214,8 @@ struct DequantGatherParams {
 // rank j; along x a thread takes kQuantUnroll items of 8 codes (one 8-byte
 // load each, all issued before any use) and writes each item's 8 lp values
 // with one 16-byte store, so a warp's loads and stores are contiguous runs.
-template <int MAXN, bool BF16>
+// FP8: the codes are E4M3, widened exactly by the conversion instruction.
+template <int MAXN, bool BF16, bool FP8>
 __global__ void __launch_bounds__(kQuantThreads)
 gather_dequant(const __grid_constant__ DequantGatherParams<MAXN> p) {
     pdl_enter();
@@ -189,15 +240,24 @@ gather_dequant(const __grid_constant__ DequantGatherParams<MAXN> p) {
         for (int u = 0; u < kQuantUnroll; ++u) {
             const long long k = k0 + u * stride;
             if (k >= p.vec_per_shard) break;
-            const uint32_t w[2] = {c[u].x ^ 0x80808080u, c[u].y ^ 0x80808080u};
             uint32_t o[4];
+            if constexpr (FP8) {
+                const uint32_t w[2] = {c[u].x, c[u].y};
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                float y[4];
+                for (int t = 0; t < 4; ++t) {
+                    const float2 f = from_e4m3x2(w[t >> 1] >> (16 * (t & 1)));
+                    o[t] = to_lp2_packed<BF16>(__fmul_rn(f.x, sc[u]), __fmul_rn(f.y, sc[u]));
+                }
+            } else {
+                const uint32_t w[2] = {c[u].x ^ 0x80808080u, c[u].y ^ 0x80808080u};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) y[q] = __fmul_rn(code_to_float(w[t], q), sc[u]);
-                o[2 * t] = to_lp2_packed<BF16>(y[0], y[1]);
-                o[2 * t + 1] = to_lp2_packed<BF16>(y[2], y[3]);
+                for (int t = 0; t < 2; ++t) {
+                    float y[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) y[q] = __fmul_rn(code_to_float(w[t], q), sc[u]);
+                    o[2 * t] = to_lp2_packed<BF16>(y[0], y[1]);
+                    o[2 * t + 1] = to_lp2_packed<BF16>(y[2], y[3]);
+                }
             }
             __stcs(out + k, make_uint4(o[0], o[1], o[2], o[3]));
         }
@@ -211,7 +271,7 @@ int blocks_per_sm(K kernel) {
     return b < 1 ? 1 : b;
 }
 
-template <int MAXN, bool BF16>
+template <int MAXN, bool BF16, bool FP8>
 cudaError_t dequant_gather_impl(const int8_t *const *codes, const float *const *scales, int n,
                                 int64_t offset, int64_t shard_len, void *out, cudaStream_t stream) {
     DequantGatherParams<MAXN> p;
@@ -226,45 +286,55 @@ cudaError_t dequant_gather_impl(const int8_t *const *codes, const float *const *
     p.out = static_cast<uint4 *>(out);
     p.vec_per_shard = shard_len / 8;
     if (p.vec_per_shard == 0 || n == 0) return cudaSuccess;
-    static const int occ = blocks_per_sm(gather_dequant<MAXN, BF16>);
+    static const int occ = blocks_per_sm(gather_dequant<MAXN, BF16, FP8>);
     // about two waves of CTAs over all ranks
     const long long per_rank_need = (p.vec_per_shard + kQuantThreads * kQuantUnroll - 1) /
                                     (kQuantThreads * kQuantUnroll);
     long long gx = (2LL * sm_count() * occ + n - 1) / n;
     if (gx > per_rank_need) gx = per_rank_need;
     if (gx < 1) gx = 1;
-    return launch_pdl(gather_dequant<MAXN, BF16>, dim3((unsigned)gx, (unsigned)n), dim3(kQuantThreads), 0, stream,
-                      p);
+    return launch_pdl(gather_dequant<MAXN, BF16, FP8>, dim3((unsigned)gx, (unsigned)n), dim3(kQuantThreads), 0,
+                      stream, p);
 }
 
-template <bool BF16>
+template <bool BF16, bool FP8>
 cudaError_t quantize_impl(const void *shard, int64_t len, int8_t *codes, float *scales, cudaStream_t stream) {
     const long long blocks = len / 128;
     if (blocks == 0) return cudaSuccess;
-    static const int occ = blocks_per_sm(quantize_shard_blocks<BF16>);
+    static const int occ = blocks_per_sm(quantize_shard_blocks<BF16, FP8>);
     long long grid = (long long)sm_count() * occ;
     const long long per_cta = (kQuantThreads / 32) * kQuantUnroll * 2;
     const long long need = (blocks + per_cta - 1) / per_cta;
     if (grid > need) grid = need;
-    return launch_pdl(quantize_shard_blocks<BF16>, dim3((unsigned)grid), dim3(kQuantThreads), 0, stream,
+    return launch_pdl(quantize_shard_blocks<BF16, FP8>, dim3((unsigned)grid), dim3(kQuantThreads), 0, stream,
                       static_cast<const uint4 *>(shard), reinterpret_cast<uint2 *>(codes), scales, blocks);
 }
 
 }  // namespace
 
-cudaError_t launch_quantize(const void *shard, int lp, int64_t len, int8_t *codes, float *scales,
+cudaError_t launch_quantize(const void *shard, int lp, int fp8, int64_t len, int8_t *codes, float *scales,
                             cudaStream_t stream) {
-    return lp ? quantize_impl<true>(shard, len, codes, scales, stream)
-              : quantize_impl<false>(shard, len, codes, scales, stream);
+    if (fp8)
+        return lp ? quantize_impl<true, true>(shard, len, codes, scales, stream)
+                  : quantize_impl<false, true>(shard, len, codes, scales, stream);
+    return lp ? quantize_impl<true, false>(shard, len, codes, scales, stream)
+              : quantize_impl<false, false>(shard, len, codes, scales, stream);
+}
+
+template <int MAXN>
+cudaError_t dequant_dispatch(const int8_t *const *codes, const float *const *scales, int n, int lp, int fp8,
+                             int64_t offset, int64_t shard_len, void *out, cudaStream_t stream) {
+    if (fp8)
+        return lp ? dequant_gather_impl<MAXN, true, true>(codes, scales, n, offset, shard_len, out, stream)
+                  : dequant_gather_impl<MAXN, false, true>(codes, scales, n, offset, shard_len, out, stream);
+    return lp ? dequant_gather_impl<MAXN, true, false>(codes, scales, n, offset, shard_len, out, stream)
+              : dequant_gather_impl<MAXN, false, false>(codes, scales, n, offset, shard_len, out, stream);
 }
 
 cudaError_t launch_dequant_gather(const int8_t *const *codes, const float *const *scales, int n, int lp,
-                                  int64_t offset, int64_t shard_len, void *out, cudaStream_t stream) {
-    if (n <= 64)
-        return lp ? dequant_gather_impl<64, true>(codes, scales, n, offset, shard_len, out, stream)
-                  : dequant_gather_impl<64, false>(codes, scales, n, offset, shard_len, out, stream);
-    return lp ? dequant_gather_impl<1024, true>(codes, scales, n, offset, shard_len, out, stream)
-              : dequant_gather_impl<1024, false>(codes, scales, n, offset, shard_len, out, stream);
+                                  int fp8, int64_t offset, int64_t shard_len, void *out, cudaStream_t stream) {
+    if (n <= 64) return dequant_dispatch<64>(codes, scales, n, lp, fp8, offset, shard_len, out, stream);
+    return dequant_dispatch<1024>(codes, scales, n, lp, fp8, offset, shard_len, out, stream);
 }
 
 }  // namespace zk

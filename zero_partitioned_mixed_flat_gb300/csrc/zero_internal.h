@@ -79,13 +79,14 @@ cudaError_t launch_gather(const void *const *shards, int n, int64_t src_offset_b
                           int64_t shard_bytes, void *out, int64_t dst_stride_bytes,
                           int64_t spin_limit, int *error, cudaStream_t stream);
 
-// quantized all-gather (block = 128 elements): shard -> int8 codes + scales;
-// codes/scales of N ranks at a unit's offset -> lp layer buffer
-cudaError_t launch_quantize(const void *shard, int lp, int64_t len, int8_t *codes,
+// quantized all-gather (block = 128 elements): shard -> 1-byte codes (int8,
+// or E4M3 when fp8) + float scales; codes/scales of N ranks at a unit's
+// offset -> lp layer buffer
+cudaError_t launch_quantize(const void *shard, int lp, int fp8, int64_t len, int8_t *codes,
                             float *scales, cudaStream_t stream);
 
 cudaError_t launch_dequant_gather(const int8_t *const *codes, const float *const *scales,
-                                  int n, int lp, int64_t offset, int64_t shard_len,
+                                  int n, int lp, int fp8, int64_t offset, int64_t shard_len,
                                   void *out, cudaStream_t stream);
 
 }  // namespace zk

@@ -101,6 +101,9 @@ class ZeroPlan:
     def set_state(self, step, good_steps=0):
         A.zero_plan_set_state(self.handle, step, good_steps)
 
+    def set_gather_quantization(self, fmt):
+        A.zero_plan_set_gather_quantization(self.handle, fmt)
+
     def set_reduce_precision(self, accumulate_in_lp):
         A.zero_plan_set_reduce_precision(self.handle, accumulate_in_lp)
 

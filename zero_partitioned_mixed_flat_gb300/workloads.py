@@ -74,7 +74,8 @@ class Workload:
     adamw: bool = True
     clip: float = 1.0
     reduce_lp_accum: bool = False  # partial sums rounded to the lp type
-    gather_quantized: bool = False  # stage 3: int8 block-quantized gathers
+    gather_quantized: bool = False  # stage 3: block-quantized gathers
+    quant_format: int = 0           # their codes: 0 int8, 1 fp8 E4M3
     notes: str = field(default="")
 
 
@@ -107,6 +108,12 @@ def _make():
         ranks=[0], steps=4, loss_scale=65536.0, growth_interval=1000,
         grads_times_scale=True, gather=True, gather_quantized=True, bucket_elems=500_000_000,
         notes="7.5b-zero3 with ZeRO++-style int8 block-quantized gathers")
+    w["7.5b-zero3-fp8"] = Workload(
+        name="7.5b-zero3-fp8", sizes=s, unit_of_tensor=u, n_ranks=64, stage=3, lp=0,
+        ranks=[0], steps=4, loss_scale=65536.0, growth_interval=1000,
+        grads_times_scale=True, gather=True, gather_quantized=True, quant_format=1,
+        bucket_elems=500_000_000,
+        notes="7.5b-zero3 with fp8 (E4M3, power-of-two block scale) quantized gathers")
     w["13b-zero2"] = Workload(
         name="13b-zero2", sizes=[13_000_000_000], n_ranks=16, stage=2, lp=1,
         ranks=[0], steps=4, loss_scale=1.0, growth_interval=0,

@@ -2,9 +2,10 @@
 //
 // ZeRO++ ("ZeRO-1/2/3 分别优化了什么" note, ZeRO++: the all-gathered
 // parameters are quantized to cut the traffic): each rank turns its lp shard
-// into int8 codes with one float scale per 128-element block (symmetric,
-// block max -> 127, nearest-even), and the gather expands code * scale back to
-// lp while it concatenates the ranks' shards.  Per layer element the gather
+// into 1-byte codes with one float scale per 128-element block -- int8
+// (symmetric, block max -> 127, nearest-even) or OCP FP8 E4M3 with a
+// power-of-two scale -- and the gather expands code * scale back to lp while
+// it concatenates the ranks' shards.  Per layer element the gather
 // moves 1 B + 4/128 B in and 2 B out, against 2 B in and 2 B out for the lp
 // gather.  Both kernels are plain streaming kernels; each thread keeps several
 // independent loads in flight before it computes, and every warp load and

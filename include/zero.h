@@ -33,6 +33,12 @@
  *    CUDA launch failure part-way may have enqueued the earlier ones).
  *  - A plan holds host-side step state: calls on one plan must not run
  *    concurrently from several host threads; different plans are independent.
+ *  - CUDA graphs: once a plan has run one step eagerly (its first device call
+ *    allocates its scratch), the asynchronous calls of a step (reduces,
+ *    zero_adam_step / _range, gathers, quantize) can be captured on a stream
+ *    and the graph replayed; each replay is one step with the arguments of
+ *    capture time (the step counter, loss scale and skip logic stay on the
+ *    device).  The synchronising calls are not capturable.
  *  - Low-precision ("lp") values are IEEE binary16 (ZERO_FP16) or bfloat16
  *    (ZERO_BF16), chosen per plan.
  */

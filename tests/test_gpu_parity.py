@@ -273,6 +273,48 @@ def test_bias_corrections_after_unread_skips(zlib, skips):
     plan.close()
 
 
+@pytest.mark.parametrize("steps", [3, 10])
+def test_captured_step_replays_like_eager_steps(zlib, steps):
+    # one step (reduce of every partition, decision, Adam) captured into a CUDA
+    # graph after an eager first step, replayed `steps` times, against the same
+    # number of eager steps; 10 replays run past the bias-correction table
+    # baked into the captured launch (the device then computes the powers)
+    w = _tiny(n_ranks=3, ranks=[0, 1, 2], sizes=[100_000, 7, 33_333], clip=0.05)
+    a, b = Harness(w), Harness(w)
+    for h in (a, b):
+        h.step_no = 1
+        for r in h.ranks:
+            h.make_slices(r)
+        h.gpu_step()
+    for _ in range(steps):
+        a.gpu_step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            for r in b.ranks:
+                s = b.st[r]
+                b.plan.reduce(r, s.slices, s.g, b.S, b.bucket, stream=int(cap.cuda_stream))
+            for r in b.ranks:
+                s = b.st[r]
+                b.plan.adam(r, s.g, s.master, s.m, s.v, b.param, w.lr, w.beta1, w.beta2, w.eps,
+                            w.wd, int(w.adamw), b.S, w.clip, stream=int(cap.cuda_stream))
+    torch.cuda.current_stream().wait_stream(cap)
+    for _ in range(steps):
+        g.replay()
+    torch.cuda.synchronize()
+    ra, rb = a.plan.result(), b.plan.result()
+    assert ra == rb and rb["step"] == 1 + steps
+    for r in a.ranks:
+        for t in ("master", "m", "v"):
+            assert torch.equal(getattr(a.st[r], t), getattr(b.st[r], t)), (r, t)
+    assert torch.equal(a.param, b.param)
+    a.close()
+    b.close()
+
+
 def test_resume_is_bit_identical(zlib):
     w = WORKLOADS["tiny-zero1"]
     a = Harness(w)

@@ -201,6 +201,34 @@ def test_adam_in_sub_groups(zlib, sub_group):
     b.close()
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_random_layouts_full_step(zlib, seed):
+    # random plans: N, stage, tensor list, stage-3 units, align, lp, buckets,
+    # partitions updated; two whole steps against the oracle, every element
+    rng = np.random.default_rng(1000 + seed)
+    n = int(rng.choice([1, 2, 3, 5, 8, 17, 64, 70]))
+    stage = int(rng.integers(1, 4))
+    k = int(rng.integers(1, 6))
+    sizes = [int(x) for x in rng.integers(1, 50_000, k)]
+    units = None
+    if stage == 3:
+        units, u = [], 0
+        for i in range(k):
+            if i > 0 and rng.random() < 0.5:
+                u += 1
+            units.append(u)
+    lp = int(rng.integers(0, 2))
+    ranks = sorted(set(int(r) for r in rng.integers(0, n, min(n, 3))))
+    w = _tiny(n_ranks=n, ranks=ranks, sizes=sizes, unit_of_tensor=units, stage=stage, lp=lp,
+              align=int(rng.choice([8, 128])), bucket_elems=int(rng.choice([0, 4096, 12_288])),
+              loss_scale=1024.0 if lp == 0 else 1.0, grads_times_scale=lp == 0,
+              clip=float(rng.choice([0.0, 0.05, 1.0])), adamw=bool(rng.integers(0, 2)))
+    h = Harness(w)
+    for _ in range(2):
+        h.step()
+    h.close()
+
+
 def test_overflow_skips_and_halves_scale(zlib):
     w = _tiny(growth_interval=1000, inject_inf_step=2, loss_scale=65536.0, steps=3)
     h = Harness(w)

@@ -10,12 +10,16 @@
 //                          all-gather destination (§10.6.2 Steps 3-4); a
 //                          warp-specialised TMA bulk-copy pipeline.
 // K4 gather_layer_tma      stage-3 per-layer all-gather of N shards
-//                          (§10.6.4 step 1), TMA bulk copies through shared
-//                          memory with bounded mbarrier waits.
+//                          (§10.6.4 step 1) and the bucketed stage-1/2
+//                          parameter all-gather (§10.6.2 Step 4): TMA bulk
+//                          copies through shared memory with bounded
+//                          mbarrier waits.
 //
 // Everything here is bandwidth-bound streaming: no tensor cores.  All float
 // arithmetic of the step uses explicit round-to-nearest intrinsics so that no
-// multiply-add is fused and the op order is the one the ABI documents.
+// multiply-add is fused and the op order is the one the ABI documents.  Every
+// kernel starts with pdl_enter() (launch.h): it waits for the previous grid of
+// the stream before touching global memory.
 #include "launch.h"
 #include "zero_internal.h"
 

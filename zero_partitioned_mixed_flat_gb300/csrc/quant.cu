@@ -59,25 +59,34 @@ __device__ __forceinline__ uint32_t code_by_division(float x, float scale) {
 // and subtracting the constant back gives k exactly.
 constexpr float kRoundMagic = 12582912.0f;
 
+// hardware reciprocal approximation (within one ulp of 1/x for normal x)
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // 8 codes of one thread's elements, packed 4 per word (byte k = element k).
-// Fast path: q = x * RN(1/scale) lies within 2^-23 |x/scale| of the exact
-// quotient and RN(x / scale) within 2^-24 |x/scale|; with |x/scale| <= 127
-// both lie within 2.3e-5 of it, so when every q is farther than 2^-13 from a
-// half-integer, rounding q gives the codes of the correctly rounded quotients
-// (and |q| < 127.5 needs no clamp).  Otherwise (rare: ties, a NaN element), and
-// for a zero, subnormal-small, huge or non-finite scale, every element is
-// divided.
+// Fast path, with p = x * rcp the exact product (rcp within one ulp of
+// 1/scale, so p lies within 2^-23 |x/scale| <= 1.6e-5 of the exact quotient):
+// one fused multiply-add rounds p to its nearest-even integer k (through the
+// 1.5 * 2^23 addition) and another gives d = p - k rounded once.  When every
+// |d| < 1/2 - 2^-13, the correctly rounded quotient RN(x / scale) (within
+// 7.6e-6 of the exact one) is farther than 9e-5 from a half-integer and rounds
+// to the same k (and |k| <= 127 needs no clamp).  Otherwise (rare: ties, a
+// NaN element), and for a zero, subnormal-small, huge or non-finite scale,
+// every element is divided.
 __device__ __forceinline__ void quant_codes8(const float v[8], float scale, uint32_t packed[2]) {
     bool divide = !(scale >= 0x1p-100f && scale <= 0x1p+100f);
     if (!divide) {
-        const float rcp = __frcp_rn(scale);
+        const float rcp = rcp_approx(scale);
         uint32_t t[8];
         bool near = false;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const float q = __fmul_rn(v[k], rcp);
-            const float r = __fadd_rn(q, kRoundMagic);
-            near |= !(fabsf(__fsub_rn(q, __fsub_rn(r, kRoundMagic))) < 0.5f - 0x1p-13f);
+            const float r = __fmaf_rn(v[k], rcp, kRoundMagic);
+            const float d = __fmaf_rn(v[k], rcp, -__fsub_rn(r, kRoundMagic));
+            near |= !(fabsf(d) < 0.5f - 0x1p-13f);
             t[k] = __float_as_uint(r);
         }
         packed[0] = __byte_perm(__byte_perm(t[0], t[1], 0x0040u), __byte_perm(t[2], t[3], 0x0040u), 0x5410u);

@@ -1,0 +1,43 @@
+"""The benchmark's own arm prints one JSON line with every key of its
+contract, on a small workload (GB300)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("extra", [[], ["--graph"]])
+def test_bench_json_line(zlib, extra):
+    r = subprocess.run([sys.executable, "bench.py", "--workload", "tiny-zero1", "--steps", "4",
+                        "--warmup", "3", "--cpu-seconds", "0.5", "--e2e-steps", "2"] + extra,
+                       cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches"):
+        assert k in d, k
+    assert d["n_gpus"] == 1 and d["steps"] == 4 and d["warmup"] == 3 and d["value"] > 0
+    assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["data"] == "synthetic"
+    assert d["config"]["workload"] == "tiny-zero1" and "flushed" in d["config"]["l2"]
+    rf = d["roofline"]
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in rf, k
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["achieved"] > 0
+    assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1 and cb["sample"]
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    # 4 ranks' reduce + one decision + 4 Adam per step
+    assert d["gpu_launches"] == 4 * 9
+    assert set(d["kernels"]) == {"reduce", "decide", "adam"}
+    if extra:
+        assert d["graph"]["graph_ms_per_step"] == d["ms_per_step"]

@@ -54,6 +54,8 @@ def parse_args():
                     help="stage 3: issue every gather on one stream (no prefetch)")
     ap.add_argument("--quantized-gather", action="store_true",
                     help="stage-3 workloads: int8 block-quantized gathers")
+    ap.add_argument("--reduce-in-lp", action="store_true",
+                    help="sum the gradient slices in the lp type (reduce_dtype=float16)")
     ap.add_argument("--quant-format", choices=["int8", "fp8"], default=None,
                     help="code format of the quantized gather (default: the workload's)")
     return ap.parse_args()
@@ -175,6 +177,8 @@ class Run:
         self.ranks = part_ranks
         self.plan = Z.ZeroPlan(-1, w.n_ranks, w.sizes, w.align, w.stage, w.unit_of_tensor, w.lp,
                                growth_interval=w.growth_interval)
+        if w.reduce_lp_accum:
+            self.plan.set_reduce_precision(1)
         P = self.P = self.plan.part_len
         self.S = w.loss_scale
         lpd = synth.LP_DTYPES[w.lp]
@@ -489,6 +493,9 @@ def main():
     ws, rank, local, dist = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
+    if args.reduce_in_lp:
+        import dataclasses
+        w = dataclasses.replace(w, reduce_lp_accum=True)
     if args.quantized_gather or args.quant_format:
         import dataclasses
         w = dataclasses.replace(w, gather_quantized=True)
@@ -671,6 +678,7 @@ def main():
                            "psi": int(sum(w.sizes)),
                            "n_ranks": w.n_ranks, "stage": w.stage,
                            "lp": ["fp16", "bf16"][w.lp], "part_len": run.P,
+                           "reduce_dtype": ["fp32", "lp"][int(w.reduce_lp_accum)],
                            "partitions_per_gpu": len(run.ranks),
                            "bucket_elems": w.bucket_elems,
                            "gather_prefetch_streams": 2 if side is not None else (

@@ -139,8 +139,9 @@ zero_status zero_plan_set_reduce_precision(zero_plan *plan, int32_t accumulate_i
 zero_status zero_plan_set_state(zero_plan *plan, int64_t step,
                                 int32_t good_steps);
 
-/* Bound on the polls of each device-side wait in zero_gather_layer; 0 makes
- * every wait give up at once (used to test the timeout path).  A wait that
+/* Bound on the polls of each device-side wait in zero_gather_layer and
+ * zero_allgather_params; 0 makes every wait give up at once (used to test the
+ * timeout path).  A wait that
  * gives up sets the plan's error word; the next synchronising call
  * (zero_step_result or zero_plan_check) returns ZERO_ETIMEOUT.  Host only. */
 zero_status zero_plan_set_spin_limit(zero_plan *plan, int64_t polls);
@@ -217,7 +218,9 @@ zero_status zero_step_set_global_stats(zero_plan *plan, double global_sumsq,
  * op rounded to nearest on its own (no fused multiply-add):
  *   g' = grad[i] * coef;  adamw == 0: g' = g' + wd * master[i]   (L2 Adam)
  *   m  = b1*m + (1-b1)*g';   v = b2*v + (1-b2)*(g'*g')
- *   upd = (lr * (m / (1-b1^t))) / (sqrt(v / (1-b2^t)) + eps)
+ *   upd = (lr * (m / bc1)) / (sqrt(v / bc2) + eps),
+ *         bc1 = float(1 - b1^t), bc2 = float(1 - b2^t)  (power and difference in
+ *         double, then rounded once)
  *   adamw != 0: master = master * float(1 - lr*wd)   (decoupled decay)
  *   master = master - upd;  param = round-to-nearest-even lp(master)
  * grad, master, m, v: P floats (device).  param_out: lp, device; stages 0-2:

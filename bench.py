@@ -54,6 +54,8 @@ def parse_args():
                     help="stage 3: issue every gather on one stream (no prefetch)")
     ap.add_argument("--quantized-gather", action="store_true",
                     help="stage-3 workloads: int8 block-quantized gathers")
+    ap.add_argument("--n-ranks", type=int, default=None,
+                    help="override the workload's N (simulated data-parallel ranks), rank 0 only")
     ap.add_argument("--reduce-in-lp", action="store_true",
                     help="sum the gradient slices in the lp type (reduce_dtype=float16)")
     ap.add_argument("--quant-format", choices=["int8", "fp8"], default=None,
@@ -493,6 +495,10 @@ def main():
     ws, rank, local, dist = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
+    if args.n_ranks:
+        import dataclasses
+        w = dataclasses.replace(w, n_ranks=args.n_ranks, ranks=[0],
+                                name="%s-n%d" % (w.name, args.n_ranks))
     if args.reduce_in_lp:
         import dataclasses
         w = dataclasses.replace(w, reduce_lp_accum=True)

@@ -33,17 +33,25 @@ namespace {
 
 constexpr int kReduceThreads = 128;
 constexpr int kVec = 8;  // lp elements per 16-byte vector
-constexpr int kTileIters = int(kTile / (kReduceThreads * kVec));
 constexpr int kBatch = 16;  // loads (slices x vectors) a thread issues before it adds
 // vectors of 8 elements a thread takes from each slice per round: 4 makes a
 // warp's load from one slice one contiguous 2 KB run and covers a 4096-element
 // tile in one round (faster than 1 or 2 at N = 8, 16 and 64 on GB300)
 constexpr int kReduceVpt = 4;
+// Few slices give a thread few loads to keep in flight (N x 4), so up to
+// kSmallN slices a tile goes to 64 threads taking 8 vectors each instead
+// (13B-sized partitions on GB300: N = 2 from 73 % to 86 % of the copy peak,
+// N = 3 from 85 % to 97 %; no gain from N = 4 on).
+constexpr int kSmallN = 3;
+constexpr int kSmallThreads = 64;
+constexpr int kSmallVpt = 8;
 constexpr int kMaxSegments = kMaxReduceSegments;  // tile runs per reduce launch
 constexpr int kGatherStages = 3;
 constexpr unsigned kGatherChunk = 32768;  // bytes per bulk copy
 constexpr long long kDrainPolls = 1ll << 21;
 static_assert(kTile % (kReduceVpt * kReduceThreads * kVec) == 0, "tile must be whole rounds");
+static_assert(kTile % (kSmallVpt * kSmallThreads * kVec) == 0, "tile must be whole rounds");
+static_assert(kBatch % kSmallVpt == 0, "a batch holds whole slices");
 static_assert(kBatch % kReduceVpt == 0, "a batch holds whole slices");
 
 // ---------------------------------------------------------------- memory ops
@@ -139,13 +147,14 @@ __device__ __forceinline__ void round_lp_pair(float &a, float &b) {
 // of float output per vector goes through shared memory so that it leaves as
 // two contiguous 512-byte stores instead of 32 lanes writing 32-byte strided
 // halves.
-template <int MAXN, bool BF16, bool ACC_LP, int VPT>
-__global__ void __launch_bounds__(kReduceThreads)
+template <int MAXN, bool BF16, bool ACC_LP, int VPT, int THREADS>
+__global__ void __launch_bounds__(THREADS, THREADS == 64 ? 6 : 4)
 reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
     pdl_enter();
     constexpr int BATCH = kBatch / VPT;
-    __shared__ double warp_sq[kReduceThreads / 32];
-    __shared__ float4 stage[kReduceThreads / 32][64];
+    constexpr int kTileIters = int(kTile / (THREADS * kVec));
+    __shared__ double warp_sq[THREADS / 32];
+    __shared__ float4 stage[THREADS / 32][64];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     bool bad = false;
     // this CTA's tile: tile t of segment seg
@@ -163,13 +172,13 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
         const long long v0 = e0 / kVec;
 #pragma unroll 1
         for (int it = 0; it < kTileIters / VPT; ++it) {
-            const long long vb = v0 + (long long)it * VPT * kReduceThreads + warp * 32;
+            const long long vb = v0 + (long long)it * VPT * THREADS + warp * 32;
             if (vb >= v_end) break;  // the whole warp is past the end
             long long vi[VPT];
             bool ok[VPT];
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
-                vi[v] = vb + (long long)v * kReduceThreads + lane;
+                vi[v] = vb + (long long)v * THREADS + lane;
                 ok[v] = vi[v] < v_end;
             }
             float s[VPT][8];
@@ -219,7 +228,7 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
                 const float4 lo = stage[warp][lane];
                 const float4 hi = stage[warp][32 + lane];
                 __syncwarp();
-                const long long wv = vb + (long long)v * kReduceThreads;  // the warp's first vector
+                const long long wv = vb + (long long)v * THREADS;  // the warp's first vector
                 if (wv + (lane >> 1) < v_end) st_stream_f4(p.g + 2 * wv + lane, lo);
                 if (wv + 16 + (lane >> 1) < v_end) st_stream_f4(p.g + 2 * wv + 32 + lane, hi);
             }
@@ -234,7 +243,7 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
         if (threadIdx.x == 0) {
             double tsum = 0.0;
 #pragma unroll
-            for (int w = 0; w < kReduceThreads / 32; ++w) tsum = __dadd_rn(tsum, warp_sq[w]);
+            for (int w = 0; w < THREADS / 32; ++w) tsum = __dadd_rn(tsum, warp_sq[w]);
             p.partials[p.seg_pbase[seg] + t] = tsum;
         }
     }
@@ -776,7 +785,7 @@ int occupancy(K kernel, int threads, size_t smem) {
     return blocks < 1 ? 1 : blocks;
 }
 
-template <int MAXN, bool BF16, bool ACC_LP, int VPT>
+template <int MAXN, bool BF16, bool ACC_LP, int VPT, int THREADS>
 cudaError_t reduce_impl(const void *const *slices, int n, const ReduceSegment *segs, int n_segs,
                         float inv, float *g, double *partials, unsigned *overflow, cudaStream_t stream) {
     if (n_segs < 1 || n_segs > kMaxSegments) return cudaErrorInvalidValue;
@@ -801,8 +810,8 @@ cudaError_t reduce_impl(const void *const *slices, int n, const ReduceSegment *s
     p.n_seg = n_segs;
     if (ctas < 1) return cudaSuccess;
     if (ctas > 0x7fffffffll) return cudaErrorInvalidValue;
-    return launch_pdl(reduce_unscale_stats<MAXN, BF16, ACC_LP, VPT>, dim3((unsigned)ctas), dim3(kReduceThreads),
-                      0, stream, p);
+    return launch_pdl(reduce_unscale_stats<MAXN, BF16, ACC_LP, VPT, THREADS>, dim3((unsigned)ctas),
+                      dim3(THREADS), 0, stream, p);
 }
 
 template <bool BF16>
@@ -858,25 +867,32 @@ int sm_count() {
     return g_dev[dev].sms;
 }
 
-template <int MAXN, int VPT>
+template <int MAXN, int VPT, int THREADS>
 cudaError_t reduce_dispatch(const void *const *slices, int n, int lp, bool acc_lp, const ReduceSegment *segs,
                             int n_segs, float inv, float *g, double *partials, unsigned *overflow,
                             cudaStream_t stream) {
     if (lp)
-        return acc_lp ? reduce_impl<MAXN, true, true, VPT>(slices, n, segs, n_segs, inv, g, partials, overflow, stream)
-                      : reduce_impl<MAXN, true, false, VPT>(slices, n, segs, n_segs, inv, g, partials, overflow, stream);
-    return acc_lp ? reduce_impl<MAXN, false, true, VPT>(slices, n, segs, n_segs, inv, g, partials, overflow, stream)
-                  : reduce_impl<MAXN, false, false, VPT>(slices, n, segs, n_segs, inv, g, partials, overflow, stream);
+        return acc_lp ? reduce_impl<MAXN, true, true, VPT, THREADS>(slices, n, segs, n_segs, inv, g, partials,
+                                                                    overflow, stream)
+                      : reduce_impl<MAXN, true, false, VPT, THREADS>(slices, n, segs, n_segs, inv, g, partials,
+                                                                     overflow, stream);
+    return acc_lp ? reduce_impl<MAXN, false, true, VPT, THREADS>(slices, n, segs, n_segs, inv, g, partials,
+                                                                 overflow, stream)
+                  : reduce_impl<MAXN, false, false, VPT, THREADS>(slices, n, segs, n_segs, inv, g, partials,
+                                                                  overflow, stream);
 }
 
 cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp, const ReduceSegment *segs,
                           int n_segs, float inv, float *g, double *partials, unsigned *overflow,
                           cudaStream_t stream) {
+    if (n <= kSmallN)
+        return reduce_dispatch<kSmallN, kSmallVpt, kSmallThreads>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g,
+                                                                  partials, overflow, stream);
     if (n <= 64)
-        return reduce_dispatch<64, kReduceVpt>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow,
-                                               stream);
-    return reduce_dispatch<1024, kReduceVpt>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g, partials, overflow,
-                                             stream);
+        return reduce_dispatch<64, kReduceVpt, kReduceThreads>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g,
+                                                               partials, overflow, stream);
+    return reduce_dispatch<1024, kReduceVpt, kReduceThreads>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g,
+                                                             partials, overflow, stream);
 }
 
 cudaError_t launch_decide(const double *partials, double *level2, unsigned *arrivals, int64_t bc_t0,

@@ -1,4 +1,4 @@
-"""Multi-rank host logic on CPU (gloo, world size 2).
+"""Multi-rank host logic on CPU (gloo, world sizes 2 and 3).
 
 Two processes each own half of the partitions of a small job.  The device
 kernels are stood in for by the CPU oracle (this is a host-logic test): each
@@ -101,12 +101,12 @@ def test_partitions_for_covers_each_partition_once():
         partitions_for(2, 2, 4)
 
 
-@pytest.mark.parametrize("inject_at", [None, (3, 1, 77)])
-def test_two_ranks_equal_one_process(orc, inject_at):
+@pytest.mark.parametrize("world,inject_at", [(2, None), (2, (3, 1, 77)), (3, None), (3, (0, 2, 5))])
+def test_ranks_equal_one_process(orc, world, inject_at):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, inject_at, q)) for r in range(2)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, inject_at, q)) for r in range(world)]
     for p in procs:
         p.start()
     res = dict(q.get(timeout=120) for _ in procs)
@@ -114,15 +114,16 @@ def test_two_ranks_equal_one_process(orc, inject_at):
         p.join(timeout=60)
         assert p.exitcode == 0
     # every rank took the same decisions
-    for a, b in zip(res[0], res[1]):
-        assert a[:4] == b[:4]
+    for r in range(1, world):
+        for a, b in zip(res[0], res[r]):
+            assert a[:4] == b[:4]
     # and they equal one process owning every partition; the single process
     # combines per-rank sums in the same order the exchange does
     state = _fresh_state()
     t = 0
     for step, got in zip(range(1, 4), res[0]):
         grads = _inputs(step, inject_at if step == 2 else None)
-        owners = [partitions_for(2, r, N) for r in range(2)]
+        owners = [partitions_for(world, r, N) for r in range(world)]
 
         def remote(_ss, _of, grads=grads, owners=owners):
             return combine_stats([combine_stats([orc.reduce(list(grads[p]), LP, S)[1:]

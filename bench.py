@@ -224,12 +224,16 @@ class Run:
                 self.gather_shards = [None] * w.n_ranks
         self.slice_lists = {r: [self.slices[r][j] for j in range(w.n_ranks)] for r in self.ranks}
         bucket = w.bucket_elems
-        tile = 32768
+        tile = Z.ZERO_NORM_TILE   # buckets are rounded up to whole norm tiles
         if bucket:
             bucket = -(-bucket // tile) * tile
             self.buckets = -(-P // bucket) if P else 0
         else:
             self.buckets = 1 if P else 0
+        # one job over several GPUs: this process's statistics are all-reduced
+        # with the other GPUs' before the decision (set by main())
+        self.group = None
+        self.stats = torch.zeros(2 * w.n_ranks, dtype=torch.float64, device=dev)
 
     def calls(self, stream, slice_lists=None, side=None):
         """The step as an ordered list of (kind, algorithmic HBM bytes, kernel
@@ -293,6 +297,10 @@ class Run:
                 out.append(("reduce", red_b * P, launches,
                             lambda r=r: self.plan.reduce(r, lists[r], self.g[r], self.S,
                                                          w.bucket_elems, sh), stream))
+        if self.group is not None:
+            # the multi-GPU exchange: per-partition statistics, all-reduced
+            # over the GPUs (nccl), then the decision reads the sum
+            out.append(("exchange", 16 * w.n_ranks, 1, lambda: self._exchange(), stream))
         for i, r in enumerate(self.ranks):
             if i == 0:
                 # the step's one decision (norm of every reduced partition,
@@ -306,6 +314,10 @@ class Run:
                                                            self.scales[r], sh), stream))
         return out
 
+    def _exchange(self):
+        from zero_partitioned_mixed_flat_gb300.parallel_host import global_decision_inputs
+        global_decision_inputs(self.plan, self.stats, self.group)
+
     def _adam(self, r, stream, decide_only=False):
         w = self.w
         out = self.shard[r] if w.stage == 3 else self.param
@@ -318,10 +330,11 @@ class Run:
                        w.beta2, w.eps, w.wd, int(w.adamw), self.S, w.clip, 0.0, 0, stream)
 
     def tiles_per_part(self):
-        """Norm tiles (4096 elements) of one partition: per unit shard in stage 3."""
+        """Norm tiles of one partition: per unit shard in stage 3."""
+        t = self.Z.ZERO_NORM_TILE
         if self.w.stage == 3:
-            return sum(-(-self.plan.shard_len(u) // 4096) for u in range(self.plan.n_units))
-        return -(-self.P // 4096)
+            return sum(-(-self.plan.shard_len(u) // t) for u in range(self.plan.n_units))
+        return -(-self.P // t)
 
     def launches_per_step(self):
         import torch
@@ -507,10 +520,22 @@ def main():
         w = dataclasses.replace(w, gather_quantized=True)
         if args.quant_format:
             w = dataclasses.replace(w, quant_format=int(args.quant_format == "fp8"))
-    # weak scaling: every GPU owns its own partition(s) of the simulated job
-    part_ranks = [(r + rank) % w.n_ranks for r in w.ranks]
+    # weak scaling: every GPU owns as many partitions as one GPU does.  When
+    # the GPUs' partitions fit in the job without overlap (rank-r configs),
+    # they form one job: GPU k owns partitions k*len .. (k+1)*len - 1 and the
+    # step's statistics are all-reduced before the decision.  Otherwise
+    # (configs that update every partition on one GPU) each GPU runs its own
+    # replica of the job.
+    per = len(w.ranks)
+    one_job = ws > 1 and ws * per <= w.n_ranks
+    if one_job:
+        part_ranks = [rank * per + i for i in range(per)]
+    else:
+        part_ranks = [(r + rank) % w.n_ranks for r in w.ranks]
     t_setup = time.perf_counter()
     run = Run(w, part_ranks, dev)
+    if one_job:
+        run.group = dist.group.WORLD
     torch.cuda.synchronize()
     log("setup %.1f s: workload %s, P=%d, N=%d, partitions %s" %
         (time.perf_counter() - t_setup, w.name, run.P, w.n_ranks, part_ranks))
@@ -603,6 +628,9 @@ def main():
     n_kind = {k: sum(1 for c in timed_calls if c[0] == k) for k in kinds}
     ms_per_step = total_ms / K
     graph_info = None
+    if args.graph and run.group is not None:
+        log("--graph: not taken with the multi-GPU exchange (its collective is not captured here)")
+        args.graph = False
     if args.graph:
         # the same call list captured once into a CUDA graph and replayed K
         # times: the launches cost no host time; per-kind times stay the eager ones
@@ -651,7 +679,7 @@ def main():
     dom = max(t_kind, key=t_kind.get)
     kname = {"reduce": "reduce_unscale_stats", "adam": "adam_fused_cast", "decide": "norm_decide",
              "gather": "gather_dequant" if run.quantized else "gather_layer_tma",
-             "quantize": "quantize_shard_blocks"}[dom]
+             "quantize": "quantize_shard_blocks", "exchange": "norm_decide"}[dom]
     achieved = b_kind[dom] / (t_kind[dom] / 1e3) / 1e9
     step_gbs = run.bytes_per_step() / (ms_per_step / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
@@ -695,8 +723,14 @@ def main():
                                  if flush is not None else
                                  "inputs larger than L2 (%.1f GB touched per step vs 129 MB L2)"
                                  % (run.bytes_per_step() / 1e9),
-                           "parallelism": "dp%d simulated on each GPU (ranks as device buffers)"
-                                          % w.n_ranks},
+                           "parallelism": ("dp%d job over %d GPUs: GPU k owns partitions %s of "
+                                           "it, step statistics all-reduced (nccl) before the "
+                                           "decision; the other ranks' slices simulated on each "
+                                           "GPU" % (w.n_ranks, ws, "k" if per == 1 else
+                                                    "k*%d..k*%d+%d" % (per, per, per - 1)))
+                                          if run.group is not None else
+                                          ("dp%d simulated on each GPU (ranks as device buffers)"
+                                           % w.n_ranks) + (", one replica per GPU" if ws > 1 else "")},
                 "step_hbm_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
                 "step_frac_of_nominal_8tbs": step_gbs / 8000.0,
                 "bytes_per_element": b, "roofline": roofline, "kernels": kernels,

@@ -25,7 +25,10 @@
  *    `stream`).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
  *    device work of a call is enqueued on it; calls return without waiting,
- *    except the ones documented as synchronising.
+ *    except the ones documented as synchronising.  A synchronising call waits
+ *    for the plan's own device work only (an event recorded after each of its
+ *    calls on each stream it used), never for other streams or other plans;
+ *    it reads and writes the plan's record on a private non-blocking stream.
  *  - Errors are returned as zero_status codes; nothing is thrown.
  *    zero_last_error() gives a message for the last failure on the calling
  *    thread.  On an argument or state error, no device work has been
@@ -38,7 +41,10 @@
  *    zero_adam_step / _range, gathers, quantize) can be captured on a stream
  *    and the graph replayed; each replay is one step with the arguments of
  *    capture time (the step counter, loss scale and skip logic stay on the
- *    device).  The synchronising calls are not capturable.
+ *    device).  The synchronising calls are not capturable.  Once any call of
+ *    a plan has been captured, the plan cannot know where its graph is
+ *    replayed, so its synchronising calls wait for the whole device from then
+ *    on (cudaDeviceSynchronize).
  *  - Low-precision ("lp") values are IEEE binary16 (ZERO_FP16) or bfloat16
  *    (ZERO_BF16), chosen per plan.
  */
@@ -59,13 +65,18 @@ typedef enum {
     ZERO_EALIGN = 2,   /* a device pointer is not 16-byte aligned           */
     ZERO_ENOMEM = 3,   /* host or device allocation of plan scratch failed */
     ZERO_ECUDA = 4,    /* a CUDA runtime call failed (see zero_last_error) */
-    ZERO_ETIMEOUT = 5, /* a bounded device wait ran out (gather pipeline)  */
+    ZERO_ETIMEOUT = 5, /* a bounded device wait ran out (Adam or gather)   */
     ZERO_ESTATE = 6    /* call out of order (e.g. Adam before any reduce)  */
 } zero_status;
 
 typedef enum { ZERO_FP16 = 0, ZERO_BF16 = 1 } zero_lp;
 
 #define ZERO_MAX_RANKS 1024
+
+/* Elements per norm tile: the reduce writes one fp64 partial sum of squares
+ * per tile of each partition (per unit shard in stage 3); buckets are rounded
+ * up to whole tiles. */
+#define ZERO_NORM_TILE 4096
 
 /* ----------------------------------------------------------------------
  * Plan: the flat-buffer partitioner.
@@ -135,15 +146,23 @@ zero_status zero_plan_set_loss_scaler(zero_plan *plan, int32_t growth_interval);
 zero_status zero_plan_set_reduce_precision(zero_plan *plan, int32_t accumulate_in_lp);
 
 /* Resume: set the device step counter t and the good-step count (e.g. from a
- * checkpoint).  Synchronises the device. */
+ * checkpoint).  Synchronising: waits for the plan's own device work first. */
 zero_status zero_plan_set_state(zero_plan *plan, int64_t step,
                                 int32_t good_steps);
 
-/* Bound on the polls of each device-side wait in zero_gather_layer and
- * zero_allgather_params; 0 makes every wait give up at once (used to test the
- * timeout path).  A wait that
- * gives up sets the plan's error word; the next synchronising call
- * (zero_step_result or zero_plan_check) returns ZERO_ETIMEOUT.  Host only. */
+/* Bound on the polls of each device-side pipeline wait (mbarrier try_wait)
+ * of the calls launched after it: zero_adam_step / _range, zero_gather_layer
+ * and zero_allgather_params.  Default 2^22; 0 makes every such wait give up
+ * at once (used to test the timeout path).  A wait that gives up sets the
+ * plan's error word and the kernel stops early: zero_adam_step then leaves
+ * every 1024-element tile it had not yet stored untouched (master, m, v and
+ * param keep their old values there), a gather leaves part of its output
+ * unwritten.  Bulk loads already issued are always waited for (with a fixed
+ * bound) before a CTA exits.  The next synchronising call (zero_step_result
+ * or zero_plan_check) returns ZERO_ETIMEOUT.  The decision of the step is
+ * taken before Adam runs, so after a timed-out zero_adam_step the step
+ * counter has advanced; restore it with zero_plan_set_state before redoing
+ * the step.  Host only. */
 zero_status zero_plan_set_spin_limit(zero_plan *plan, int64_t polls);
 
 /* ----------------------------------------------------------------------
@@ -187,20 +206,37 @@ zero_status zero_reduce_units(zero_plan *plan, int32_t rank, int32_t first_unit,
                               int32_t n_units, const void *const *grad_slices,
                               float *grad_out, float loss_scale, void *stream);
 
-/* Local result of the reduces of the current step: sum of squares (fp64)
- * and overflow flag, for exchanging with other real ranks (pass the others'
- * totals as remote_* to zero_adam_step).  Synchronises `stream`. */
-zero_status zero_partition_stats(zero_plan *plan, double *sumsq,
-                                 int32_t *overflow, void *stream);
+/* Multi-rank use (one process per rank; "10.6 ZeRO 与 FSDP" §10.6.1: the
+ * global norm and overflow need an all-reduce over the ranks; "年糕切片" §4.2
+ * global clipping).  Each rank reduces the partitions it owns, then exports
+ * its per-partition statistics:
+ *   stats: 2*N doubles (N = n_ranks), device memory of the current device,
+ *   managed or pinned host memory, 8-byte aligned.  Written on `stream`:
+ *     stats[p]     = sum over partition p's reduced gradient of g^2, added in
+ *                    the library's fixed order (one fp64 partial per norm
+ *                    tile, a fixed tree over chunks of tiles), if partition p
+ *                    was reduced in the current step (stage 0: p = 0), else +0;
+ *     stats[N + p] = 1.0 if one of partition p's sums was not finite, else 0.
+ * Asynchronous; valid after the step's reduces, before its first Adam call.
+ * A partition is reduced by exactly one rank, so the element-wise sum of every
+ * rank's vector (an all-reduce with sum, in any order) adds only exact zeros:
+ * it equals, bit for bit, the vector of a single process that reduced every
+ * partition. */
+zero_status zero_partition_stats(zero_plan *plan, double *stats, void *stream);
 
-/* Multi-rank use: make this step's decision use exactly these global values
- * (instead of the device's local sum plus remote_sumsq), so that every real
- * rank, given the same totals, takes the bit-identical decision.  global_sumsq
- * is the sum over all ranks of zero_partition_stats' sumsq (added in rank
- * order by the caller); global_overflow the OR of their flags.  Valid after
- * the step's reduces and before its first zero_adam_step.  Host only. */
-zero_status zero_step_set_global_stats(zero_plan *plan, double global_sumsq,
-                                       int32_t global_overflow);
+/* Make this step's decision use an all-reduced statistics vector (2*N
+ * doubles, the layout of zero_partition_stats; same memory kinds) instead of
+ * the plan's own partitions and the remote_* arguments:
+ *   sumsq = the per-partition sums added in partition order by the fixed
+ *           tree the single-process decision uses;  skip = any stats[N + p] != 0.
+ * Every rank holding the same vector takes the bit-identical decision, equal
+ * to the single-process decision over all N partitions.  Host only: the vector
+ * is read by the decision kernel that the step's first zero_adam_step (or
+ * _range) launches, on that call's stream, so it must hold the summed values
+ * by then (e.g. all-reduced on the same stream) and stay unchanged until that
+ * kernel has run.  Valid after the step's reduces and before its first Adam
+ * call (ZERO_ESTATE otherwise). */
+zero_status zero_step_set_global_stats(zero_plan *plan, const double *stats);
 
 /* ----------------------------------------------------------------------
  * Decision + fused Adam/AdamW + cast ("10.6 ZeRO 与 FSDP" §10.6.2 Steps 3-4;
@@ -258,13 +294,14 @@ zero_status zero_adam_step_range(zero_plan *plan, int32_t rank, int64_t begin,
 
 /* Decision of the last decided step: global norm, skipped flag, loss scale
  * for the next step, and the step counter t.  Any pointer may be NULL.
- * Synchronises the device.  Returns ZERO_ETIMEOUT (and clears it) if a
- * bounded device wait gave up since the last check. */
+ * Synchronising: waits for the plan's own device work (not for other streams'
+ * work).  Returns ZERO_ETIMEOUT (and clears it) if a bounded device wait gave
+ * up since the last check. */
 zero_status zero_step_result(zero_plan *plan, double *norm, int32_t *skipped,
                              float *new_loss_scale, int64_t *step);
 
-/* Synchronises the device and reports (then clears) the plan's device error
- * word: ZERO_OK or ZERO_ETIMEOUT. */
+/* Waits for the plan's own device work and reports (then clears) the plan's
+ * device error word: ZERO_OK or ZERO_ETIMEOUT. */
 zero_status zero_plan_check(zero_plan *plan);
 
 /* ----------------------------------------------------------------------
@@ -353,15 +390,17 @@ zero_status zero_gather_layer_quantized(zero_plan *plan, int32_t unit,
  * Computes exactly what zero_reduce_partition computes for one partition in
  * one bucket (same kernel, same bits): grad_out[i] = (sum over j of
  * grad_slices[j][i]) * float(1/(loss_scale*n_ranks)) for i < len, plus
- * *sumsq_out (device double) = the partition's sum of grad_out^2 and
- * *overflow_out (device int32) = 1 if any sum is not finite, else 0.
- * No plan is involved and no step state is touched.
+ * *sumsq_out (device double) = the partition's sum of grad_out^2, added in
+ * the same fixed order, so it equals zero_partition_stats' entry for that
+ * partition bit for bit, and *overflow_out (device int32) = 1 if any sum is
+ * not finite, else 0.  No plan is involved and no step state is touched.
  *
  * Scratch: one fixed array of ZERO_NOALLOC_SCRATCH_BYTES in device memory
  * that belongs to the library image (present on every GPU that loads the
  * library until the process exits); no cudaMalloc/cudaFree or other
  * allocating call is made.  len is limited to ZERO_NOALLOC_MAX_ELEMS (a
- * multiple of 8); larger len returns ZERO_EINVAL.  The first call on each
+ * multiple of 8); larger len returns ZERO_EINVAL.  Devices 0-63 only (the
+ * array's address is kept per device; ZERO_EINVAL beyond).  The first call on each
  * device looks up the array's device address (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture.
  * All calls share the array and it keeps the last call's contents (the
@@ -370,7 +409,9 @@ zero_status zero_gather_layer_quantized(zero_plan *plan, int32_t unit,
  * by the caller.  Inputs and outputs are caller-owned device memory, as for
  * every other call.  Asynchronous on `stream`.
  */
-#define ZERO_NOALLOC_MAX_ELEMS (8192LL * 32768LL)
+/* 65,536 norm tiles of ZERO_NORM_TILE elements */
+#define ZERO_NOALLOC_MAX_ELEMS (65536LL * ZERO_NORM_TILE)
+/* one double per tile + a 256-byte tail (chunk sums, overflow word) */
 #define ZERO_NOALLOC_SCRATCH_BYTES (65536 * 8 + 256)
 zero_status zero_reduce_partition_noalloc(int32_t n_ranks, zero_lp lp,
                                           const void *const *grad_slices,

@@ -15,7 +15,7 @@ import zero_partitioned_mixed_flat_gb300 as Z
 from zero_partitioned_mixed_flat_gb300 import synth
 from zero_partitioned_mixed_flat_gb300.workloads import WORKLOADS, Workload
 
-from .zstep import Harness, max_rel_err, same_floats
+from .zstep import Harness, lp_ulp_dist, max_rel_err, plan_stats, same_floats
 
 pytestmark = pytest.mark.gpu
 TILE = 4096
@@ -35,7 +35,7 @@ def _reduce_case(zlib, n, part, lp, scale, bucket=0, rank=0, seed=0, acc_lp=Fals
     slices = [synth.grad_slice(part, lp, 1.0, scale, seed, 1, j, rank, dev) for j in range(n)]
     g = torch.empty(part, dtype=torch.float32, device=dev)
     plan.reduce(rank, slices, g, scale, bucket)
-    ss, of = plan.stats()
+    ss, of, _ = plan_stats(plan)
     host = [synth.to_numpy_codes(t) for t in slices]
     og, oss, oof = (oracle.reduce_lp_accum if acc_lp else oracle.reduce)(host, lp, scale)
     assert same_floats(g.cpu().numpy(), og)
@@ -254,7 +254,7 @@ def test_nan_and_remote_terms(zlib):
     assert r["skipped"] == 1 and r["step"] == 0 and not w.any().item()
     # remote sum of squares joins the global norm
     plan.reduce(0, sl, g, 1.0)
-    ss, _ = plan.stats()
+    ss, _, _ = plan_stats(plan)
     plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0, 3.0 * ss, 0)
     r = plan.result()
     assert abs(r["norm"] - np.sqrt(4.0 * ss)) <= 1e-6 * r["norm"] and r["step"] == 1
@@ -425,6 +425,91 @@ def test_gather_wait_timeout_is_reported_and_recoverable(zlib):
     plan2.close()
 
 
+@pytest.mark.parametrize("part", [40_000, 4_000_000])
+def test_adam_wait_timeout_is_reported_and_recoverable(zlib, part):
+    # spin limit 0: every pipeline wait of the Adam kernel gives up at once.
+    # 40,000 elements: one tile per CTA (the producer issues everything, then
+    # drains); 4M: ~13 tiles per CTA (the producer's own wait gives up after
+    # four tiles, then it drains).  No tile may be stored: master, m, v and
+    # the lp param keep their old values; the error word reports ZERO_ETIMEOUT
+    # and is cleared; the same plan then redoes the step (counter restored)
+    # and matches the oracle.
+    dev = torch.device("cuda")
+    n, rank, lp, lr, b1, b2, eps, wd, clip = 3, 1, 0, 1e-3, 0.9, 0.999, 1e-8, 0.01, 0.05
+    plan = _plan(n * part, n, lp, stage=2)
+    assert plan.part_len == part
+    sl = [synth.grad_slice(part, lp, 1e-2, 64.0, 8, 1, j, rank, dev) for j in range(n)]
+    g = torch.empty(part, device=dev)
+    w0 = synth.master_init(part, 0.02, 8, rank, dev)
+    m0 = torch.full((part,), 1e-3, device=dev)
+    v0 = torch.full((part,), 1e-6, device=dev)
+    w, m, v = w0.clone(), m0.clone(), v0.clone()
+    param = torch.full((n * part,), 7.0, dtype=torch.float16, device=dev)
+    hp = (lr, b1, b2, eps, wd, 1, 64.0, clip)
+    plan.reduce(rank, sl, g, 64.0)
+    plan.set_spin_limit(0)
+    plan.adam(rank, g, w, m, v, param, *hp)
+    with pytest.raises(Z.ZeroError) as e:
+        plan.result()
+    assert e.value.code == Z.ZERO_ETIMEOUT
+    plan.check()   # the error word was cleared
+    assert torch.equal(w, w0) and torch.equal(m, m0) and torch.equal(v, v0)
+    assert bool((param == 7.0).all())
+    # redo the step on the same plan and context
+    plan.set_state(0, 0)
+    plan.set_spin_limit(1 << 22)
+    plan.reduce(rank, sl, g, 64.0)
+    plan.adam(rank, g, w, m, v, param, *hp)
+    r = plan.result()
+    og, oss, oof = oracle.reduce([synth.to_numpy_codes(t) for t in sl], lp, 64.0)
+    assert same_floats(g.cpu().numpy(), og)
+    d = oracle.decide(oss, oof, np.float32(clip), 64.0, 0, 0, 1000, np.float32(b1), np.float32(b2))
+    assert r["step"] == d["step"] == 1 and r["skipped"] == 0
+    assert abs(r["norm"] - d["norm"]) <= 1e-5 * d["norm"]
+    ow, om, ov = w0.cpu().numpy().copy(), m0.cpu().numpy().copy(), v0.cpu().numpy().copy()
+    op = oracle.adam(og, ow, om, ov, lp, d["coef"], d["skip"], np.float32(lr), np.float32(b1),
+                     np.float32(b2), np.float32(eps), np.float32(wd), 1, d["bc1"], d["bc2"])
+    for got, exp in ((w, ow), (m, om), (v, ov)):
+        assert max_rel_err(got.cpu().numpy(), exp) <= 1e-6
+    assert lp_ulp_dist(synth.to_numpy_codes(param[rank * part:(rank + 1) * part]), op) <= 1
+    plan.close()
+
+
+def test_synchronising_calls_wait_only_for_the_plan(zlib):
+    # zero_step_result, zero_plan_check and zero_plan_set_state wait for the
+    # plan's own work, not for a long kernel on an unrelated stream
+    import time
+    dev = torch.device("cuda")
+    n, part = 2, 2 * TILE
+    plan = _plan(n * part, n, 0)
+    sl = [synth.grad_slice(part, 0, 1e-2, 1.0, 9, 1, j, 0, dev) for j in range(n)]
+    g = torch.empty(part, device=dev)
+    w, m, v = (torch.zeros(part, device=dev) for _ in range(3))
+    mine, other = torch.cuda.Stream(), torch.cuda.Stream()
+    hp = (1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0)
+    plan.reduce(0, sl, g, 1.0, stream=mine)          # warm: scratch, modules
+    plan.adam(0, g, w, m, v, None, *hp, stream=mine)
+    plan.result()
+    torch.cuda.synchronize()
+    done = torch.cuda.Event()
+    with torch.cuda.stream(other):
+        torch.cuda._sleep(int(3e9))                  # about 1.5 s of spinning
+        done.record(other)
+    t0 = time.perf_counter()
+    plan.reduce(0, sl, g, 1.0, stream=mine)
+    plan.adam(0, g, w, m, v, None, *hp, stream=mine)
+    r = plan.result()
+    plan.check()
+    plan.set_state(r["step"], 0)
+    el = time.perf_counter() - t0
+    still_running = not done.query()
+    torch.cuda.synchronize()
+    assert done.query()
+    assert r["step"] == 2
+    assert still_running, "a synchronising call waited for another stream's kernel (%.3f s)" % el
+    plan.close()
+
+
 @pytest.mark.parametrize("n,lp,bucket", [(2, 0, 0), (3, 1, 4096), (8, 0, 1000), (64, 1, 200_000),
                                          (5, 0, 8)])
 def test_allgather_params_buckets(zlib, n, lp, bucket):
@@ -450,33 +535,89 @@ def test_allgather_params_buckets(zlib, n, lp, bucket):
 
 
 def test_global_stats_replace_the_local_sum(zlib):
-    # multi-rank use: the caller's global totals decide the step exactly
+    # multi-rank use: an all-reduced statistics vector decides the step.  One
+    # process reducing all four partitions (identical slices) and one that
+    # reduced only partition 0 but is handed the vector of all four take the
+    # same decision, bit for bit.
     dev = torch.device("cuda")
-    n, part = 4, 3 * TILE
-    plan = _plan(n * part, n, 1)
+    n, part = 4, 3 * TILE + 40
     sl = [synth.grad_slice(part, 1, 1e-3, 1.0, 0, 1, j, 0, dev) for j in range(n)]
-    g = torch.empty(part, device=dev)
-    w = torch.zeros(part, device=dev); m = torch.zeros(part, device=dev); v = torch.zeros(part, device=dev)
-    plan.reduce(0, sl, g, 1.0)
-    ss, of = plan.stats()
-    plan.set_global_stats(4.0 * ss, 0)
-    plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0, 123.0, 0)
-    r = plan.result()
-    assert r["norm"] == float(np.sqrt(4.0 * ss)) and r["skipped"] == 0
-    d = oracle.decide(4.0 * ss, 0, 1.0, 1.0, 0)
-    assert d["norm"] == r["norm"]
-    # a global overflow skips even though this rank's partition is finite
-    plan.reduce(0, sl, g, 1.0)
-    plan.set_global_stats(ss, 1)
+    hp = (1e-3, .9, .999, 1e-8, 0., 1, 1.0, 0.05)
+
+    def fresh():
+        z = lambda: torch.zeros(part, device=dev)
+        return torch.empty(part, device=dev), z(), z(), z()
+
+    full = _plan(n * part, n, 1)
+    gs = [fresh() for _ in range(n)]
+    for r in range(n):
+        full.reduce(r, sl, gs[r][0], 1.0)
+    _, _, vec_all = plan_stats(full)
+    for r in range(n):
+        full.adam(r, *gs[r], None, *hp)
+    ref = full.result()
+    one = _plan(n * part, n, 1)
+    g, w, m, v = fresh()
+    one.reduce(0, sl, g, 1.0)
+    _, _, vec0 = plan_stats(one)
+    assert vec0[0] == vec_all[0] and not vec0[1:].any()     # only partition 0, exact zeros elsewhere
+    assert np.array_equal(vec_all[:n], np.full(n, vec_all[0]))
+    stats = torch.from_numpy(vec_all.copy()).to(dev)
+    one.set_global_stats(stats)
+    one.adam(0, g, w, m, v, None, *hp, 123.0, 1)               # remote terms are ignored
+    r1 = one.result()
+    assert r1 == ref, (r1, ref)
+    assert torch.equal(w, gs[0][1]) and torch.equal(m, gs[0][2]) and torch.equal(v, gs[0][3])
+    # the vector's sums match the oracle's
+    _, oss, _ = oracle.reduce([synth.to_numpy_codes(t) for t in sl], 1, 1.0)
+    assert abs(vec_all[0] - oss) <= 1e-9 * oss
+    # an overflow flag of another partition skips this rank's step
+    one.reduce(0, sl, g, 1.0)
+    flagged = stats.clone()
+    flagged[n + 2] = 1.0
+    one.set_global_stats(flagged)
     before = w.clone()
-    plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0)
-    r = plan.result()
-    assert r["skipped"] == 1 and torch.equal(before, w)
+    one.adam(0, g, w, m, v, None, *hp)
+    r2 = one.result()
+    assert r2["skipped"] == 1 and torch.equal(before, w)
     # out of order: after the decision the step's stats are fixed
     with pytest.raises(Z.ZeroError) as e:
-        plan.set_global_stats(ss, 0)
+        one.set_global_stats(stats)
     assert e.value.code == Z.ZERO_ESTATE
-    plan.close()
+    with pytest.raises(Z.ZeroError) as e:
+        one.partition_stats(stats)
+    assert e.value.code == Z.ZERO_ESTATE
+    full.close()
+    one.close()
+
+
+def test_exported_stats_decide_like_the_local_sum(zlib):
+    # every partition of a ragged random plan reduced in one process: deciding
+    # from the exported vector gives the local decision's bits (norm included)
+    dev = torch.device("cuda")
+    rng = np.random.default_rng(77)
+    for n, sizes in [(3, [100_000, 7, 33_333]), (17, [int(x) for x in rng.integers(1, 90_000, 6)])]:
+        res = []
+        for mode in ("local", "global"):
+            plan = _plan(-1, n, 0, stage=2, sizes=sizes)
+            P = plan.part_len
+            g = torch.empty((n, P), device=dev)
+            w = synth.master_init(n * P, 0.02, 3, 0, dev).view(n, P)
+            m, v = torch.zeros_like(w), torch.zeros_like(w)
+            for r in range(n):
+                sl = [synth.grad_slice(P, 0, 1e-2, 64.0, 3, 1, j, r, dev) for j in range(n)]
+                plan.reduce(r, sl, g[r], 64.0)
+            if mode == "global":
+                stats = torch.empty(2 * n, dtype=torch.float64, device=dev)
+                plan.partition_stats(stats)
+                plan.set_global_stats(stats)
+            for r in range(n):
+                plan.adam(r, g[r], w[r], m[r], v[r], None, 1e-3, .9, .999, 1e-8, 0.01, 1, 64.0, 0.05)
+            res.append((plan.result(), w.clone(), m.clone(), v.clone()))
+            plan.close()
+        assert res[0][0] == res[1][0]
+        for a, b in zip(res[0][1:], res[1][1:]):
+            assert torch.equal(a, b)
 
 
 # ------------------------------------------------------ quantized gather
@@ -648,7 +789,7 @@ def test_reduce_reads_pinned_host_slices(zlib, lp):
         plan = _plan(n * part, n, lp)
         g = torch.empty(part, dtype=torch.float32, device=dev)
         plan.reduce(0, sl, g, 1.0)
-        out.append((g, plan.stats()))
+        out.append((g, plan_stats(plan)[:2]))
         plan.close()
     assert same_floats(out[0][0].cpu().numpy(), out[1][0].cpu().numpy())
     assert out[0][1] == out[1][1]
@@ -678,7 +819,7 @@ def test_stage3_unit_by_unit_reduce_equals_partition_reduce(zlib, lp):
             plan.reduce_units(1, 0, 1, sl, g, 1.0)
         else:
             plan.reduce(1, sl, g, 1.0, bucket_elems=3 * TILE + 5)
-        res.append((g.cpu().numpy(), plan.stats(), [synth.to_numpy_codes(t) for t in sl]))
+        res.append((g.cpu().numpy(), plan_stats(plan)[:2], [synth.to_numpy_codes(t) for t in sl]))
         plan.close()
     for other in res[1:]:
         assert same_floats(res[0][0], other[0])
@@ -700,7 +841,7 @@ def test_partly_reduced_partition_counts_only_its_part(zlib):
     w = torch.zeros(P, device=dev); m = torch.zeros(P, device=dev); v = torch.zeros(P, device=dev)
     plan.adam(0, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 0.0)
     plan.reduce_units(0, 1, 1, sl, g, 1.0)          # step 2: unit 1 only
-    ss, _ = plan.stats()
+    ss, _, _ = plan_stats(plan)
     off = plan.unit_shard_offset(1)
     _, oss, _ = oracle.reduce([synth.to_numpy_codes(t[off:]) for t in sl], 0, 1.0)
     assert abs(ss - oss) <= 1e-9 * oss

@@ -1,11 +1,18 @@
 """Multi-rank host logic on CPU (gloo, world sizes 2 and 3).
 
-Two processes each own half of the partitions of a small job.  The device
-kernels are stood in for by the CPU oracle (this is a host-logic test): each
-rank reduces its partitions, the ranks exchange (sum of squares, overflow)
-with parallel_host.exchange_stats, decide, update, and all-gather the new
-parameters.  Both ranks must take the identical decision, and the result must
-equal the single-process step over all partitions bit for bit.
+Processes each own some of the partitions of a small job.  The device kernels
+are stood in for by the CPU oracle (this is a host-logic test; the same flow
+through libzero runs on the GPU in test_gpu_multirank.py).  Each rank reduces
+its partitions into a per-partition statistics vector (zero for partitions it
+does not own), the ranks all-reduce the vectors with
+parallel_host.allreduce_stats, decide, update their partitions, and
+all-gather the new parameters with parallel_host.allgather_partitions.
+
+The all-reduced vector must equal, bit for bit, the vector of one process
+that reduced every partition (only exact zeros are added), so every rank and
+the single process take the same decision and produce the same parameters,
+whatever the world size or the ownership.  The reduce-scatter's data path
+(exchange_gradients, an all-to-all) is checked on its own.
 """
 import os
 import socket
@@ -15,7 +22,9 @@ import pytest
 import torch
 import torch.multiprocessing as mp
 
-from zero_partitioned_mixed_flat_gb300.parallel_host import (combine_stats, exchange_stats,
+from zero_partitioned_mixed_flat_gb300.parallel_host import (allgather_partitions,
+                                                            allreduce_stats,
+                                                            exchange_gradients,
                                                             partitions_for)
 
 N, P, LP, S = 4, 4096, 0, 1024.0
@@ -30,16 +39,30 @@ def _inputs(step, inject=None):
     return g.view(np.uint16)
 
 
-def _step_partitions(orc, parts, grads, state, t, remote=None):
-    """Reduce + (exchange) + decide + Adam on `parts`; returns (decision, params)."""
-    local = []
+def _fresh_state():
+    rng = np.random.default_rng(7)
+    return {p: ((rng.standard_normal(P) * 0.02).astype(np.float32), np.zeros(P, np.float32),
+                np.zeros(P, np.float32)) for p in range(N)}
+
+
+def _reduce_into_vector(orc, parts, grads):
+    """Reduced gradients of `parts` and the 2N statistics vector (zeros elsewhere)."""
+    vec = np.zeros(2 * N, np.float64)
     red = {}
     for p in parts:
         red[p], ss, of = orc.reduce(list(grads[p]), LP, S)
-        local.append((ss, of))
-    ss, of = combine_stats(local)
-    if remote is not None:
-        ss, of = remote(ss, of)
+        vec[p] = ss
+        vec[N + p] = 1.0 if of else 0.0
+    return red, vec
+
+
+def _decide_and_update(orc, parts, red, vec, state, t):
+    # any fixed order stands in for the library's tree: every rank applies it
+    # to the same vector
+    ss = 0.0
+    for p in range(N):
+        ss += float(vec[p])
+    of = int(np.any(vec[N:] != 0))
     d = orc.decide(ss, of, HP["clip"], S, t, 0, 1000, HP["beta1"], HP["beta2"])
     params = {}
     for p in parts:
@@ -50,12 +73,6 @@ def _step_partitions(orc, parts, grads, state, t, remote=None):
     return d, params
 
 
-def _fresh_state():
-    rng = np.random.default_rng(7)
-    return {p: ((rng.standard_normal(P) * 0.02).astype(np.float32), np.zeros(P, np.float32),
-                np.zeros(P, np.float32)) for p in range(N)}
-
-
 def _worker(rank, world, port, inject_at, q):
     import torch.distributed as dist
     import oracle as orc
@@ -64,23 +81,27 @@ def _worker(rank, world, port, inject_at, q):
     try:
         mine = partitions_for(world, rank, N)
         state = _fresh_state()
+        full = torch.zeros(N * P, dtype=torch.int16)       # lp codes of the full layout
         t = 0
         out = []
         for step in range(1, 4):
             grads = _inputs(step, inject_at if step == 2 else None)
-            # the combine must be in rank order: sum of each rank's (already
-            # rank-ordered) partition sums -- exchange_stats does exactly that
-            d, params = _step_partitions(orc, mine, grads, state, t,
-                                         remote=lambda ss, of: exchange_stats(ss, of))
+            red, vec = _reduce_into_vector(orc, mine, grads)
+            stats = torch.from_numpy(vec)
+            allreduce_stats(stats)
+            d, params = _decide_and_update(orc, mine, red, stats.numpy(), state, t)
             if not d["skip"]:
                 t = d["step"]
-            full = [None] * world
-            dist.all_gather_object(full, {p: params[p].tolist() for p in mine})
-            merged = {}
-            for f in full:
-                merged.update(f)
-            out.append((d["norm"], d["coef"], d["skip"], d["step"],
-                        [merged[p] for p in range(N)] if not d["skip"] else None))
+                for p in mine:
+                    full[p * P:(p + 1) * P] = torch.from_numpy(params[p].view(np.int16))
+            # every partition's owner sends it; round-robin owners -> gather per owner
+            for p in range(N):
+                owner = p % world
+                piece = full[p * P:(p + 1) * P].clone().view(torch.float16)  # gloo moves fp16 bytes
+                dist.broadcast(piece, src=owner)
+                full[p * P:(p + 1) * P] = piece.view(torch.int16)
+            out.append((stats.numpy().copy(), d["norm"], d["coef"], d["skip"], d["step"],
+                        full.numpy().copy()))
         q.put((rank, out))
     finally:
         dist.destroy_process_group()
@@ -90,6 +111,25 @@ def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
         return s.getsockname()[1]
+
+
+def _spawn(target, world, *args, timeout=120):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=target, args=(r, world, port) + args + (q,)) for r in range(world)]
+    for p in procs:
+        p.start()
+    try:
+        res = dict(q.get(timeout=timeout) for _ in procs)
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.kill()
+    for p in procs:
+        assert p.exitcode == 0
+    return res
 
 
 def test_partitions_for_covers_each_partition_once():
@@ -103,36 +143,55 @@ def test_partitions_for_covers_each_partition_once():
 
 @pytest.mark.parametrize("world,inject_at", [(2, None), (2, (3, 1, 77)), (3, None), (3, (0, 2, 5))])
 def test_ranks_equal_one_process(orc, world, inject_at):
-    ctx = mp.get_context("spawn")
-    q = ctx.Queue()
-    port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, world, port, inject_at, q)) for r in range(world)]
-    for p in procs:
-        p.start()
-    res = dict(q.get(timeout=120) for _ in procs)
-    for p in procs:
-        p.join(timeout=60)
-        assert p.exitcode == 0
-    # every rank took the same decisions
-    for r in range(1, world):
+    res = _spawn(_worker, world, inject_at)
+    for r in range(1, world):      # every rank holds the same vector, decision and layout
         for a, b in zip(res[0], res[r]):
-            assert a[:4] == b[:4]
-    # and they equal one process owning every partition; the single process
-    # combines per-rank sums in the same order the exchange does
+            assert a[0].tobytes() == b[0].tobytes()
+            assert a[1:5] == b[1:5]
+            assert np.array_equal(a[5], b[5])
     state = _fresh_state()
+    full = np.zeros(N * P, np.int16)
     t = 0
     for step, got in zip(range(1, 4), res[0]):
         grads = _inputs(step, inject_at if step == 2 else None)
-        owners = [partitions_for(world, r, N) for r in range(world)]
-
-        def remote(_ss, _of, grads=grads, owners=owners):
-            return combine_stats([combine_stats([orc.reduce(list(grads[p]), LP, S)[1:]
-                                                 for p in o]) for o in owners])
-        d, params = _step_partitions(orc, list(range(N)), grads, state, t, remote=remote)
+        red, vec = _reduce_into_vector(orc, list(range(N)), grads)
+        assert vec.tobytes() == got[0].tobytes()   # the all-reduce added only exact zeros
+        d, params = _decide_and_update(orc, list(range(N)), red, vec, state, t)
+        assert (d["norm"], d["coef"], d["skip"], d["step"]) == got[1:5]
         if not d["skip"]:
             t = d["step"]
-        assert (d["norm"], d["coef"], d["skip"], d["step"]) == got[:4]
-        if not d["skip"]:
-            assert [params[p].tolist() for p in range(N)] == got[4]
+            for p in range(N):
+                full[p * P:(p + 1) * P] = params[p].view(np.int16)
+        assert np.array_equal(full, got[5])
     if inject_at is not None:
-        assert res[0][1][2] == 1     # the overflow on one rank skipped the step everywhere
+        assert res[0][1][3] == 1     # the overflow on one rank skipped the step everywhere
+
+
+def _data_path_worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        part = 40
+        # rank j's flat gradient: value 1000*j + flat index (exact in fp16 below 2048)
+        grad = (torch.arange(world * part, dtype=torch.float32) + 1000 * rank).to(torch.float16)
+        slices = torch.empty((world, part), dtype=torch.float16)
+        exchange_gradients(grad, slices)
+        layout = torch.full((world * part,), -1, dtype=torch.float16)
+        layout[rank * part:(rank + 1) * part] = rank
+        allgather_partitions(layout, rank, part)
+        q.put((rank, (slices.float().numpy(), layout.float().numpy())))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_reduce_scatter_input_and_allgather_move_the_right_bytes(world):
+    res = _spawn(_data_path_worker, world)
+    part = 40
+    for r in range(world):
+        slices, layout = res[r]
+        for j in range(world):      # row j: rank j's gradient over partition r
+            exp = 1000 * j + np.arange(r * part, (r + 1) * part)
+            assert np.array_equal(slices[j], exp.astype(np.float16).astype(np.float32)), (r, j)
+        assert np.array_equal(layout, np.repeat(np.arange(world), part))

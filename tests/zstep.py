@@ -59,6 +59,19 @@ def lp_ulp_dist(a: np.ndarray, b: np.ndarray) -> int:
     return int(np.max(np.abs(key(a) - key(b))))
 
 
+def plan_stats(plan, stream=None):
+    """The plan's exported statistics for the current step (zero_partition_stats):
+    (exact sum of the per-partition sums of squares, any overflow, the 2N vector).
+    The exact sum (math.fsum) is only the test's yardstick for the oracle's
+    sequential sum; the library's own sum is the one inside the decision."""
+    n = plan.n_ranks
+    t = torch.full((2 * n,), float("nan"), dtype=torch.float64, device="cuda")
+    plan.partition_stats(t, stream)
+    torch.cuda.synchronize()
+    v = t.cpu().numpy()
+    return math.fsum(v[:n]), int(np.any(v[n:] != 0)), v
+
+
 def coef_from_norm(norm: float, clip: float) -> float:
     if clip > 0:
         c = clip / (norm + 1e-6)

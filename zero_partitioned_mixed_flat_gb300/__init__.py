@@ -7,7 +7,8 @@ used for device memory and streams.
 """
 from ._abi import (  # noqa: F401
     LIB_PATH, SIGNATURES, STATUS_NAMES, ZERO_BF16, ZERO_EALIGN, ZERO_ECUDA, ZERO_EINVAL,
-    ZERO_ENOMEM, ZERO_ESTATE, ZERO_ETIMEOUT, ZERO_FP16, ZERO_MAX_RANKS, ZERO_OK, ZeroError,
+    ZERO_ENOMEM, ZERO_ESTATE, ZERO_ETIMEOUT, ZERO_FP16, ZERO_MAX_RANKS, ZERO_NORM_TILE, ZERO_OK,
+    ZeroError,
     load, zero_adam_step, zero_adam_step_range, zero_allgather_params, zero_gather_layer,
     zero_last_error,
     zero_memory_report, zero_partition_stats, zero_plan_check, zero_plan_create,

@@ -20,6 +20,7 @@ STATUS_NAMES = ["ZERO_OK", "ZERO_EINVAL", "ZERO_EALIGN", "ZERO_ENOMEM", "ZERO_EC
                 "ZERO_ETIMEOUT", "ZERO_ESTATE"]
 ZERO_FP16, ZERO_BF16 = 0, 1
 ZERO_MAX_RANKS = 1024
+ZERO_NORM_TILE = 4096
 ZERO_QUANT_INT8, ZERO_QUANT_FP8_E4M3 = 0, 1
 
 # every exported entry point of include/zero.h, with its ctypes signature
@@ -36,8 +37,8 @@ SIGNATURES = {
     "zero_plan_set_gather_quantization": (_i32, [_vp, _i32]),
     "zero_reduce_partition": (_i32, [_vp, _i32, _vp, _vp, _f32, _i64, _vp]),
     "zero_reduce_units": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _f32, _vp]),
-    "zero_partition_stats": (_i32, [_vp, _vp, _vp, _vp]),
-    "zero_step_set_global_stats": (_i32, [_vp, _f64, _i32]),
+    "zero_partition_stats": (_i32, [_vp, _vp, _vp]),
+    "zero_step_set_global_stats": (_i32, [_vp, _vp]),
     "zero_adam_step": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32,
                               _f32, _i32, _f32, _f32, _f64, _i32, _vp]),
     "zero_adam_step_range": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _f32, _f32,
@@ -197,16 +198,14 @@ def zero_reduce_units(plan: int, rank: int, first_unit: int, n_units: int, grad_
                                     _stream(stream)), "zero_reduce_units")
 
 
-def zero_partition_stats(plan: int, stream=None):
-    ss, of = _f64(), _i32()
-    _check(load().zero_partition_stats(plan, C.byref(ss), C.byref(of), _stream(stream)),
-           "zero_partition_stats")
-    return ss.value, of.value
+def zero_partition_stats(plan: int, stats, stream=None):
+    """stats: 2*N float64 (device, managed or pinned host), written on stream."""
+    _check(load().zero_partition_stats(plan, _ptr(stats), _stream(stream)), "zero_partition_stats")
 
 
-def zero_step_set_global_stats(plan: int, global_sumsq: float, global_overflow: int):
-    _check(load().zero_step_set_global_stats(plan, global_sumsq, int(global_overflow)),
-           "zero_step_set_global_stats")
+def zero_step_set_global_stats(plan: int, stats):
+    """stats: the all-reduced 2*N float64 vector (read by the step's decision)."""
+    _check(load().zero_step_set_global_stats(plan, _ptr(stats)), "zero_step_set_global_stats")
 
 
 def zero_adam_step(plan: int, rank: int, grad, master, m, v, param_out, lr: float,
@@ -268,7 +267,7 @@ def zero_gather_layer_quantized(plan: int, unit: int, codes: Sequence, scales: S
                                               _stream(stream)), "zero_gather_layer_quantized")
 
 
-ZERO_NOALLOC_MAX_ELEMS = 8192 * 32768
+ZERO_NOALLOC_MAX_ELEMS = 65536 * ZERO_NORM_TILE
 
 
 def zero_reduce_partition_noalloc(n_ranks: int, lp: int, grad_slices: Sequence, length: int,

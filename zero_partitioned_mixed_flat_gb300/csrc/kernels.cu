@@ -21,6 +21,7 @@
 // kernel starts with pdl_enter() (launch.h): it waits for the previous grid of
 // the stream before touching global memory.
 #include "launch.h"
+#include "norm_tree.cuh"
 #include "zero_internal.h"
 
 #include <cuda_bf16.h>
@@ -255,124 +256,129 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
 struct DecideParams {
     const double *partials;
     double *level2;
-    unsigned *arrivals;  // 0 at launch; the last block resets it
+    const unsigned *overflow;  // per slot
+    unsigned *arrivals;        // 0 at launch; the last block resets it
+    double *stats_out;         // export: 2 * n_slots
+    const double *stats_in;    // global: 2 * n_slots
     long long tiles_per_slot;
     int chunks_per_slot;
-    int n_items;         // reduced slots x chunks per slot (>= 1)
+    int n_active;              // reduced slots (local, export)
+    int n_slots;
+    int mode;                  // NormMode
     double remote_sumsq;
-    double global_sumsq;
     int remote_overflow;
-    int use_global;  // 1: the caller's global sum replaces local + remote
     float clip, loss_scale, beta1, beta2;
     int growth_interval;
     StepRecord *rec;
     long long bc_t0;             // bc*_tab[i] is for step counter bc_t0 - i
     float bc1_tab[kBcTable], bc2_tab[kBcTable];
-    short slots[1024];   // the step's reduced partition slots, ascending
+    short slots[kNormMaxSlots];  // the step's reduced partition slots, ascending
 };
 
-constexpr int kDecideThreads = 256;
+constexpr int kDecideThreads = kNormThreads;
 
+// The norm in fixed-order fp64 levels (norm_tree.cuh) and, unless exporting,
+// the step decision, in one launch.  Local and export modes: block `item`
+// sums one chunk of one reduced partition's tile partials (level 1); the last
+// block to arrive (counted after a fence) forms each partition's sum (level 2)
+// in a vector indexed by partition.  Global mode: one block takes that vector
+// from the caller (every rank's vectors summed element-wise).  Then export
+// writes the vector and the partitions' overflow flags; the decision sums the
+// vector (level 3), adds the remote term (local mode), and decides.  The order
+// of every addition depends only on the partition sizes, never on which block
+// finishes first.
 // fp64 adds are slow on this part (a 64-cycle latency, under 2 per cycle per
-// SM), so every fixed-order sum here is a tree, never a long chain.
-__device__ __forceinline__ double warp_sum_fixed(double acc) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
-    return acc;  // lane 0's value is the one used
-}
-
-__device__ __forceinline__ double block_sum_fixed(double acc, double *wsum) {
-    acc = warp_sum_fixed(acc);
-    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = acc;
-    __syncthreads();
-    double t = 0.0;
-    if (threadIdx.x == 0) {  // pairwise over the warps
-        double w[kDecideThreads / 32];
-#pragma unroll
-        for (int i = 0; i < kDecideThreads / 32; ++i) w[i] = wsum[i];
-#pragma unroll
-        for (int h = kDecideThreads / 64; h >= 1; h >>= 1)
-#pragma unroll
-            for (int i = 0; i < h; ++i) w[i] = __dadd_rn(w[i], w[i + h]);
-        t = w[0];
-    }
-    return t;  // valid in thread 0
-}
-
-// The norm in two fixed-order fp64 levels and the step decision, in one
-// launch: block `item` sums one fixed chunk of one reduced partition's tile
-// partials; the last block to arrive (counted after a fence) sums those
-// chunk sums in item order and decides.  The order of every addition depends
-// only on the partition sizes, never on which block finishes first.
+// SM), so every fixed-order sum is a tree, never a long chain.
 __global__ void __launch_bounds__(kDecideThreads)
 norm_decide(const __grid_constant__ DecideParams p) {
     pdl_enter();
     __shared__ double wsum[kDecideThreads / 32];
+    __shared__ double vec[kNormMaxSlots];
+    __shared__ unsigned char flag[kNormMaxSlots];
     __shared__ float bias_corr[2];
+    __shared__ int any_overflow;
     __shared__ bool last;
     StepRecord *rec = p.rec;
-    {
+    if (p.mode != kDecideGlobal) {
         const int item = blockIdx.x;
         const int slot = p.slots[item / p.chunks_per_slot];
         const long long t0 = (long long)(item % p.chunks_per_slot) * kPartialChunk;
         const long long t1 = t0 + kPartialChunk < p.tiles_per_slot ? t0 + kPartialChunk : p.tiles_per_slot;
-        const double *q = p.partials + (long long)slot * p.tiles_per_slot;
-        // every load first, then a pairwise tree (a missing term adds 0)
-        constexpr int kPer = (int)(kPartialChunk / kDecideThreads);
-        static_assert((kPer & (kPer - 1)) == 0 && ((kDecideThreads / 32) & (kDecideThreads / 32 - 1)) == 0,
-                      "pairwise trees need powers of two");
-        double x[kPer];
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            const long long t = t0 + threadIdx.x + (long long)i * kDecideThreads;
-            x[i] = t < t1 ? q[t] : 0.0;
-        }
-        // bias corrections for t + 1 (the step counter if the step is not
-        // skipped): from the host's table when it holds that counter, else two
-        // lanes compute them in fp64 while the loads are in flight.  The record
-        // is written only by the last block, after every block has arrived, so
-        // every block reads the step's old t.
-        if (threadIdx.x == 32 || threadIdx.x == 64) {
-            const int b = threadIdx.x == 64;
-            const long long tn = rec->step + 1;
-            const long long i = p.bc_t0 - tn;
-            if (i >= 0 && i < kBcTable) {
-                bias_corr[b] = b ? p.bc2_tab[i] : p.bc1_tab[i];
-            } else {
-                const double beta = b ? (double)p.beta2 : (double)p.beta1;
-                bias_corr[b] = __double2float_rn(__dsub_rn(1.0, pow(beta, (double)tn)));
-            }
-        }
-#pragma unroll
-        for (int h = kPer / 2; h >= 1; h >>= 1)  // pairwise within the thread
-#pragma unroll
-            for (int i = 0; i < h; ++i) x[i] = __dadd_rn(x[i], x[i + h]);
-        const double chunk = block_sum_fixed(x[0], wsum);
+        const double chunk = chunk_sum(p.partials + (long long)slot * p.tiles_per_slot, t0, t1, wsum);
         if (threadIdx.x == 0) {
             p.level2[item] = chunk;
             __threadfence();
             last = atomicAdd(p.arrivals, 1u) == gridDim.x - 1;
         }
         __syncthreads();
+        if (!last) return;
+        __threadfence();
     }
-    if (!last) return;
-    __threadfence();
-    double sumsq;
-    if (p.n_items <= 32) {  // one warp: item l in lane l, then the warp tree
-        if (threadIdx.x >= 32) return;
-        sumsq = warp_sum_fixed((int)threadIdx.x < p.n_items ? __ldcg(p.level2 + threadIdx.x) : 0.0);
+    // the last (or only) block: per-partition sums and flags in partition order
+    for (int i = threadIdx.x; i < p.n_slots; i += kDecideThreads) {
+        vec[i] = 0.0;
+        flag[i] = 0;
+    }
+    if (threadIdx.x == 0) any_overflow = 0;
+    __syncthreads();
+    if (p.mode == kDecideGlobal) {
+        for (int i = threadIdx.x; i < p.n_slots; i += kDecideThreads) {
+            vec[i] = p.stats_in[i];
+            if (p.stats_in[p.n_slots + i] != 0.0) {
+                flag[i] = 1;
+                any_overflow = 1;  // every writer stores the same value
+            }
+        }
     } else {
-        double acc = 0.0;
-        for (int t = threadIdx.x; t < p.n_items; t += kDecideThreads) acc = __dadd_rn(acc, __ldcg(p.level2 + t));
-        __syncthreads();  // wsum is reused
-        sumsq = block_sum_fixed(acc, wsum);
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int a = warp; a < p.n_active; a += kDecideThreads / 32) {
+            const double *c = p.level2 + (long long)a * p.chunks_per_slot;
+            const double sum = slot_sum_warp([c](int k) { return __ldcg(c + k); }, p.chunks_per_slot);
+            if (lane == 0) {
+                const int slot = p.slots[a];
+                vec[slot] = sum;
+                if (__ldcg(p.overflow + slot) != 0u) {
+                    flag[slot] = 1;
+                    any_overflow = 1;
+                }
+            }
+        }
     }
+    if (p.mode != kExportStats && (threadIdx.x == 32 || threadIdx.x == 64)) {
+        // bias corrections for t + 1 (the step counter if the step is not
+        // skipped): from the host's table when it holds that counter, else
+        // computed here in fp64
+        const int b = threadIdx.x == 64;
+        const long long tn = rec->step + 1;
+        const long long i = p.bc_t0 - tn;
+        if (i >= 0 && i < kBcTable) {
+            bias_corr[b] = b ? p.bc2_tab[i] : p.bc1_tab[i];
+        } else {
+            const double beta = b ? (double)p.beta2 : (double)p.beta1;
+            bias_corr[b] = __double2float_rn(__dsub_rn(1.0, pow(beta, (double)tn)));
+        }
+    }
+    __syncthreads();
+    if (p.mode == kExportStats) {
+        for (int i = threadIdx.x; i < p.n_slots; i += kDecideThreads) {
+            p.stats_out[i] = vec[i];
+            p.stats_out[p.n_slots + i] = flag[i] ? 1.0 : 0.0;
+        }
+        if (threadIdx.x == 0) *p.arrivals = 0u;
+        return;
+    }
+    double sumsq;
+    if (p.mode == kDecideLocal && p.n_active == 1)
+        sumsq = vec[p.slots[0]];  // the other entries are zeros: adding them is exact
+    else
+        sumsq = vector_sum_block(vec, p.n_slots, wsum);
     if (threadIdx.x != 0) return;
-    *p.arrivals = 0u;
-
-    sumsq = p.use_global ? p.global_sumsq : __dadd_rn(sumsq, p.remote_sumsq);
+    if (p.mode == kDecideLocal) {
+        *p.arrivals = 0u;
+        sumsq = __dadd_rn(sumsq, p.remote_sumsq);
+    }
     const double norm = sqrt(sumsq);
-    const int skip = (rec->overflow != 0u) || (p.remote_overflow != 0);
+    const int skip = any_overflow != 0 || (p.mode == kDecideLocal && p.remote_overflow != 0);
     float coef = 1.0f;
     if (p.clip > 0.0f) {
         const double c = __ddiv_rn((double)p.clip, __dadd_rn(norm, 1e-6));
@@ -522,9 +528,14 @@ __device__ __forceinline__ void adam1(const AdamScalars &c, float g, float &w, f
 // stage (empty mbarrier), write master/m/v/param into one of 2 output stages,
 // and one consumer thread stores them back with bulk copies.  Two such
 // pipelines (CTAs, 92 KB of shared memory each) run per SM.
-// Every mbarrier wait is bounded; a wait that gives up makes all consumers
-// leave together (the barrier vote), sets the error word, and the producer
-// drains the loads it issued before the CTA exits.
+// Every pipeline wait polls at most `spin_limit` times (the plan's setting); a
+// consumer wait that gives up makes all consumers leave together (the barrier
+// vote, before any store of that tile), a producer wait that gives up stops the
+// loads, and either sets the error word.  Whatever happens, the producer then
+// waits (with its own fixed bound) for every load it issued that no consumer
+// is known to have received, so no bulk copy into this CTA's shared memory is
+// in flight when the CTA exits; the consumers' store thread waits for its
+// stores.
 constexpr int kAdamTile = 1024;
 constexpr int kAdamInStages = 4;
 constexpr int kAdamOutStages = 2;
@@ -534,7 +545,6 @@ constexpr int kAdamTmaThreads = kAdamConsumers + 32;
 constexpr size_t kAdamInStageBytes = 4 * kAdamTile * sizeof(float);
 constexpr size_t kAdamOutStageBytes = 3 * kAdamTile * sizeof(float) + kAdamTile * 2;
 constexpr size_t kAdamTmaSmem = kAdamInStages * kAdamInStageBytes + kAdamOutStages * kAdamOutStageBytes;
-constexpr long long kPipePolls = 1ll << 22;
 constexpr int kAdamCtasPerSm = 2;
 static_assert(kAdamTile == kAdamConsumers * 4, "4 elements per consumer thread");
 
@@ -545,6 +555,7 @@ struct AdamTmaParams {
     const StepRecord *rec;
     int *error;
     long long len;  // multiple of 8
+    long long spin_limit;
     float lr, beta1, beta2, omb1, omb2, eps, wd, decay;
     int adamw;
 };
@@ -586,7 +597,7 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
         for (; k < count; ++k) {
             const int s = (int)(k % kAdamInStages);
             if (k >= kAdamInStages &&
-                !mbar_wait_bounded(&empty[s], (uint32_t)(((k / kAdamInStages) - 1) & 1), kPipePolls)) {
+                !mbar_wait_bounded(&empty[s], (uint32_t)(((k / kAdamInStages) - 1) & 1), p.spin_limit)) {
                 ok = false;
                 break;
             }
@@ -600,13 +611,16 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
             bulk_load(dst + 2 * kAdamTile * sizeof(float), p.m + e0, bytes, &full[s]);
             bulk_load(dst + 3 * kAdamTile * sizeof(float), p.v + e0, bytes, &full[s]);
         }
-        if (!ok) {
-            atomicExch(p.error, 1);
-            const long long first = k > kAdamInStages ? k - kAdamInStages : 0;
-            for (long long kk = first; kk < k; ++kk)
-                mbar_wait_bounded(&full[kk % kAdamInStages], (uint32_t)((kk / kAdamInStages) & 1),
-                                  kDrainPolls);
-        }
+        if (!ok) atomicExch(p.error, 1);
+        // Drain.  k tiles were issued.  Every tile kk < k - kAdamInStages has
+        // landed: issuing tile kk + kAdamInStages into the same stage needed
+        // the consumers to release tile kk first.  Tile kk >= k - kAdamInStages
+        // is the last load of its stage, so waiting for its phase is
+        // unambiguous.  In a normal run the consumers wait for these same
+        // loads; after a consumer timeout nobody else would.
+        const long long first = k > kAdamInStages ? k - kAdamInStages : 0;
+        for (long long kk = first; kk < k; ++kk)
+            mbar_wait_bounded(&full[kk % kAdamInStages], (uint32_t)((kk / kAdamInStages) & 1), kDrainPolls);
         return;
     }
 
@@ -631,7 +645,7 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
         const int so = (int)(k % kAdamOutStages);
         const long long e0 = (blockIdx.x + k * gridDim.x) * (long long)kAdamTile;
         const int n = (int)(p.len - e0 < kAdamTile ? p.len - e0 : kAdamTile);
-        const bool got = mbar_wait_bounded(&full[s], (uint32_t)((k / kAdamInStages) & 1), kPipePolls);
+        const bool got = mbar_wait_bounded(&full[s], (uint32_t)((k / kAdamInStages) & 1), p.spin_limit);
         const bool mine = got && ct * 4 < n;
         float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f), w4 = g4, m4 = g4, v4 = g4;
         if (mine) {
@@ -895,46 +909,49 @@ cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp, 
                                                              partials, overflow, stream);
 }
 
-cudaError_t launch_decide(const double *partials, double *level2, unsigned *arrivals, int64_t bc_t0,
-                          const float *bc1_tab, const float *bc2_tab, int64_t tiles_per_slot,
-                          const uint64_t *active_mask, int n_slots, double remote_sumsq, int remote_overflow,
-                          int use_global, double global_sumsq, float clip, float loss_scale,
-                          int growth_interval, float beta1, float beta2, StepRecord *rec,
-                          cudaStream_t stream) {
+cudaError_t launch_norm(const NormLaunch &a, cudaStream_t stream) {
     DecideParams p;
-    p.partials = partials;
-    p.level2 = level2;
-    p.arrivals = arrivals;
-    p.tiles_per_slot = tiles_per_slot;
-    p.chunks_per_slot = (int)((tiles_per_slot + kPartialChunk - 1) / kPartialChunk);
+    p.partials = a.partials;
+    p.level2 = a.level2;
+    p.overflow = a.overflow;
+    p.arrivals = a.arrivals;
+    p.stats_out = a.stats_out;
+    p.stats_in = a.stats_in;
+    p.tiles_per_slot = a.tiles_per_slot;
+    p.chunks_per_slot = (int)((a.tiles_per_slot + kPartialChunk - 1) / kPartialChunk);
     if (p.chunks_per_slot < 1) p.chunks_per_slot = 1;
+    if (a.n_slots < 1 || a.n_slots > kNormMaxSlots) return cudaErrorInvalidValue;
+    p.n_slots = a.n_slots;
+    p.mode = a.mode;
     int active = 0;
-    for (int r = 0; r < n_slots; ++r)
-        if ((active_mask[r >> 6] >> (r & 63)) & 1u) p.slots[active++] = (short)r;
-    if (active == 0) return cudaErrorInvalidValue;
-    p.n_items = active * p.chunks_per_slot;
-    p.remote_sumsq = remote_sumsq;
-    p.remote_overflow = remote_overflow;
-    p.use_global = use_global;
-    p.global_sumsq = global_sumsq;
-    p.clip = clip;
-    p.loss_scale = loss_scale;
-    p.beta1 = beta1;
-    p.beta2 = beta2;
-    p.growth_interval = growth_interval;
-    p.rec = rec;
-    p.bc_t0 = bc_t0;
-    for (int i = 0; i < kBcTable; ++i) {
-        p.bc1_tab[i] = bc1_tab[i];
-        p.bc2_tab[i] = bc2_tab[i];
+    if (a.mode != kDecideGlobal) {
+        for (int r = 0; r < a.n_slots; ++r)
+            if ((a.active_mask[r >> 6] >> (r & 63)) & 1u) p.slots[active++] = (short)r;
+        if (active == 0) return cudaErrorInvalidValue;
     }
-    return launch_pdl(norm_decide, dim3((unsigned)p.n_items), dim3(kDecideThreads), 0, stream, p);
+    p.n_active = active;
+    p.remote_sumsq = a.remote_sumsq;
+    p.remote_overflow = a.remote_overflow;
+    p.clip = a.clip;
+    p.loss_scale = a.loss_scale;
+    p.beta1 = a.beta1;
+    p.beta2 = a.beta2;
+    p.growth_interval = a.growth_interval;
+    p.rec = a.rec;
+    p.bc_t0 = a.bc_t0;
+    for (int i = 0; i < kBcTable; ++i) {
+        p.bc1_tab[i] = a.bc1_tab ? a.bc1_tab[i] : 0.0f;
+        p.bc2_tab[i] = a.bc2_tab ? a.bc2_tab[i] : 0.0f;
+    }
+    const long long blocks = a.mode == kDecideGlobal ? 1 : (long long)active * p.chunks_per_slot;
+    if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+    return launch_pdl(norm_decide, dim3((unsigned)blocks), dim3(kDecideThreads), 0, stream, p);
 }
 
 cudaError_t launch_adam(const float *g, float *master, float *m, float *v, void *param, int lp,
-                        int64_t len, const StepRecord *rec, int *error, float lr, float beta1,
-                        float beta2, float omb1, float omb2, float eps, float wd, float decay,
-                        int adamw, cudaStream_t stream) {
+                        int64_t len, const StepRecord *rec, int *error, int64_t spin_limit, float lr,
+                        float beta1, float beta2, float omb1, float omb2, float eps, float wd,
+                        float decay, int adamw, cudaStream_t stream) {
     AdamTmaParams q;
     q.g = g;
     q.master = master;
@@ -944,6 +961,7 @@ cudaError_t launch_adam(const float *g, float *master, float *m, float *v, void 
     q.rec = rec;
     q.error = error;
     q.len = len;
+    q.spin_limit = spin_limit;
     q.lr = lr;
     q.beta1 = beta1;
     q.beta2 = beta2;

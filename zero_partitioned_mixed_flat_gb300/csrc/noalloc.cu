@@ -12,6 +12,7 @@
 // The array lives on every GPU that loads the library, until the process
 // exits.  Every call shares it and it keeps the last call's contents, so calls
 // whose device work overlaps (two streams, two host threads) race on it.
+#include "norm_tree.cuh"
 #include "zero.h"
 #include "zero_internal.h"
 
@@ -25,37 +26,46 @@
 namespace {
 
 constexpr int64_t kMaxTiles = ZERO_NOALLOC_MAX_ELEMS / zk::kTile;
+constexpr int64_t kMaxChunks = (kMaxTiles + zk::kPartialChunk - 1) / zk::kPartialChunk;
 constexpr size_t kScratchBytes = size_t(kMaxTiles) * sizeof(double) + 256;
 static_assert(ZERO_NOALLOC_MAX_ELEMS % zk::kTile == 0, "maximum must be whole norm tiles");
+static_assert(kScratchBytes == size_t(ZERO_NOALLOC_SCRATCH_BYTES),
+              "the header's scratch size must match the array");
+static_assert(kMaxChunks * sizeof(double) + sizeof(unsigned) <= 256, "tail holds chunk sums and the flag");
 
-// [0, kMaxTiles*8): per-tile fp64 partial sums; then one 32-bit overflow word
+// [0, kMaxTiles*8): per-tile fp64 partial sums; then, in the 256-byte tail, one
+// 32-bit overflow word
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void *g_scratch_addr[64];  // device address of g_noalloc_scratch, per device
+constexpr int kMaxDevices = 64;
+void *g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
 
 zero_status noalloc_fail(zero_status code, const char *msg) {
     zk::set_last_error(msg);  // reported by zero_last_error()
     return code;
 }
 
-constexpr int kFinalThreads = 1024;
-
-// Sum of the tile partials in a fixed order (strided per thread, xor tree,
-// warps in order) and the overflow word -> the caller's outputs.
-__global__ void __launch_bounds__(kFinalThreads)
+// The partition's sum of squares with the plan path's tree (norm_tree.cuh:
+// chunk sums, then one warp over the chunks), so *sumsq_out equals what
+// zero_partition_stats exports for the same partition, bit for bit; and the
+// overflow word.  One block of kNormThreads.
+__global__ void __launch_bounds__(zk::kNormThreads)
 noalloc_finalize(const double *partials, long long n_tiles, const unsigned *overflow,
                  double *sumsq_out, int *overflow_out) {
-    __shared__ double wsum[kFinalThreads / 32];
-    double acc = 0.0;
-    for (long long t = threadIdx.x; t < n_tiles; t += kFinalThreads) acc = __dadd_rn(acc, partials[t]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
-    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = acc;
+    __shared__ double wsum[zk::kNormThreads / 32];
+    __shared__ double chunks[kMaxChunks];
+    const int n_chunks = n_tiles > 0 ? (int)((n_tiles + zk::kPartialChunk - 1) / zk::kPartialChunk) : 1;
+    for (int c = 0; c < n_chunks; ++c) {
+        const long long t0 = (long long)c * zk::kPartialChunk;
+        const long long t1 = t0 + zk::kPartialChunk < n_tiles ? t0 + zk::kPartialChunk : n_tiles;
+        const double s = zk::chunk_sum(partials, t0, t1, wsum);
+        if (threadIdx.x == 0) chunks[c] = s;
+    }
     __syncthreads();
+    if (threadIdx.x >= 32) return;
+    const double s = zk::slot_sum_warp([](int k) { return chunks[k]; }, n_chunks);
     if (threadIdx.x == 0) {
-        double s = 0.0;
-        for (int w = 0; w < kFinalThreads / 32; ++w) s = __dadd_rn(s, wsum[w]);
         *sumsq_out = s;
         *overflow_out = *overflow ? 1 : 0;
     }
@@ -90,8 +100,13 @@ extern "C" zero_status zero_reduce_partition_noalloc(int32_t n_ranks, zero_lp lp
     // set-up, once per device, with that device current: the host-side name of
     // the array is only a stand-in, the kernels need its device address
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
         return noalloc_fail(ZERO_ECUDA, "cudaGetDevice failed");
+    }
+    if (dev < 0 || dev >= kMaxDevices)
+        return noalloc_fail(ZERO_EINVAL, "device ordinal is 64 or more: the allocation-free reduce keeps "
+                                         "its scratch address for devices 0-63 only");
     void *base = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -121,7 +136,7 @@ extern "C" zero_status zero_reduce_partition_noalloc(int32_t n_ranks, zero_lp lp
         if (e != cudaSuccess) return noalloc_fail(ZERO_ECUDA, cudaGetErrorString(e));
     }
     const long long n_tiles = (len + zk::kTile - 1) / zk::kTile;
-    noalloc_finalize<<<1, kFinalThreads, 0, s>>>(partials, n_tiles, overflow, sumsq_out, overflow_out);
+    noalloc_finalize<<<1, zk::kNormThreads, 0, s>>>(partials, n_tiles, overflow, sumsq_out, overflow_out);
     e = cudaGetLastError();
     if (e != cudaSuccess) return noalloc_fail(ZERO_ECUDA, cudaGetErrorString(e));
     return ZERO_OK;

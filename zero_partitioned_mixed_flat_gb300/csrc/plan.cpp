@@ -39,13 +39,15 @@ int64_t round_up(int64_t x, int64_t q) { return q == 0 ? x : ((x + q - 1) / q) *
 
 enum Phase { kIdle = 0, kReducing = 1, kDecided = 2 };
 
-constexpr int64_t kDefaultSpinLimit = int64_t(1) << 21;
+constexpr int64_t kDefaultSpinLimit = int64_t(1) << 22;
 
 }  // namespace
 
 namespace zk {
 void set_last_error(const char *msg) { g_last_error = msg ? msg : ""; }
 }  // namespace zk
+
+static_assert(zk::kTile == ZERO_NORM_TILE, "the header's norm tile is the kernels' tile");
 
 struct zero_plan {
     // layout
@@ -63,8 +65,16 @@ struct zero_plan {
     // device scratch (allocated on first device call)
     int device = -1;
     double *d_partials = nullptr;
-    double *d_level2 = nullptr;  // first-level sums of the partials
+    double *d_level2 = nullptr;   // chunk sums of the partials (decision)
+    double *d_level2x = nullptr;  // the same for the statistics export
+    unsigned *d_overflow = nullptr;  // one overflow word per partition slot
     zk::StepRecord *d_rec = nullptr;
+    cudaStream_t io = nullptr;  // private non-blocking stream for record reads/writes
+    // completion of the plan's own device work: one event per stream used
+    // since the last synchronising call
+    std::vector<std::pair<cudaStream_t, cudaEvent_t>> pending;
+    std::vector<cudaEvent_t> spare_events;
+    bool captured = false;  // some call was enqueued on a capturing stream
     // step state (host)
     Phase phase = kIdle;
     uint64_t active[ZERO_MAX_RANKS / 64] = {0};
@@ -76,8 +86,7 @@ struct zero_plan {
     // the last value read back or set, plus one per decision launched since
     int64_t t_hint = 0;
     bool use_global = false;  // zero_step_set_global_stats was called this step
-    double global_sumsq = 0.0;
-    int32_t global_overflow = 0;
+    const double *global_stats = nullptr;  // device address of the caller's vector
 
     int32_t n_units() const { return int32_t(unit_pad.size()); }
     int64_t shard_len(int32_t u) const { return stage == 0 ? unit_pad[u] : unit_pad[u] / n_ranks; }
@@ -129,6 +138,19 @@ zero_status build_layout(zero_plan *p) {
     return ZERO_OK;
 }
 
+void free_scratch(zero_plan *p) {
+    cudaFree(p->d_partials);
+    cudaFree(p->d_level2);
+    cudaFree(p->d_level2x);
+    cudaFree(p->d_overflow);
+    cudaFree(p->d_rec);
+    p->d_partials = p->d_level2 = p->d_level2x = nullptr;
+    p->d_overflow = nullptr;
+    p->d_rec = nullptr;
+    if (p->io) cudaStreamDestroy(p->io);
+    p->io = nullptr;
+}
+
 zero_status ensure_device(zero_plan *p) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -140,34 +162,86 @@ zero_status ensure_device(zero_plan *p) {
         return ZERO_OK;
     }
     const size_t n_part = size_t(p->slots) * size_t(p->tiles_per_part > 0 ? p->tiles_per_part : 1);
-    e = cudaMalloc(reinterpret_cast<void **>(&p->d_partials), n_part * sizeof(double));
-    if (e != cudaSuccess) {
-        p->d_partials = nullptr;
-        cudaGetLastError();
-        return fail(ZERO_ENOMEM, "cudaMalloc of %zu partial sums failed", n_part);
-    }
     const size_t n_level2 = size_t(p->slots) *
                             size_t(std::max<int64_t>(1, (p->tiles_per_part + zk::kPartialChunk - 1) / zk::kPartialChunk));
-    e = cudaMalloc(reinterpret_cast<void **>(&p->d_rec), sizeof(zk::StepRecord));
-    cudaError_t e2 = cudaMalloc(reinterpret_cast<void **>(&p->d_level2), n_level2 * sizeof(double));
-    if (e != cudaSuccess || e2 != cudaSuccess) {
-        cudaFree(p->d_partials);
-        if (e == cudaSuccess) cudaFree(p->d_rec);
-        if (e2 == cudaSuccess) cudaFree(p->d_level2);
-        p->d_partials = nullptr;
-        p->d_rec = nullptr;
-        p->d_level2 = nullptr;
+    bool ok = cudaMalloc(reinterpret_cast<void **>(&p->d_partials), n_part * sizeof(double)) == cudaSuccess;
+    ok = ok && cudaMalloc(reinterpret_cast<void **>(&p->d_level2), n_level2 * sizeof(double)) == cudaSuccess;
+    ok = ok && cudaMalloc(reinterpret_cast<void **>(&p->d_level2x), n_level2 * sizeof(double)) == cudaSuccess;
+    ok = ok && cudaMalloc(reinterpret_cast<void **>(&p->d_overflow), size_t(p->slots) * sizeof(unsigned)) ==
+                   cudaSuccess;
+    ok = ok && cudaMalloc(reinterpret_cast<void **>(&p->d_rec), sizeof(zk::StepRecord)) == cudaSuccess;
+    if (!ok) {
         cudaGetLastError();
-        return fail(ZERO_ENOMEM, "cudaMalloc of the step record or the norm scratch failed");
+        free_scratch(p);
+        return fail(ZERO_ENOMEM, "cudaMalloc of the plan scratch (%zu partial sums) failed", n_part);
+    }
+    e = cudaStreamCreateWithFlags(&p->io, cudaStreamNonBlocking);
+    if (e != cudaSuccess) {
+        p->io = nullptr;
+        free_scratch(p);
+        return cuda_fail(e, "cudaStreamCreateWithFlags");
     }
     zk::StepRecord init;
     std::memset(&init, 0, sizeof init);
     init.coef = 1.0f;
-    e = cudaMemcpy(p->d_rec, &init, sizeof init, cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step record)");
-    e = cudaMemset(p->d_partials, 0, n_part * sizeof(double));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(partials)");
+    e = cudaMemcpyAsync(p->d_rec, &init, sizeof init, cudaMemcpyHostToDevice, p->io);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->d_partials, 0, n_part * sizeof(double), p->io);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->d_overflow, 0, size_t(p->slots) * sizeof(unsigned), p->io);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->io);
+    if (e != cudaSuccess) {
+        free_scratch(p);
+        return cuda_fail(e, "initialising the plan scratch");
+    }
     p->device = dev;
+    return ZERO_OK;
+}
+
+// Remember that the plan's device work was enqueued on stream s (called after
+// a call's launches succeeded).  A capturing stream records nothing: the graph
+// may be replayed anywhere, so the plan then waits for the whole device.
+zero_status note_work(zero_plan *p, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        cs = cudaStreamCaptureStatusActive;
+    }
+    if (cs != cudaStreamCaptureStatusNone) {
+        p->captured = true;
+        return ZERO_OK;
+    }
+    cudaEvent_t ev = nullptr;
+    for (auto &pe : p->pending)
+        if (pe.first == s) ev = pe.second;
+    if (!ev) {
+        if (!p->spare_events.empty()) {
+            ev = p->spare_events.back();
+            p->spare_events.pop_back();
+        } else {
+            cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreateWithFlags");
+        }
+        p->pending.emplace_back(s, ev);
+    }
+    cudaError_t e = cudaEventRecord(ev, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    return ZERO_OK;
+}
+
+// Wait for the plan's own device work: the events of the streams it used since
+// the last wait (or the whole device if a call was captured into a graph).
+zero_status wait_own_work(zero_plan *p) {
+    cudaError_t err = cudaSuccess;
+    if (p->captured) {
+        err = cudaDeviceSynchronize();
+    } else {
+        for (auto &pe : p->pending) {
+            cudaError_t e = cudaEventSynchronize(pe.second);
+            if (err == cudaSuccess) err = e;
+        }
+    }
+    for (auto &pe : p->pending) p->spare_events.push_back(pe.second);
+    p->pending.clear();
+    if (err != cudaSuccess) return cuda_fail(err, p->captured ? "cudaDeviceSynchronize" : "cudaEventSynchronize");
     return ZERO_OK;
 }
 
@@ -363,15 +437,17 @@ zero_status zero_plan_set_state(zero_plan *p, int64_t step, int32_t good_steps) 
     if (!p || step < 0 || good_steps < 0) return fail(ZERO_EINVAL, "bad plan state");
     zero_status st = ensure_device(p);
     if (st != ZERO_OK) return st;
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    st = wait_own_work(p);
+    if (st != ZERO_OK) return st;
     zk::StepRecord rec;
-    e = cudaMemcpy(&rec, p->d_rec, sizeof rec, cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step record)");
+    cudaError_t e = cudaMemcpyAsync(&rec, p->d_rec, sizeof rec, cudaMemcpyDeviceToHost, p->io);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->io);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the step record");
     rec.step = step;
     rec.good_steps = good_steps;
-    e = cudaMemcpy(p->d_rec, &rec, sizeof rec, cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step record)");
+    e = cudaMemcpyAsync(p->d_rec, &rec, sizeof rec, cudaMemcpyHostToDevice, p->io);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->io);
+    if (e != cudaSuccess) return cuda_fail(e, "writing the step record");
     p->t_hint = step;
     return ZERO_OK;
 }
@@ -409,7 +485,8 @@ zero_status begin_reduce(zero_plan *p, int32_t rank, const void *const *grad_sli
         // overflow (a partition reduced only in part then adds only that part)
         std::memset(p->active, 0, sizeof p->active);
         p->use_global = false;
-        cudaError_t e = cudaMemsetAsync(&p->d_rec->overflow, 0, sizeof(unsigned), s);
+        p->global_stats = nullptr;
+        cudaError_t e = cudaMemsetAsync(p->d_overflow, 0, size_t(p->slots) * sizeof(unsigned), s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(overflow)");
         if (p->tiles_per_part > 0) {
             e = cudaMemsetAsync(p->d_partials, 0, size_t(p->slots) * size_t(p->tiles_per_part) * sizeof(double), s);
@@ -436,7 +513,7 @@ zero_status reduce_units(zero_plan *p, int32_t slot, int32_t first, int32_t coun
     auto flush = [&]() -> zero_status {
         if (segs.empty()) return ZERO_OK;
         cudaError_t e = zk::launch_reduce(src, p->n_ranks, p->lp, p->reduce_lp_accum, segs.data(),
-                                          int(segs.size()), inv, grad_out, partials, &p->d_rec->overflow, s);
+                                          int(segs.size()), inv, grad_out, partials, p->d_overflow + slot, s);
         segs.clear();
         launch_elems = 0;
         if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
@@ -474,7 +551,9 @@ zero_status zero_reduce_partition(zero_plan *p, int32_t rank, const void *const 
     if (st != ZERO_OK) return st;
     const int32_t slot = p->stage == 0 ? 0 : rank;
     p->active[slot >> 6] |= uint64_t(1) << (slot & 63);
-    return reduce_units(p, slot, 0, p->n_units(), src.data(), grad_out, loss_scale, bucket_elems, s);
+    st = reduce_units(p, slot, 0, p->n_units(), src.data(), grad_out, loss_scale, bucket_elems, s);
+    if (st != ZERO_OK) return st;
+    return note_work(p, s);
 }
 
 zero_status zero_reduce_units(zero_plan *p, int32_t rank, int32_t first_unit, int32_t n_units,
@@ -491,43 +570,51 @@ zero_status zero_reduce_units(zero_plan *p, int32_t rank, int32_t first_unit, in
     if (st != ZERO_OK) return st;
     const int32_t slot = rank;
     p->active[slot >> 6] |= uint64_t(1) << (slot & 63);
-    return reduce_units(p, slot, first_unit, n_units, src.data(), grad_out, loss_scale, 0, s);
+    st = reduce_units(p, slot, first_unit, n_units, src.data(), grad_out, loss_scale, 0, s);
+    if (st != ZERO_OK) return st;
+    return note_work(p, s);
 }
 
-zero_status zero_partition_stats(zero_plan *p, double *sumsq, int32_t *overflow, void *stream) {
+zero_status zero_partition_stats(zero_plan *p, double *stats, void *stream) {
     if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (!stats) return fail(ZERO_EINVAL, "stats is NULL");
+    if (reinterpret_cast<uintptr_t>(stats) & 7u) return fail(ZERO_EALIGN, "stats is not 8-byte aligned");
     if (p->phase != kReducing) return fail(ZERO_ESTATE, "no partition reduced in the current step");
     zero_status st = ensure_device(p);
     if (st != ZERO_OK) return st;
+    const void *dst = nullptr;
+    st = readable_by_device(stats, p->device, "stats", 0, &dst);
+    if (st != ZERO_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    // sum the partials of the active slots on the host, in slot then tile order
-    double acc = 0.0;
-    std::vector<double> host(size_t(p->tiles_per_part));
-    for (int32_t r = 0; r < p->slots; ++r) {
-        if (!((p->active[r >> 6] >> (r & 63)) & 1u)) continue;
-        e = cudaMemcpy(host.data(), p->d_partials + int64_t(r) * p->tiles_per_part,
-                       host.size() * sizeof(double), cudaMemcpyDeviceToHost);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(partials)");
-        for (double x : host) acc += x;
-    }
-    unsigned of = 0;
-    e = cudaMemcpy(&of, &p->d_rec->overflow, sizeof of, cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(overflow)");
-    if (sumsq) *sumsq = acc;
-    if (overflow) *overflow = of ? 1 : 0;
-    return ZERO_OK;
+    zk::NormLaunch a = {};
+    a.mode = zk::kExportStats;
+    a.partials = p->d_partials;
+    a.level2 = p->d_level2x;
+    a.arrivals = &p->d_rec->arrivals_x;
+    a.overflow = p->d_overflow;
+    a.stats_out = static_cast<double *>(const_cast<void *>(dst));
+    a.tiles_per_slot = p->tiles_per_part;
+    a.active_mask = p->active;
+    a.n_slots = p->n_ranks;
+    a.rec = p->d_rec;
+    cudaError_t e = zk::launch_norm(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "statistics kernel launch");
+    return note_work(p, s);
 }
 
-zero_status zero_step_set_global_stats(zero_plan *p, double global_sumsq, int32_t global_overflow) {
+zero_status zero_step_set_global_stats(zero_plan *p, const double *stats) {
     if (!p) return fail(ZERO_EINVAL, "plan is NULL");
-    if (global_sumsq < 0.0) return fail(ZERO_EINVAL, "global_sumsq must be >= 0");
+    if (!stats) return fail(ZERO_EINVAL, "stats is NULL");
+    if (reinterpret_cast<uintptr_t>(stats) & 7u) return fail(ZERO_EALIGN, "stats is not 8-byte aligned");
     if (p->phase != kReducing)
         return fail(ZERO_ESTATE, "global stats belong between a step's reduces and its first Adam call");
+    zero_status st = ensure_device(p);
+    if (st != ZERO_OK) return st;
+    const void *src = nullptr;
+    st = readable_by_device(stats, p->device, "stats", 0, &src);
+    if (st != ZERO_OK) return st;
     p->use_global = true;
-    p->global_sumsq = global_sumsq;
-    p->global_overflow = global_overflow ? 1 : 0;
+    p->global_stats = static_cast<const double *>(src);
     return ZERO_OK;
 }
 
@@ -558,7 +645,6 @@ zero_status adam_impl(zero_plan *p, int32_t rank, int64_t begin, int64_t len, co
         bool any = false;
         for (uint64_t w : p->active) any = any || w != 0;
         if (!any) return fail(ZERO_ESTATE, "no partition was reduced in the current step");
-        const int r_of = p->use_global ? (p->global_overflow ? 1 : 0) : (remote_overflow ? 1 : 0);
         // bias corrections, computed as the oracle does, for the counters
         // t_hint + 1 down to t_hint + 2 - kBcTable (t_hint + 1 unless earlier
         // steps were skipped since the counter was last read back)
@@ -569,16 +655,33 @@ zero_status adam_impl(zero_plan *p, int32_t rank, int64_t begin, int64_t len, co
             bc1[i] = t > 0 ? float(1.0 - std::pow(double(beta1), double(t))) : 0.0f;
             bc2[i] = t > 0 ? float(1.0 - std::pow(double(beta2), double(t))) : 0.0f;
         }
-        cudaError_t e = zk::launch_decide(p->d_partials, p->d_level2, &p->d_rec->arrivals, bc_t0, bc1, bc2,
-                                          p->tiles_per_part, p->active, p->slots,
-                                          remote_sumsq, r_of, p->use_global ? 1 : 0,
-                                          p->global_sumsq, clip, loss_scale, p->growth_interval,
-                                          beta1, beta2, p->d_rec, s);
+        zk::NormLaunch a = {};
+        a.mode = p->use_global ? zk::kDecideGlobal : zk::kDecideLocal;
+        a.partials = p->d_partials;
+        a.level2 = p->d_level2;
+        a.arrivals = &p->d_rec->arrivals;
+        a.overflow = p->d_overflow;
+        a.stats_in = p->global_stats;
+        a.tiles_per_slot = p->tiles_per_part;
+        a.active_mask = p->active;
+        a.n_slots = p->n_ranks;
+        a.remote_sumsq = remote_sumsq;
+        a.remote_overflow = remote_overflow ? 1 : 0;
+        a.clip = clip;
+        a.loss_scale = loss_scale;
+        a.beta1 = beta1;
+        a.beta2 = beta2;
+        a.growth_interval = p->growth_interval;
+        a.bc_t0 = bc_t0;
+        a.bc1_tab = bc1;
+        a.bc2_tab = bc2;
+        a.rec = p->d_rec;
+        cudaError_t e = zk::launch_norm(a, s);
         if (e != cudaSuccess) return cuda_fail(e, "decide kernel launch");
         p->phase = kDecided;
         p->t_hint += 1;
     }
-    if (len == 0) return ZERO_OK;
+    if (len == 0) return note_work(p, s);
     const float omb1 = 1.0f - beta1;
     const float omb2 = 1.0f - beta2;
     const float decay = float(1.0 - double(lr) * double(wd));
@@ -588,10 +691,10 @@ zero_status adam_impl(zero_plan *p, int32_t rank, int64_t begin, int64_t len, co
         param = static_cast<uint16_t *>(param_out) + off;
     }
     cudaError_t e = zk::launch_adam(grad + begin, master + begin, m + begin, v + begin, param, p->lp, len,
-                                    p->d_rec, &p->d_rec->error, lr, beta1, beta2, omb1, omb2, eps, wd,
-                                    decay, adamw ? 1 : 0, s);
+                                    p->d_rec, &p->d_rec->error, p->spin_limit, lr, beta1, beta2, omb1, omb2,
+                                    eps, wd, decay, adamw ? 1 : 0, s);
     if (e != cudaSuccess) return cuda_fail(e, "adam kernel launch");
-    return ZERO_OK;
+    return note_work(p, s);
 }
 
 }  // namespace
@@ -627,20 +730,21 @@ zero_status zero_step_result(zero_plan *p, double *norm, int32_t *skipped, float
     if (!p) return fail(ZERO_EINVAL, "plan is NULL");
     zero_status st = ensure_device(p);
     if (st != ZERO_OK) return st;
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    st = wait_own_work(p);
+    if (st != ZERO_OK) return st;
     zk::StepRecord rec;
-    e = cudaMemcpy(&rec, p->d_rec, sizeof rec, cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step record)");
+    cudaError_t e = cudaMemcpyAsync(&rec, p->d_rec, sizeof rec, cudaMemcpyDeviceToHost, p->io);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->io);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the step record");
     p->t_hint = rec.step;
     if (norm) *norm = rec.norm;
     if (skipped) *skipped = rec.skip;
     if (new_loss_scale) *new_loss_scale = rec.loss_scale;
     if (step) *step = rec.step;
     if (rec.error) {
-        const int zero = 0;
-        e = cudaMemcpy(&p->d_rec->error, &zero, sizeof zero, cudaMemcpyHostToDevice);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+        e = cudaMemsetAsync(&p->d_rec->error, 0, sizeof(int), p->io);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(p->io);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
         return fail(ZERO_ETIMEOUT, "a bounded device wait gave up");
     }
     return ZERO_OK;
@@ -669,7 +773,7 @@ zero_status zero_gather_layer(zero_plan *p, int32_t unit, const void *const *sha
     cudaError_t e = zk::launch_gather(shards, p->n_ranks, off * 2, shard * 2, out, shard * 2, p->spin_limit,
                                       &p->d_rec->error, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
-    return ZERO_OK;
+    return note_work(p, static_cast<cudaStream_t>(stream));
 }
 
 zero_status zero_allgather_params(zero_plan *p, const void *const *partitions, void *out,
@@ -697,7 +801,7 @@ zero_status zero_allgather_params(zero_plan *p, const void *const *partitions, v
                                           &p->d_rec->error, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
     }
-    return ZERO_OK;
+    return note_work(p, static_cast<cudaStream_t>(stream));
 }
 
 zero_status zero_quantize_shard(zero_plan *p, const void *shard, int8_t *codes, float *scales,
@@ -714,7 +818,7 @@ zero_status zero_quantize_shard(zero_plan *p, const void *shard, int8_t *codes, 
     cudaError_t e = zk::launch_quantize(shard, p->lp, p->quant_format == ZERO_QUANT_FP8_E4M3, p->part, codes, scales,
                                         static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "quantize kernel launch");
-    return ZERO_OK;
+    return note_work(p, static_cast<cudaStream_t>(stream));
 }
 
 zero_status zero_gather_layer_quantized(zero_plan *p, int32_t unit, const int8_t *const *codes,
@@ -740,7 +844,7 @@ zero_status zero_gather_layer_quantized(zero_plan *p, int32_t unit, const int8_t
                                               p->quant_format == ZERO_QUANT_FP8_E4M3, off, shard, out,
                                               static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "dequantizing gather kernel launch");
-    return ZERO_OK;
+    return note_work(p, static_cast<cudaStream_t>(stream));
 }
 
 zero_status zero_memory_report(int64_t psi, int32_t n_ranks, int32_t align, double formula_bytes[4],
@@ -781,10 +885,10 @@ void zero_plan_destroy(zero_plan *p) {
         int cur = 0;
         cudaGetDevice(&cur);
         cudaSetDevice(p->device);
-        cudaDeviceSynchronize();
-        cudaFree(p->d_partials);
-        cudaFree(p->d_level2);
-        cudaFree(p->d_rec);
+        wait_own_work(p);  // the plan's kernels may still use its scratch
+        free_scratch(p);
+        for (cudaEvent_t ev : p->spare_events) cudaEventDestroy(ev);
+        cudaGetLastError();
         cudaSetDevice(cur);
     }
     delete p;

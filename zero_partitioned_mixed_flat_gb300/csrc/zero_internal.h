@@ -20,18 +20,19 @@ constexpr int64_t kPartialChunk = 4096;
 // Per-plan device record of the step decision and the optimizer step state.
 struct StepRecord {
     double norm;          // global gradient norm of the decided step
-    double sumsq;         // local + remote sum of squares
+    double sumsq;         // the global sum of squares it is the root of
     float coef;           // clip coefficient (1 when not clipping)
     float loss_scale;     // S for the next step
     float bc1, bc2;       // 1 - beta1^t, 1 - beta2^t
     long long step;       // Adam step counter t
     int skip;             // 1: overflow, the update is skipped
     int good_steps;       // consecutive non-skipped steps since the last growth
-    unsigned overflow;    // set by the reduce kernel when a sum is not finite
     int error;            // set when a bounded device wait gives up
-    unsigned arrivals;    // blocks of the norm kernel done (0 between launches)
+    unsigned arrivals;    // blocks of the decision kernel done (0 between launches)
+    unsigned arrivals_x;  // the same for the statistics export
     int pad_;
 };
+static_assert(sizeof(StepRecord) == 64, "one 64-byte record");
 
 int sm_count();
 
@@ -58,21 +59,41 @@ cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp,
 // rounded to float).  A counter outside the table is computed on the device.
 constexpr int kBcTable = 8;
 
-// level2: scratch for n_slots * ceil(tiles_per_slot / kPartialChunk) doubles
-cudaError_t launch_decide(const double *partials, double *level2, unsigned *arrivals,
-                          int64_t bc_t0, const float *bc1_tab, const float *bc2_tab,
-                          int64_t tiles_per_slot,
-                          const uint64_t *active_mask, int n_slots,
-                          double remote_sumsq, int remote_overflow,
-                          int use_global, double global_sumsq, float clip,
-                          float loss_scale, int growth_interval, float beta1,
-                          float beta2, StepRecord *rec, cudaStream_t stream);
+// What a launch of the norm kernel does with the step's partials.
+enum NormMode {
+    kDecideLocal = 0,   // the step's partitions (+ remote terms) -> the decision
+    kExportStats = 1,   // the step's partitions -> per-partition stats vector
+    kDecideGlobal = 2,  // an all-reduced stats vector -> the decision
+};
+
+struct NormLaunch {
+    int mode;
+    const double *partials;     // n_slots x tiles_per_slot (local, export)
+    double *level2;             // active x chunks doubles of scratch (local, export)
+    unsigned *arrivals;         // 0 between launches (local, export)
+    const unsigned *overflow;   // per slot (local, export)
+    double *stats_out;          // export: 2 * n_slots doubles
+    const double *stats_in;     // global: 2 * n_slots doubles
+    int64_t tiles_per_slot;
+    const uint64_t *active_mask;
+    int n_slots;                // N (the stats vector has 2N entries)
+    double remote_sumsq;        // local mode only
+    int remote_overflow;        // local mode only
+    float clip, loss_scale, beta1, beta2;
+    int growth_interval;
+    int64_t bc_t0;
+    const float *bc1_tab, *bc2_tab;
+    StepRecord *rec;
+};
+
+cudaError_t launch_norm(const NormLaunch &a, cudaStream_t stream);
 
 cudaError_t launch_adam(const float *g, float *master, float *m, float *v,
                         void *param, int lp, int64_t len,
-                        const StepRecord *rec, int *error, float lr, float beta1,
-                        float beta2, float omb1, float omb2, float eps,
-                        float wd, float decay, int adamw, cudaStream_t stream);
+                        const StepRecord *rec, int *error, int64_t spin_limit,
+                        float lr, float beta1, float beta2, float omb1, float omb2,
+                        float eps, float wd, float decay, int adamw,
+                        cudaStream_t stream);
 
 // out + j * dst_stride_bytes + [0, shard_bytes) <- shards[j] + src_offset_bytes + [0, shard_bytes)
 cudaError_t launch_gather(const void *const *shards, int n, int64_t src_offset_bytes,

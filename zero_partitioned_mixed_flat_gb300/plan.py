@@ -62,11 +62,13 @@ class ZeroPlan:
         A.zero_reduce_units(self.handle, rank, first_unit, n_units, grad_slices, grad_out, loss_scale,
                             stream)
 
-    def stats(self, stream=None):
-        return A.zero_partition_stats(self.handle, stream)
+    def partition_stats(self, stats, stream=None):
+        """Write this step's per-partition statistics (2*N float64) into `stats`."""
+        A.zero_partition_stats(self.handle, stats, stream)
 
-    def set_global_stats(self, global_sumsq, global_overflow):
-        A.zero_step_set_global_stats(self.handle, global_sumsq, global_overflow)
+    def set_global_stats(self, stats):
+        """Decide this step from the all-reduced statistics vector `stats`."""
+        A.zero_step_set_global_stats(self.handle, stats)
 
     def adam(self, rank, grad, master, m, v, param_out, lr, beta1, beta2, eps, wd, adamw,
              loss_scale, clip, remote_sumsq=0.0, remote_overflow=0, stream=None):

@@ -223,122 +223,33 @@ class Run:
                 del others
                 self.gather_shards = [None] * w.n_ranks
         self.slice_lists = {r: [self.slices[r][j] for j in range(w.n_ranks)] for r in self.ranks}
-        bucket = w.bucket_elems
-        tile = Z.ZERO_NORM_TILE   # buckets are rounded up to whole norm tiles
-        if bucket:
-            bucket = -(-bucket // tile) * tile
-            self.buckets = -(-P // bucket) if P else 0
-        else:
-            self.buckets = 1 if P else 0
-        # one job over several GPUs: this process's statistics are all-reduced
-        # with the other GPUs' before the decision (set by main())
-        self.group = None
-        self.stats = torch.zeros(2 * w.n_ranks, dtype=torch.float64, device=dev)
+        from zero_partitioned_mixed_flat_gb300.schedule import Hyper, StepBuffers, StepSchedule
+        self.bufs = StepBuffers(
+            ranks=self.ranks, slices=self.slice_lists, g=self.g, master=self.master, m=self.m,
+            v=self.v, param=self.param, shard=self.shard, gather_shards=self.gather_shards,
+            codes=getattr(self, "codes", None), scales=getattr(self, "scales", None),
+            layer_bufs=[self.gather_out, self.gather_out2] if w.stage == 3 and w.gather else [],
+            stats=torch.zeros(2 * w.n_ranks, dtype=torch.float64, device=dev))
+        self.sched = StepSchedule(self.plan, self.bufs,
+                                  Hyper(w.lr, w.beta1, w.beta2, w.eps, w.wd, int(w.adamw), w.clip),
+                                  self.S, w.bucket_elems, gather=w.stage == 3 and w.gather,
+                                  quantized=self.quantized)
+
+    def set_group(self, group):
+        """One job over several GPUs: this process's statistics are all-reduced
+        over `group` before the decision."""
+        self.bufs.group = group
 
     def calls(self, stream, slice_lists=None, side=None):
-        """The step as an ordered list of (kind, algorithmic HBM bytes, kernel
-        launches, callable, stream).  Stage 3 follows the pages' order:
-        forward gathers of every unit, then per unit in reverse order its
-        backward gather, its gradients joining the reduce bucket and a full
-        bucket reduce-scattered, then the local update.  With a `side` stream
-        the gathers alternate between two streams and two layer buffers
-        (prefetching the next unit while the current one is gathered, "10.6
-        ZeRO 与 FSDP" §10.6.4 预取); the reduce waits for the side stream, the
-        side stream's first gather waits for the previous update.  Entries of
-        kind "wait" are those stream orderings."""
-        import torch
-        w, P = self.w, self.P
-        lists = slice_lists or self.slice_lists
-        out = []
-        red_b = 2 * w.n_ranks + 4
-        sh = int(stream.cuda_stream)
-        if self.gather_shards is not None:
-            units = list(range(self.plan.n_units))
-            gb = self.gather_bytes_per_element()
-            bufs = [self.gather_out, self.gather_out2] if side is not None else [self.gather_out]
-            streams = [stream, side] if side is not None else [stream]
-            ev_main, ev_side = torch.cuda.Event(), torch.cuda.Event()
-            if side is not None:
-                out.append(("wait", 0, 0, lambda: (ev_main.record(stream), side.wait_event(ev_main)),
-                            None))
-            nth = [0]
-
-            def add_gather(u):
-                k = nth[0] % len(streams)
-                nth[0] += 1
-                st, buf = streams[k], bufs[k]
-
-                def fn(u=u, st=st, buf=buf):
-                    if self.quantized:
-                        self.plan.gather_quantized(u, self.codes, self.scales, buf, int(st.cuda_stream))
-                    else:
-                        self.plan.gather(u, self.gather_shards, buf, int(st.cuda_stream))
-                out.append(("gather", gb * int(self.plan.unit_padded[u]), 1, fn, st))
-            for u in units:
-                add_gather(u)
-            pending = []
-            for u in units[::-1]:
-                add_gather(u)
-                pending.append(u)
-                elems = sum(self.plan.shard_len(v) for v in pending)
-                if not w.bucket_elems or elems >= w.bucket_elems or u == 0:
-                    if side is not None:
-                        out.append(("wait", 0, 0, lambda: (ev_side.record(side), stream.wait_event(ev_side)),
-                                    None))
-                    first, cnt = min(pending), len(pending)
-                    for r in self.ranks:
-                        out.append(("reduce", red_b * elems, -(-cnt // 64),
-                                    lambda first=first, cnt=cnt, r=r: self.plan.reduce_units(
-                                        r, first, cnt, lists[r], self.g[r], self.S, sh), stream))
-                    pending = []
-        else:
-            launches = self.buckets if w.stage != 3 else -(-self.plan.n_units // 64)
-            for r in self.ranks:
-                out.append(("reduce", red_b * P, launches,
-                            lambda r=r: self.plan.reduce(r, lists[r], self.g[r], self.S,
-                                                         w.bucket_elems, sh), stream))
-        if self.group is not None:
-            # the multi-GPU exchange: per-partition statistics, all-reduced
-            # over the GPUs (nccl), then the decision reads the sum
-            out.append(("exchange", 16 * w.n_ranks, 1, lambda: self._exchange(), stream))
-        for i, r in enumerate(self.ranks):
-            if i == 0:
-                # the step's one decision (norm of every reduced partition,
-                # clip, skip, loss scale, t) as its own call: an empty Adam range
-                out.append(("decide", 8 * self.tiles_per_part() * len(self.ranks), 1,
-                            lambda r=r: self._adam(r, sh, decide_only=True), stream))
-            out.append(("adam", 30 * P, 1, lambda r=r: self._adam(r, sh), stream))
-            if self.quantized:
-                out.append(("quantize", int((3 + 4 / 128) * P), 1,
-                            lambda r=r: self.plan.quantize(self.shard[r], self.codes[r],
-                                                           self.scales[r], sh), stream))
-        return out
-
-    def _exchange(self):
-        from zero_partitioned_mixed_flat_gb300.parallel_host import global_decision_inputs
-        global_decision_inputs(self.plan, self.stats, self.group)
-
-    def _adam(self, r, stream, decide_only=False):
-        w = self.w
-        out = self.shard[r] if w.stage == 3 else self.param
-        if decide_only:
-            self.plan.adam_range(r, 0, 0, self.g[r], self.master[r], self.m[r], self.v[r], out,
-                                 w.lr, w.beta1, w.beta2, w.eps, w.wd, int(w.adamw), self.S, w.clip,
-                                 0.0, 0, stream)
-            return
-        self.plan.adam(r, self.g[r], self.master[r], self.m[r], self.v[r], out, w.lr, w.beta1,
-                       w.beta2, w.eps, w.wd, int(w.adamw), self.S, w.clip, 0.0, 0, stream)
+        """The step's ordered call list (zero_partitioned_mixed_flat_gb300.schedule)."""
+        return self.sched.calls(stream, side=side, slice_lists=slice_lists)
 
     def tiles_per_part(self):
-        """Norm tiles of one partition: per unit shard in stage 3."""
-        t = self.Z.ZERO_NORM_TILE
-        if self.w.stage == 3:
-            return sum(-(-self.plan.shard_len(u) // t) for u in range(self.plan.n_units))
-        return -(-self.P // t)
+        return self.sched.tiles_per_partition()
 
     def launches_per_step(self):
         import torch
-        return sum(c[2] for c in self.calls(torch.cuda.current_stream()))
+        return sum(c.launches for c in self.calls(torch.cuda.current_stream()))
 
     def gather_bytes_per_element(self):
         # lp gather: 2 B in + 2 B out; quantized: 1 B code + 4/128 B scale in, 2 B out
@@ -346,7 +257,7 @@ class Run:
 
     def bytes_per_step(self):
         import torch
-        return int(sum(c[1] for c in self.calls(torch.cuda.current_stream())))
+        return int(sum(c.nbytes for c in self.calls(torch.cuda.current_stream())))
 
 
 def dist_setup(n_gpus):
@@ -535,7 +446,7 @@ def main():
     t_setup = time.perf_counter()
     run = Run(w, part_ranks, dev)
     if one_job:
-        run.group = dist.group.WORLD
+        run.set_group(dist.group.WORLD)
     torch.cuda.synchronize()
     log("setup %.1f s: workload %s, P=%d, N=%d, partitions %s" %
         (time.perf_counter() - t_setup, w.name, run.P, w.n_ranks, part_ranks))
@@ -544,20 +455,20 @@ def main():
 
     side = torch.cuda.Stream() if (run.gather_shards is not None and not args.no_overlap) else None
     calls = run.calls(stream, side=side)
-    timed_calls = [c for c in calls if c[0] != "wait"]
-    kinds = sorted({c[0] for c in timed_calls})
+    timed_calls = [c for c in calls if c.kind != "wait"]
+    kinds = sorted({c.kind for c in timed_calls})
 
     def step(evs=None):
         i = 0
         for c in calls:
-            if c[0] == "wait":
-                c[3]()
+            if c.kind == "wait":
+                c.fn()
                 continue
             if evs is not None:
-                evs[i][0].record(c[4])
-            c[3]()
+                evs[i][0].record(c.stream)
+            c.fn()
             if evs is not None:
-                evs[i][1].record(c[4])
+                evs[i][1].record(c.stream)
             i += 1
 
     # a step that touches less than a few L2 sizes is timed step by step with a
@@ -612,7 +523,7 @@ def main():
     for e in evs:
         spans = {k: [] for k in kinds}
         for i, c in enumerate(timed_calls):
-            spans[c[0]].append((start.elapsed_time(e[i][0]), start.elapsed_time(e[i][1])))
+            spans[c.kind].append((start.elapsed_time(e[i][0]), start.elapsed_time(e[i][1])))
         for k, iv in spans.items():
             iv.sort()
             cur0, cur1 = iv[0]
@@ -624,11 +535,11 @@ def main():
                     cur1 = max(cur1, b_)
             t_kind[k] += cur1 - cur0
     t_kind = {k: v / K for k, v in t_kind.items()}
-    b_kind = {k: sum(c[1] for c in timed_calls if c[0] == k) for k in kinds}
-    n_kind = {k: sum(1 for c in timed_calls if c[0] == k) for k in kinds}
+    b_kind = {k: sum(c.nbytes for c in timed_calls if c.kind == k) for k in kinds}
+    n_kind = {k: sum(1 for c in timed_calls if c.kind == k) for k in kinds}
     ms_per_step = total_ms / K
     graph_info = None
-    if args.graph and run.group is not None:
+    if args.graph and run.bufs.group is not None:
         log("--graph: not taken with the multi-GPU exchange (its collective is not captured here)")
         args.graph = False
     if args.graph:
@@ -641,8 +552,8 @@ def main():
             gcalls = run.calls(cap, side=None)
             with torch.cuda.graph(g, stream=cap):
                 for c in gcalls:
-                    if c[0] != "wait":
-                        c[3]()
+                    if c.kind != "wait":
+                        c.fn()
         stream.wait_stream(cap)
         for _ in range(args.warmup):
             g.replay()
@@ -728,7 +639,7 @@ def main():
                                            "decision; the other ranks' slices simulated on each "
                                            "GPU" % (w.n_ranks, ws, "k" if per == 1 else
                                                     "k*%d..k*%d+%d" % (per, per, per - 1)))
-                                          if run.group is not None else
+                                          if run.bufs.group is not None else
                                           ("dp%d simulated on each GPU (ranks as device buffers)"
                                            % w.n_ranks) + (", one replica per GPU" if ws > 1 else "")},
                 "step_hbm_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
@@ -793,12 +704,12 @@ def measure_e2e(run, steps, stream, side, ws, dist, dev):
         for r in run.ranks:
             run.slices[r].copy_(host[r], non_blocking=True)
         for c in staged_calls:
-            c[3]()
+            c.fn()
         return run.plan.result()          # synchronises and reads the record
 
     def direct():
         for c in direct_calls:
-            c[3]()
+            c.fn()
         return run.plan.result()
 
     def timed(fn):

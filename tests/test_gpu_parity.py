@@ -829,6 +829,29 @@ def test_stage3_unit_by_unit_reduce_equals_partition_reduce(zlib, lp):
     assert abs(res[0][1][0] - oss) <= 1e-9 * oss
 
 
+@pytest.mark.parametrize("quant", [None, Z.ZERO_QUANT_INT8, Z.ZERO_QUANT_FP8_E4M3])
+@pytest.mark.parametrize("prefetch", [True, False])
+def test_stage3_prefetch_schedule_matches_the_oracle(zlib, quant, prefetch):
+    # the benchmark's stage-3 call list (schedule module): forward gathers of
+    # the 3 units, backward gathers in reverse order with bucketed reduces,
+    # the decision, Adam (+ quantize); with prefetch the gathers alternate
+    # between two streams and two layer buffers.  Every gathered layer buffer
+    # (both streams, both buffers) is compared whole with the oracle's gather
+    # of the shards as they stood before the step, and the step's state
+    # with the oracle's, over 3 steps (the own shard changes every step).
+    import dataclasses
+    w = WORKLOADS["profile-zero3"]
+    w = dataclasses.replace(w, bucket_elems=300_000)   # units 2 and 1 share a bucket, unit 0 alone
+    if quant is not None:
+        w = dataclasses.replace(w, gather_quantized=True, quant_format=quant)
+    h = Harness(w, full=True, threads=16, prefetch=prefetch)
+    assert (h.side is not None) == prefetch
+    for _ in range(3):
+        h.step()
+    assert h.gather_log == [2 * h.plan.n_units] * 3
+    h.close()
+
+
 def test_partly_reduced_partition_counts_only_its_part(zlib):
     # a unit reduced alone contributes only its own tiles to the step's norm
     dev = torch.device("cuda")

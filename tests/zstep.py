@@ -24,6 +24,7 @@ import torch
 import oracle
 import zero_partitioned_mixed_flat_gb300 as Z
 from zero_partitioned_mixed_flat_gb300 import synth
+from zero_partitioned_mixed_flat_gb300.schedule import Hyper, StepBuffers, StepSchedule
 from zero_partitioned_mixed_flat_gb300.workloads import Workload
 
 SEED = 0
@@ -102,7 +103,7 @@ class Harness:
 
     def __init__(self, w: Workload, ranks=None, full: bool = True, n_sample: int = 1 << 20,
                  threads: int = 8, chunk: int = 1 << 22, device="cuda", bucket=None,
-                 stage=None, sub_group: int = 0):
+                 stage=None, sub_group: int = 0, prefetch: bool = True):
         self.w = w
         self.sub_group = sub_group  # > 0: Adam in sub-groups of this many elements
         self.dev = torch.device(device)
@@ -161,6 +162,86 @@ class Harness:
                 mask[a:a + n] = False
             s.pad_idx = torch.nonzero(mask).flatten()
             self.st[r] = s
+        self._build_schedule(gen, prefetch)
+
+    # ------------------------------------------------------- the schedule
+    def _build_schedule(self, gen, prefetch):
+        """The benchmark's call list (zero_partitioned_mixed_flat_gb300.schedule)
+        over this harness's buffers; stage-3 workloads with gathers add the
+        other ranks' synthetic shards, two layer buffers and (prefetch) a side
+        stream, and every gathered layer buffer is checked against the oracle."""
+        w = self.w
+        self.gathers = bool(self.stage == 3 and w.gather)
+        self.quantized = bool(self.gathers and w.gather_quantized)
+        self.side = None
+        self.gather_log: List[Dict] = []
+        bufs = StepBuffers(ranks=self.ranks, slices={}, g={r: self.st[r].g for r in self.ranks},
+                           master={r: self.st[r].master for r in self.ranks},
+                           m={r: self.st[r].m for r in self.ranks},
+                           v={r: self.st[r].v for r in self.ranks}, param=self.param,
+                           shard={r: self.st[r].shard for r in self.ranks} if self.stage == 3 else {})
+        if self.gathers:
+            lpd = synth.LP_DTYPES[w.lp]
+            n = w.n_ranks
+            bufs.gather_shards = [self.st[j].shard if j in self.st else
+                                  synth.lp_shard(self.P, w.lp, w.master_std, 0, j, self.dev)
+                                  for j in range(n)]
+            biggest = max(self.plan.shard_len(u) for u in range(self.plan.n_units)) * n
+            bufs.layer_bufs = [torch.full((biggest,), float("nan"), dtype=lpd, device=self.dev)
+                               for _ in range(2)]
+            if self.quantized:
+                self.plan.set_gather_quantization(w.quant_format)
+                bufs.codes = [torch.empty(self.P, dtype=torch.int8, device=self.dev) for _ in range(n)]
+                bufs.scales = [torch.empty(self.P // 128, dtype=torch.float32, device=self.dev)
+                               for _ in range(n)]
+                for j in range(n):
+                    self.plan.quantize(bufs.gather_shards[j], bufs.codes[j], bufs.scales[j])
+            if prefetch:
+                self.side = torch.cuda.Stream(self.dev)
+            # compared positions of each unit's layer buffer: all of it, or
+            # (sampled harness) block-aligned windows of every rank's segment
+            self.g_windows, self.g_index = {}, {}
+            host_pos = []
+            for u in range(self.plan.n_units):
+                sl, off = self.plan.shard_len(u), self.plan.unit_shard_offset(u)
+                if self.full:
+                    wins = [(0, sl)]
+                else:
+                    L = min(2048, sl)
+                    starts = {0, (sl - L) // 128 * 128}
+                    starts |= {int(x) // 128 * 128 for x in gen.integers(0, max(1, sl - L), 6)}
+                    wins = [(k0, min(L, sl - k0)) for k0 in sorted(starts)]
+                self.g_windows[u] = wins
+                idx = np.concatenate([j * sl + k0 + np.arange(L) for k0, L in wins for j in range(n)])
+                self.g_index[u] = torch.from_numpy(idx).to(self.dev)
+                host_pos += [off + k0 + np.arange(L) for k0, L in wins]
+            self.g_host_pos = np.concatenate(host_pos)
+            self.g_host_pos_dev = torch.from_numpy(self.g_host_pos).to(self.dev)
+        self.bufs = bufs
+        self.sched = StepSchedule(self.plan, bufs, Hyper(w.lr, w.beta1, w.beta2, w.eps, w.wd,
+                                                         int(w.adamw), w.clip),
+                                  self.S, self.bucket, gather=self.gathers, quantized=self.quantized)
+
+    def _expected_gathers(self):
+        """The oracle's gather of every unit (at the compared positions) from
+        the shards as they stand before the step."""
+        w, n = self.w, self.w.n_ranks
+        host = [synth.to_numpy_codes(t[self.g_host_pos_dev]) for t in self.bufs.gather_shards]
+        exp, pos = {}, 0
+        for u in range(self.plan.n_units):
+            parts = []
+            for k0, L in self.g_windows[u]:
+                win = [h[pos:pos + L] for h in host]
+                pos += L
+                if self.quantized:
+                    qf = oracle.quantize_blocks_fp8 if w.quant_format else oracle.quantize_blocks
+                    dq = oracle.dequant_gather_fp8 if w.quant_format else oracle.dequant_gather
+                    qs = [qf(x, w.lp, 128) for x in win]
+                    parts.append(dq([q for q, _ in qs], [c for _, c in qs], w.lp, 128))
+                else:
+                    parts.append(oracle.gather(win))
+            exp[u] = np.concatenate(parts)
+        return exp
 
     # ------------------------------------------------------------ inputs
     def make_slices(self, r: int):
@@ -176,28 +257,38 @@ class Harness:
     # ------------------------------------------------------------- GPU
     def gpu_step(self):
         w = self.w
+        if not self.sub_group:
+            # the benchmark's own call list for this step
+            self.bufs.slices = {r: self.st[r].slices for r in self.ranks}
+            self.sched.loss_scale = self.S
+            stream = torch.cuda.current_stream(self.dev)
+            snaps = []
+            exp = None
+            hook = None
+            if self.gathers:
+                exp = self._expected_gathers()
+
+                def hook(u, buf, st):
+                    with torch.cuda.stream(st):
+                        snaps.append((u, buf[self.g_index[u]]))
+            StepSchedule.run(self.sched.calls(stream, side=self.side, on_gather=hook))
+            if self.side is not None:
+                stream.wait_stream(self.side)
+            res = self.plan.result()
+            if self.gathers:
+                torch.cuda.synchronize()
+                assert len(snaps) == 2 * self.plan.n_units   # forward and backward
+                for u, snap in snaps:
+                    got = synth.to_numpy_codes(snap)
+                    assert np.array_equal(got, exp[u]), "gathered layer %d differs from the oracle" % u
+                self.gather_log.append(len(snaps))
+            return res
         for r in self.ranks:
             s = self.st[r]
-            if self.stage == 3 and w.gather:
-                # the benchmark's stage-3 schedule: units in reverse order, a
-                # bucket reduce-scattered once it holds bucket_elems (or at unit 0)
-                pending = []
-                for u in reversed(range(self.plan.n_units)):
-                    pending.append(u)
-                    elems = sum(self.plan.shard_len(v) for v in pending)
-                    if not self.bucket or elems >= self.bucket or u == 0:
-                        self.plan.reduce_units(r, min(pending), len(pending), s.slices, s.g,
-                                               self.S)
-                        pending = []
-            else:
-                self.plan.reduce(r, s.slices, s.g, self.S, self.bucket)
+            self.plan.reduce(r, s.slices, s.g, self.S, self.bucket)
         for r in self.ranks:
             s = self.st[r]
             out = s.shard if self.stage == 3 else self.param
-            if not self.sub_group:
-                self.plan.adam(r, s.g, s.master, s.m, s.v, out, w.lr, w.beta1, w.beta2, w.eps,
-                               w.wd, int(w.adamw), self.S, w.clip)
-                continue
             # an empty range first (it only takes the decision), then the
             # sub-groups in reverse order, the last one ragged
             self.plan.adam_range(r, 0, 0, s.g, s.master, s.m, s.v, out, w.lr, w.beta1, w.beta2,

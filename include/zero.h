@@ -192,6 +192,21 @@ zero_status zero_reduce_partition(zero_plan *plan, int32_t rank,
                                   float *grad_out, float loss_scale,
                                   int64_t bucket_elems, void *stream);
 
+/* Several partitions in one call (one process simulating several ranks, or
+ * owning several partitions): exactly the results of calling
+ * zero_reduce_partition for ranks[0], ..., ranks[n_parts-1] in that order,
+ * bit for bit, in fewer kernel launches.  grad_slices: n_parts * N pointers,
+ * partition-major (the N slices of ranks[i] at [i*N, (i+1)*N)); grad_out:
+ * n_parts pointers.  The ranks must be distinct (ZERO_EINVAL).  The pieces of
+ * every partition (bucket_elems as for zero_reduce_partition) share launches:
+ * a launch takes consecutive pieces while they hold at most bucket_elems
+ * elements in total (all of them when bucket_elems is 0), at most 64 pieces
+ * and the slices of at most 512/N partitions (N <= 64; one partition per
+ * launch when N > 512).  Every argument is validated before any launch. */
+zero_status zero_reduce_partitions(zero_plan *plan, int32_t n_parts, const int32_t *ranks,
+                                   const void *const *grad_slices, float *const *grad_out,
+                                   float loss_scale, int64_t bucket_elems, void *stream);
+
 /* Stage 3: reduce only units [first_unit, first_unit + n_units) of rank
  * `rank`'s partition ("10.6 ZeRO 与 FSDP" §10.6.4 backward step 4: each
  * layer's gradients are reduce-scattered once its backward is done, in
@@ -291,6 +306,22 @@ zero_status zero_adam_step_range(zero_plan *plan, int32_t rank, int64_t begin,
                                  int32_t adamw, float loss_scale, float clip,
                                  double remote_sumsq, int32_t remote_overflow,
                                  void *stream);
+
+/* Several partitions' updates in one call: exactly the results of calling
+ * zero_adam_step for ranks[0], ..., ranks[n_parts-1] in that order with
+ * these arguments, bit for bit (the first call of a step takes the decision),
+ * in one kernel launch per 64 partitions.  grad, master, m, v, param_out:
+ * n_parts pointers each, entry i as zero_adam_step takes it for ranks[i]
+ * (param_out[i] may be NULL; stages 0-2: the full layout, to which the
+ * library adds ranks[i]*P; stage 3: ranks[i]'s shard).  The ranks must be
+ * distinct (ZERO_EINVAL).  Every argument is validated before any launch. */
+zero_status zero_adam_step_partitions(zero_plan *plan, int32_t n_parts, const int32_t *ranks,
+                                      const float *const *grad, float *const *master,
+                                      float *const *m, float *const *v,
+                                      void *const *param_out, float lr, float beta1,
+                                      float beta2, float eps, float wd, int32_t adamw,
+                                      float loss_scale, float clip, double remote_sumsq,
+                                      int32_t remote_overflow, void *stream);
 
 /* Decision of the last decided step: global norm, skipped flag, loss scale
  * for the next step, and the step counter t.  Any pointer may be NULL.

@@ -182,6 +182,78 @@ def test_all_ranks_of_a_maximal_plan_in_one_step(zlib):
     plan.close()
 
 
+@pytest.mark.parametrize("n,ranks,lp,bucket", [
+    (8, list(range(8)), 1, 0),
+    (8, [5, 2, 7], 0, 3 * TILE),            # a subset, out of order, ragged bucket pieces
+    (3, [0, 1, 2], 0, 0),                   # the few-slice reduce variant
+    (70, list(range(70)), 1, 0),            # > 64 slices: 14 partitions per launch; Adam in 2 launches
+    (16, list(range(16)), 0, 5 * TILE + 8),
+])
+def test_many_partitions_in_one_call_equal_one_by_one(zlib, n, ranks, lp, bucket):
+    # zero_reduce_partitions / zero_adam_step_partitions against the same
+    # per-partition calls: outputs, statistics, decision and state bit for bit
+    dev = torch.device("cuda")
+    part = 2 * TILE + 8 * (n % 5 + 1)
+    scale = 64.0 if lp == 0 else 1.0
+    sl = {r: [synth.grad_slice(part, lp, 1e-2, scale, 21, 1, j, r, dev) for j in range(n)] for r in ranks}
+    w0 = {r: synth.master_init(part, 0.02, 21, r, dev) for r in ranks}
+    hp = (1e-3, .9, .999, 1e-8, 0.01, 1, scale, 0.05)
+    res = []
+    for mode in ("one", "many"):
+        plan = _plan(n * part, n, lp, stage=2)
+        g = {r: torch.full((part,), float("nan"), device=dev) for r in ranks}
+        w = {r: w0[r].clone() for r in ranks}
+        m = {r: torch.zeros(part, device=dev) for r in ranks}
+        v = {r: torch.zeros(part, device=dev) for r in ranks}
+        param = torch.zeros(n * part, dtype=synth.LP_DTYPES[lp], device=dev)
+        for step in range(2):
+            if mode == "one":
+                for r in ranks:
+                    plan.reduce(r, sl[r], g[r], scale, bucket)
+            else:
+                plan.reduce_many(ranks, [sl[r] for r in ranks], [g[r] for r in ranks], scale, bucket)
+            _, _, vec = plan_stats(plan)
+            if mode == "one":
+                for r in ranks:
+                    plan.adam(r, g[r], w[r], m[r], v[r], param, *hp)
+            else:
+                plan.adam_many(ranks, [g[r] for r in ranks], [w[r] for r in ranks], [m[r] for r in ranks],
+                               [v[r] for r in ranks], [param] * len(ranks), *hp)
+            res.append((mode, step, plan.result(), vec, {r: (g[r].clone(), w[r].clone(), m[r].clone(),
+                                                             v[r].clone()) for r in ranks}, param.clone()))
+        plan.close()
+    one, many = res[:2], res[2:]
+    for a, b in zip(one, many):
+        assert a[2] == b[2] and a[3].tobytes() == b[3].tobytes()
+        for r in ranks:
+            for x, y in zip(a[4][r], b[4][r]):
+                assert torch.equal(x, y), r
+        assert torch.equal(a[5], b[5])
+    # and the reduced gradients are the oracle's
+    og, _, _ = oracle.reduce([synth.to_numpy_codes(t) for t in sl[ranks[-1]]], lp, scale)
+    assert same_floats(many[0][4][ranks[-1]][0].cpu().numpy(), og)
+
+
+def test_many_partitions_validation(zlib):
+    dev = torch.device("cuda")
+    plan = _plan(4 * 64, 4, 0)
+    buf = torch.zeros(64, dtype=torch.float16, device=dev)
+    g = torch.zeros(64, device=dev)
+    with pytest.raises(Z.ZeroError) as e:
+        plan.reduce_many([1, 1], [[buf] * 4, [buf] * 4], [g, g], 1.0)
+    assert e.value.code == Z.ZERO_EINVAL and "twice" in Z.zero_last_error()
+    with pytest.raises(Z.ZeroError) as e:
+        plan.reduce_many([0, 4], [[buf] * 4, [buf] * 4], [g, g], 1.0)
+    assert e.value.code == Z.ZERO_EINVAL
+    plan.reduce_many([0, 1], [[buf] * 4, [buf] * 4], [g, torch.zeros(64, device=dev)], 1.0)
+    with pytest.raises(Z.ZeroError) as e:
+        plan.adam_many([0, 0], [g, g], [g, g], [g, g], [g, g], [None, None], 1e-3, .9, .999, 1e-8,
+                       0., 1, 1.0, 1.0)
+    assert e.value.code == Z.ZERO_EINVAL
+    plan.result()
+    plan.close()
+
+
 @pytest.mark.parametrize("sub_group", [8, 40_000, 1 << 20])
 def test_adam_in_sub_groups(zlib, sub_group):
     # the optimizer step taken a sub-group at a time (sub_group_size) against

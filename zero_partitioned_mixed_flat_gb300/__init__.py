@@ -15,6 +15,7 @@ from ._abi import (  # noqa: F401
     zero_plan_destroy, zero_plan_fragments, zero_plan_query, zero_plan_set_loss_scaler,
     zero_plan_set_spin_limit, zero_plan_set_state, zero_plan_set_reduce_precision,
     zero_plan_units, zero_reduce_partition, zero_reduce_units, zero_step_result,
+    zero_reduce_partitions, zero_adam_step_partitions,
     zero_step_set_global_stats, zero_reduce_partition_noalloc, ZERO_NOALLOC_MAX_ELEMS,
     zero_quantize_shard, zero_gather_layer_quantized, ZERO_QUANT_BLOCK,
     zero_plan_set_gather_quantization, ZERO_QUANT_INT8, ZERO_QUANT_FP8_E4M3,

@@ -37,6 +37,9 @@ SIGNATURES = {
     "zero_plan_set_gather_quantization": (_i32, [_vp, _i32]),
     "zero_reduce_partition": (_i32, [_vp, _i32, _vp, _vp, _f32, _i64, _vp]),
     "zero_reduce_units": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _f32, _vp]),
+    "zero_reduce_partitions": (_i32, [_vp, _i32, _vp, _vp, _vp, _f32, _i64, _vp]),
+    "zero_adam_step_partitions": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _f32,
+                                         _f32, _f32, _i32, _f32, _f32, _f64, _i32, _vp]),
     "zero_partition_stats": (_i32, [_vp, _vp, _vp]),
     "zero_step_set_global_stats": (_i32, [_vp, _vp]),
     "zero_adam_step": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32,
@@ -196,6 +199,29 @@ def zero_reduce_units(plan: int, rank: int, first_unit: int, n_units: int, grad_
     _check(load().zero_reduce_units(plan, rank, first_unit, n_units,
                                     C.cast(_ptr_array(grad_slices), _vp), _ptr(grad_out), loss_scale,
                                     _stream(stream)), "zero_reduce_units")
+
+
+def zero_reduce_partitions(plan: int, ranks: Sequence[int], grad_slices: Sequence[Sequence],
+                           grad_out: Sequence, loss_scale: float, bucket_elems: int = 0, stream=None):
+    """grad_slices[i]: the N slices of partition ranks[i]; grad_out[i]: its output."""
+    rk = np.ascontiguousarray(ranks, np.int32)
+    flat = [x for sl in grad_slices for x in sl]
+    _check(load().zero_reduce_partitions(plan, int(rk.size), _ptr(rk), C.cast(_ptr_array(flat), _vp),
+                                         C.cast(_ptr_array(grad_out), _vp), loss_scale,
+                                         int(bucket_elems), _stream(stream)), "zero_reduce_partitions")
+
+
+def zero_adam_step_partitions(plan: int, ranks: Sequence[int], grad: Sequence, master: Sequence,
+                              m: Sequence, v: Sequence, param_out: Sequence, lr: float, beta1: float,
+                              beta2: float, eps: float, wd: float, adamw: int, loss_scale: float,
+                              clip: float, remote_sumsq: float = 0.0, remote_overflow: int = 0,
+                              stream=None):
+    rk = np.ascontiguousarray(ranks, np.int32)
+    arrs = [C.cast(_ptr_array(x), _vp) for x in (grad, master, m, v, param_out)]
+    _check(load().zero_adam_step_partitions(plan, int(rk.size), _ptr(rk), *arrs, lr, beta1, beta2,
+                                            eps, wd, int(adamw), loss_scale, clip, remote_sumsq,
+                                            int(remote_overflow), _stream(stream)),
+           "zero_adam_step_partitions")
 
 
 def zero_partition_stats(plan: int, stats, stream=None):

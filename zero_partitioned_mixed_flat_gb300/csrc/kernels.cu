@@ -112,15 +112,17 @@ __device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float x) {
 
 template <int MAXN>
 struct ReduceParams {
-    const uint4 *src[MAXN];  // slice j at the partition start
-    float4 *g;               // output at the partition start
-    double *partials;        // the partition's tile partials
-    unsigned *overflow;
-    long long seg_off[kMaxSegments];    // first element of each segment (multiple of 8)
-    long long seg_end[kMaxSegments];    // one past its last element (multiple of 8)
-    long long seg_pbase[kMaxSegments];  // partial index of its first tile
-    int seg_cta0[kMaxSegments + 1];     // first CTA of each segment; [n_seg] = grid
-    float inv;                          // float(1 / (S * N))
+    static constexpr int kSrc = MAXN > kReduceSrcTable ? MAXN : kReduceSrcTable;
+    const uint4 *src[kSrc];              // slice pointers (partition starts)
+    long long seg_off[kMaxSegments];     // first element of each segment (multiple of 8)
+    long long seg_end[kMaxSegments];     // one past its last element (multiple of 8)
+    long long seg_pbase[kMaxSegments];   // partial index of its first tile
+    float4 *seg_g[kMaxSegments];         // its partition's output (partition start)
+    double *seg_partials[kMaxSegments];  // its partition's tile partials
+    unsigned *seg_overflow[kMaxSegments];
+    int seg_src0[kMaxSegments];          // its partition's slice j is src[seg_src0 + j]
+    int seg_cta0[kMaxSegments + 1];      // first CTA of each segment; [n_seg] = grid
+    float inv;                           // float(1 / (S * N))
     int n;
     int n_seg;
 };
@@ -165,6 +167,8 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
     const long long e0 = p.seg_off[seg] + t * kTile;
     const long long e1 = e0 + kTile < p.seg_end[seg] ? e0 + kTile : p.seg_end[seg];
     const long long v_end = e1 / kVec;
+    const int s0 = p.seg_src0[seg];
+    float4 *const gout = p.seg_g[seg];
     {
         // per-thread sum of squares as an unevaluated float pair (hi + lo):
         // compensated, so the tile sum is accurate to ~1e-13 relative and the
@@ -185,7 +189,7 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
             float s[VPT][8];
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
-                const uint4 z = ok[v] ? ld_stream(p.src[0] + vi[v]) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 z = ok[v] ? ld_stream(p.src[s0] + vi[v]) : make_uint4(0u, 0u, 0u, 0u);
                 unpack8<BF16>(z, s[v]);
             }
             for (int j0 = 1; j0 < p.n; j0 += BATCH) {
@@ -194,7 +198,7 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
                 for (int v = 0; v < VPT; ++v)
 #pragma unroll
                     for (int b = 0; b < BATCH; ++b)
-                        if (j0 + b < p.n && ok[v]) q[v][b] = ld_stream(p.src[j0 + b] + vi[v]);
+                        if (j0 + b < p.n && ok[v]) q[v][b] = ld_stream(p.src[s0 + j0 + b] + vi[v]);
 #pragma unroll
                 for (int v = 0; v < VPT; ++v) {
 #pragma unroll
@@ -230,8 +234,8 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
                 const float4 hi = stage[warp][32 + lane];
                 __syncwarp();
                 const long long wv = vb + (long long)v * THREADS;  // the warp's first vector
-                if (wv + (lane >> 1) < v_end) st_stream_f4(p.g + 2 * wv + lane, lo);
-                if (wv + 16 + (lane >> 1) < v_end) st_stream_f4(p.g + 2 * wv + 32 + lane, hi);
+                if (wv + (lane >> 1) < v_end) st_stream_f4(gout + 2 * wv + lane, lo);
+                if (wv + 16 + (lane >> 1) < v_end) st_stream_f4(gout + 2 * wv + 32 + lane, hi);
             }
         }
         // fixed-shape fp64 tree: lanes (xor butterfly), then warps in order
@@ -245,10 +249,10 @@ reduce_unscale_stats(const __grid_constant__ ReduceParams<MAXN> p) {
             double tsum = 0.0;
 #pragma unroll
             for (int w = 0; w < THREADS / 32; ++w) tsum = __dadd_rn(tsum, warp_sq[w]);
-            p.partials[p.seg_pbase[seg] + t] = tsum;
+            p.seg_partials[seg][p.seg_pbase[seg] + t] = tsum;
         }
     }
-    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.overflow, 1u);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.seg_overflow[seg], 1u);
 }
 
 // ------------------------------------------------------------------ K2 decide
@@ -548,17 +552,33 @@ constexpr size_t kAdamTmaSmem = kAdamInStages * kAdamInStageBytes + kAdamOutStag
 constexpr int kAdamCtasPerSm = 2;
 static_assert(kAdamTile == kAdamConsumers * 4, "4 elements per consumer thread");
 
-struct AdamTmaParams {
+// One segment of the tile space: len elements (a multiple of 8) from these
+// pointers; its tiles are tile0 .. tile0 + ceil(len / kAdamTile) - 1.
+struct AdamSegDev {
     const float *g;
     float *master, *m, *v;
     uint16_t *param;  // NULL: no cast
+    long long len;
+    long long tile0;
+};
+
+struct AdamTmaParams {
+    AdamSegDev seg[kMaxAdamSegments];
+    long long n_tiles;  // over every segment
+    int n_seg;
     const StepRecord *rec;
     int *error;
-    long long len;  // multiple of 8
     long long spin_limit;
     float lr, beta1, beta2, omb1, omb2, eps, wd, decay;
     int adamw;
 };
+
+// the segment holding tile t, searched forward from segment c (a CTA's tiles
+// increase, so each thread's cursor only moves forward)
+__device__ __forceinline__ int adam_seg_of(const AdamTmaParams &p, long long t, int c) {
+    while (c + 1 < p.n_seg && t >= p.seg[c + 1].tile0) ++c;
+    return c;
+}
 
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
@@ -574,7 +594,7 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
     pdl_enter();
     const StepRecord *rec = p.rec;
     if (rec->skip) return;
-    const long long n_tiles = (p.len + kAdamTile - 1) / kAdamTile;
+    const long long n_tiles = p.n_tiles;
     if ((long long)blockIdx.x >= n_tiles) return;
     const long long count = (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
     unsigned char *in_base = smem;
@@ -594,6 +614,7 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
         if (lane != 0) return;
         long long k = 0;
         bool ok = true;
+        int c = 0;
         for (; k < count; ++k) {
             const int s = (int)(k % kAdamInStages);
             if (k >= kAdamInStages &&
@@ -601,15 +622,18 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
                 ok = false;
                 break;
             }
-            const long long e0 = (blockIdx.x + k * gridDim.x) * (long long)kAdamTile;
-            const long long n = p.len - e0 < kAdamTile ? p.len - e0 : kAdamTile;
+            const long long t = blockIdx.x + k * gridDim.x;
+            c = adam_seg_of(p, t, c);
+            const AdamSegDev &sg = p.seg[c];
+            const long long e0 = (t - sg.tile0) * (long long)kAdamTile;
+            const long long n = sg.len - e0 < kAdamTile ? sg.len - e0 : kAdamTile;
             const uint32_t bytes = (uint32_t)(n * sizeof(float));
             unsigned char *dst = in_base + (size_t)s * kAdamInStageBytes;
             mbar_expect_tx(&full[s], 4 * bytes);
-            bulk_load(dst, p.g + e0, bytes, &full[s]);
-            bulk_load(dst + 1 * kAdamTile * sizeof(float), p.master + e0, bytes, &full[s]);
-            bulk_load(dst + 2 * kAdamTile * sizeof(float), p.m + e0, bytes, &full[s]);
-            bulk_load(dst + 3 * kAdamTile * sizeof(float), p.v + e0, bytes, &full[s]);
+            bulk_load(dst, sg.g + e0, bytes, &full[s]);
+            bulk_load(dst + 1 * kAdamTile * sizeof(float), sg.master + e0, bytes, &full[s]);
+            bulk_load(dst + 2 * kAdamTile * sizeof(float), sg.m + e0, bytes, &full[s]);
+            bulk_load(dst + 3 * kAdamTile * sizeof(float), sg.v + e0, bytes, &full[s]);
         }
         if (!ok) atomicExch(p.error, 1);
         // Drain.  k tiles were issued.  Every tile kk < k - kAdamInStages has
@@ -640,11 +664,15 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
     c.decay = p.decay;
     c.adamw = p.adamw;
     bool ok = true;
+    int cur = 0;
     for (long long k = 0; k < count; ++k) {
         const int s = (int)(k % kAdamInStages);
         const int so = (int)(k % kAdamOutStages);
-        const long long e0 = (blockIdx.x + k * gridDim.x) * (long long)kAdamTile;
-        const int n = (int)(p.len - e0 < kAdamTile ? p.len - e0 : kAdamTile);
+        const long long t = blockIdx.x + k * gridDim.x;
+        cur = adam_seg_of(p, t, cur);
+        const AdamSegDev &sg = p.seg[cur];
+        const long long e0 = (t - sg.tile0) * (long long)kAdamTile;
+        const int n = (int)(sg.len - e0 < kAdamTile ? sg.len - e0 : kAdamTile);
         const bool got = mbar_wait_bounded(&full[s], (uint32_t)((k / kAdamInStages) & 1), p.spin_limit);
         const bool mine = got && ct * 4 < n;
         float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f), w4 = g4, m4 = g4, v4 = g4;
@@ -684,10 +712,10 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
         named_barrier(1, kAdamConsumers);
         if (ct == 0) {
             const uint32_t bytes = (uint32_t)(n * sizeof(float));
-            bulk_store(p.master + e0, ob, bytes);
-            bulk_store(p.m + e0, ob + kAdamTile * sizeof(float), bytes);
-            bulk_store(p.v + e0, ob + 2 * kAdamTile * sizeof(float), bytes);
-            if (p.param) bulk_store(p.param + e0, ob + 3 * kAdamTile * sizeof(float), (uint32_t)(n * 2));
+            bulk_store(sg.master + e0, ob, bytes);
+            bulk_store(sg.m + e0, ob + kAdamTile * sizeof(float), bytes);
+            bulk_store(sg.v + e0, ob + 2 * kAdamTile * sizeof(float), bytes);
+            if (sg.param) bulk_store(sg.param + e0, ob + 3 * kAdamTile * sizeof(float), (uint32_t)(n * 2));
             bulk_commit();
         }
     }
@@ -800,24 +828,33 @@ int occupancy(K kernel, int threads, size_t smem) {
 }
 
 template <int MAXN, bool BF16, bool ACC_LP, int VPT, int THREADS>
-cudaError_t reduce_impl(const void *const *slices, int n, const ReduceSegment *segs, int n_segs,
-                        float inv, float *g, double *partials, unsigned *overflow, cudaStream_t stream) {
-    if (n_segs < 1 || n_segs > kMaxSegments) return cudaErrorInvalidValue;
-    ReduceParams<MAXN> p;
-    for (int j = 0; j < n; ++j) p.src[j] = static_cast<const uint4 *>(slices[j]);
-    for (int j = n; j < MAXN; ++j) p.src[j] = nullptr;
-    p.g = reinterpret_cast<float4 *>(g);
-    p.partials = partials;
-    p.overflow = overflow;
+cudaError_t reduce_impl(const void *const *slices, int n_src, int n, const ReduceSegment *segs, int n_segs,
+                        float inv, cudaStream_t stream) {
+    using Params = ReduceParams<MAXN>;
+    if (n_segs < 1 || n_segs > kMaxSegments || n_src < n || n_src > Params::kSrc) return cudaErrorInvalidValue;
+    Params p;
+    for (int j = 0; j < n_src; ++j) p.src[j] = static_cast<const uint4 *>(slices[j]);
+    for (int j = n_src; j < Params::kSrc; ++j) p.src[j] = nullptr;
     long long ctas = 0;
     for (int i = 0; i < n_segs; ++i) {
+        if (segs[i].src0 < 0 || segs[i].src0 + n > n_src) return cudaErrorInvalidValue;
         p.seg_off[i] = segs[i].off;
         p.seg_end[i] = segs[i].off + segs[i].len;
         p.seg_pbase[i] = segs[i].pbase;
+        p.seg_g[i] = reinterpret_cast<float4 *>(segs[i].g);
+        p.seg_partials[i] = segs[i].partials;
+        p.seg_overflow[i] = segs[i].overflow;
+        p.seg_src0[i] = segs[i].src0;
         p.seg_cta0[i] = (int)ctas;
         ctas += (segs[i].len + kTile - 1) / kTile;  // one tile per CTA
     }
-    for (int i = n_segs; i < kMaxSegments; ++i) p.seg_off[i] = p.seg_end[i] = p.seg_pbase[i] = 0;
+    for (int i = n_segs; i < kMaxSegments; ++i) {
+        p.seg_off[i] = p.seg_end[i] = p.seg_pbase[i] = 0;
+        p.seg_g[i] = nullptr;
+        p.seg_partials[i] = nullptr;
+        p.seg_overflow[i] = nullptr;
+        p.seg_src0[i] = 0;
+    }
     p.seg_cta0[n_segs] = (int)ctas;
     p.inv = inv;
     p.n = n;
@@ -833,7 +870,7 @@ cudaError_t adam_tma_impl(const AdamTmaParams &p, cudaStream_t stream) {
     static const cudaError_t attr = cudaFuncSetAttribute(
         adam_fused_cast<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAdamTmaSmem);
     if (attr != cudaSuccess) return attr;
-    const long long tiles = (p.len + kAdamTile - 1) / kAdamTile;
+    const long long tiles = p.n_tiles;
     static const int occ = occupancy(adam_fused_cast<BF16>, kAdamTmaThreads, kAdamTmaSmem);
     long long grid = (long long)sm_count() * occ;
     if (grid > tiles) grid = tiles;
@@ -882,31 +919,26 @@ int sm_count() {
 }
 
 template <int MAXN, int VPT, int THREADS>
-cudaError_t reduce_dispatch(const void *const *slices, int n, int lp, bool acc_lp, const ReduceSegment *segs,
-                            int n_segs, float inv, float *g, double *partials, unsigned *overflow,
-                            cudaStream_t stream) {
+cudaError_t reduce_dispatch(const void *const *slices, int n_src, int n, int lp, bool acc_lp,
+                            const ReduceSegment *segs, int n_segs, float inv, cudaStream_t stream) {
     if (lp)
-        return acc_lp ? reduce_impl<MAXN, true, true, VPT, THREADS>(slices, n, segs, n_segs, inv, g, partials,
-                                                                    overflow, stream)
-                      : reduce_impl<MAXN, true, false, VPT, THREADS>(slices, n, segs, n_segs, inv, g, partials,
-                                                                     overflow, stream);
-    return acc_lp ? reduce_impl<MAXN, false, true, VPT, THREADS>(slices, n, segs, n_segs, inv, g, partials,
-                                                                 overflow, stream)
-                  : reduce_impl<MAXN, false, false, VPT, THREADS>(slices, n, segs, n_segs, inv, g, partials,
-                                                                  overflow, stream);
+        return acc_lp ? reduce_impl<MAXN, true, true, VPT, THREADS>(slices, n_src, n, segs, n_segs, inv, stream)
+                      : reduce_impl<MAXN, true, false, VPT, THREADS>(slices, n_src, n, segs, n_segs, inv, stream);
+    return acc_lp ? reduce_impl<MAXN, false, true, VPT, THREADS>(slices, n_src, n, segs, n_segs, inv, stream)
+                  : reduce_impl<MAXN, false, false, VPT, THREADS>(slices, n_src, n, segs, n_segs, inv, stream);
 }
 
-cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp, const ReduceSegment *segs,
-                          int n_segs, float inv, float *g, double *partials, unsigned *overflow,
-                          cudaStream_t stream) {
+cudaError_t launch_reduce(const void *const *slices, int n_src, int n, int lp, int acc_lp,
+                          const ReduceSegment *segs, int n_segs, float inv, cudaStream_t stream) {
+    if (n_src > reduce_src_table(n)) return cudaErrorInvalidValue;
     if (n <= kSmallN)
-        return reduce_dispatch<kSmallN, kSmallVpt, kSmallThreads>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g,
-                                                                  partials, overflow, stream);
+        return reduce_dispatch<kSmallN, kSmallVpt, kSmallThreads>(slices, n_src, n, lp, acc_lp != 0, segs,
+                                                                  n_segs, inv, stream);
     if (n <= 64)
-        return reduce_dispatch<64, kReduceVpt, kReduceThreads>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g,
-                                                               partials, overflow, stream);
-    return reduce_dispatch<1024, kReduceVpt, kReduceThreads>(slices, n, lp, acc_lp != 0, segs, n_segs, inv, g,
-                                                             partials, overflow, stream);
+        return reduce_dispatch<64, kReduceVpt, kReduceThreads>(slices, n_src, n, lp, acc_lp != 0, segs, n_segs,
+                                                               inv, stream);
+    return reduce_dispatch<1024, kReduceVpt, kReduceThreads>(slices, n_src, n, lp, acc_lp != 0, segs, n_segs,
+                                                             inv, stream);
 }
 
 cudaError_t launch_norm(const NormLaunch &a, cudaStream_t stream) {
@@ -948,19 +980,33 @@ cudaError_t launch_norm(const NormLaunch &a, cudaStream_t stream) {
     return launch_pdl(norm_decide, dim3((unsigned)blocks), dim3(kDecideThreads), 0, stream, p);
 }
 
-cudaError_t launch_adam(const float *g, float *master, float *m, float *v, void *param, int lp,
-                        int64_t len, const StepRecord *rec, int *error, int64_t spin_limit, float lr,
-                        float beta1, float beta2, float omb1, float omb2, float eps, float wd,
-                        float decay, int adamw, cudaStream_t stream) {
+cudaError_t launch_adam(const AdamSegment *segs, int n_segs, int lp, const StepRecord *rec, int *error,
+                        int64_t spin_limit, float lr, float beta1, float beta2, float omb1, float omb2,
+                        float eps, float wd, float decay, int adamw, cudaStream_t stream) {
+    if (n_segs < 1 || n_segs > kMaxAdamSegments) return cudaErrorInvalidValue;
     AdamTmaParams q;
-    q.g = g;
-    q.master = master;
-    q.m = m;
-    q.v = v;
-    q.param = static_cast<uint16_t *>(param);
+    long long tiles = 0;
+    int k = 0;
+    for (int i = 0; i < n_segs; ++i) {
+        if (segs[i].len <= 0) continue;
+        q.seg[k].g = segs[i].g;
+        q.seg[k].master = segs[i].master;
+        q.seg[k].m = segs[i].m;
+        q.seg[k].v = segs[i].v;
+        q.seg[k].param = static_cast<uint16_t *>(segs[i].param);
+        q.seg[k].len = segs[i].len;
+        q.seg[k].tile0 = tiles;
+        tiles += (segs[i].len + kAdamTile - 1) / kAdamTile;
+        ++k;
+    }
+    if (k == 0) return cudaSuccess;
+    for (int i = k; i < kMaxAdamSegments; ++i) {
+        q.seg[i] = AdamSegDev{nullptr, nullptr, nullptr, nullptr, nullptr, 0, tiles};
+    }
+    q.n_tiles = tiles;
+    q.n_seg = k;
     q.rec = rec;
     q.error = error;
-    q.len = len;
     q.spin_limit = spin_limit;
     q.lr = lr;
     q.beta1 = beta1;

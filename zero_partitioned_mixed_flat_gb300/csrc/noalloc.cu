@@ -131,8 +131,8 @@ extern "C" zero_status zero_reduce_partition_noalloc(int32_t n_ranks, zero_lp lp
     if (e != cudaSuccess) return noalloc_fail(ZERO_ECUDA, cudaGetErrorString(e));
     const float inv = float(1.0 / (double(loss_scale) * double(n_ranks)));
     if (len > 0) {
-        const zk::ReduceSegment whole = {0, len, 0};
-        e = zk::launch_reduce(grad_slices, n_ranks, lp, 0, &whole, 1, inv, grad_out, partials, overflow, s);
+        const zk::ReduceSegment whole = {0, len, 0, grad_out, partials, overflow, 0};
+        e = zk::launch_reduce(grad_slices, n_ranks, n_ranks, lp, 0, &whole, 1, inv, s);
         if (e != cudaSuccess) return noalloc_fail(ZERO_ECUDA, cudaGetErrorString(e));
     }
     const long long n_tiles = (len + zk::kTile - 1) / zk::kTile;

@@ -456,17 +456,13 @@ zero_status zero_plan_set_state(zero_plan *p, int64_t step, int32_t good_steps) 
 
 namespace {
 
-// Validation, pointer classification and (on the first reduce of a step) the
-// step reset shared by zero_reduce_partition and zero_reduce_unit.
-zero_status begin_reduce(zero_plan *p, int32_t rank, const void *const *grad_slices, float *grad_out,
-                         float loss_scale, int64_t bucket_elems, cudaStream_t s,
-                         std::vector<const void *> *src) {
+// Validation and pointer classification of one partition's reduce inputs
+// (no device work): the N translated slice pointers go to *src.
+zero_status check_reduce_job(zero_plan *p, int32_t rank, const void *const *grad_slices, float *grad_out,
+                             std::vector<const void *> *src) {
     zero_status st = check_rank(p, rank);
     if (st != ZERO_OK) return st;
     if (!grad_slices || (!grad_out && p->part > 0)) return fail(ZERO_EINVAL, "NULL slices or output");
-    if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale))
-        return fail(ZERO_EINVAL, "loss_scale must be finite and > 0");
-    if (bucket_elems < 0) return fail(ZERO_EINVAL, "bucket_elems < 0");
     for (int32_t j = 0; j < p->n_ranks; ++j) {
         if (!grad_slices[j] && p->part > 0) return fail(ZERO_EINVAL, "grad_slices[%d] is NULL", j);
         if (!aligned16(grad_slices[j])) return fail(ZERO_EALIGN, "grad_slices[%d] is not 16-byte aligned", j);
@@ -480,58 +476,94 @@ zero_status begin_reduce(zero_plan *p, int32_t rank, const void *const *grad_sli
             st = readable_by_device(grad_slices[j], p->device, "grad_slices", j, &(*src)[size_t(j)]);
             if (st != ZERO_OK) return st;
         }
-    if (p->phase != kReducing) {
-        // a new step: forget the previous step's partitions, partial sums and
-        // overflow (a partition reduced only in part then adds only that part)
-        std::memset(p->active, 0, sizeof p->active);
-        p->use_global = false;
-        p->global_stats = nullptr;
-        cudaError_t e = cudaMemsetAsync(p->d_overflow, 0, size_t(p->slots) * sizeof(unsigned), s);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(overflow)");
-        if (p->tiles_per_part > 0) {
-            e = cudaMemsetAsync(p->d_partials, 0, size_t(p->slots) * size_t(p->tiles_per_part) * sizeof(double), s);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(partials)");
-        }
-        p->phase = kReducing;
-    }
     return ZERO_OK;
 }
 
-// Reduce units [first, first + count) of the partition (one unit unless stage
-// 3).  Each unit is cut into pieces of whole norm tiles counted from the unit's
-// start (bucket_elems rounded up to tiles; 0 = the whole unit); consecutive
-// pieces share one kernel launch while their total stays within one bucket
-// (any number when bucket_elems is 0), up to the kernel's segment limit.  The
+zero_status check_reduce_scalars(float loss_scale, int64_t bucket_elems) {
+    if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale))
+        return fail(ZERO_EINVAL, "loss_scale must be finite and > 0");
+    if (bucket_elems < 0) return fail(ZERO_EINVAL, "bucket_elems < 0");
+    return ZERO_OK;
+}
+
+// On the first reduce of a step: forget the previous step's partitions,
+// partial sums and overflow words (a partition reduced only in part then adds
+// only that part).
+zero_status start_step(zero_plan *p, cudaStream_t s) {
+    if (p->phase == kReducing) return ZERO_OK;
+    std::memset(p->active, 0, sizeof p->active);
+    p->use_global = false;
+    p->global_stats = nullptr;
+    cudaError_t e = cudaMemsetAsync(p->d_overflow, 0, size_t(p->slots) * sizeof(unsigned), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(overflow)");
+    if (p->tiles_per_part > 0) {
+        e = cudaMemsetAsync(p->d_partials, 0, size_t(p->slots) * size_t(p->tiles_per_part) * sizeof(double), s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(partials)");
+    }
+    p->phase = kReducing;
+    return ZERO_OK;
+}
+
+// One partition's reduce: units [first, first + count) of partition slot
+// `slot` (one unit unless stage 3) from the N slices src into grad_out.
+struct ReduceJob {
+    int32_t slot;
+    int32_t first, count;
+    const void *const *src;
+    float *grad_out;
+};
+
+// Reduce the jobs in order.  Each unit is cut into pieces of whole norm tiles
+// counted from the unit's start (bucket_elems rounded up to tiles; 0 = the
+// whole unit); consecutive pieces, of one partition or of several, share one
+// kernel launch while their total stays within one bucket (any number when
+// bucket_elems is 0), up to the kernel's segment and slice-table limits.  The
 // grouping only decides launches: every tile's partial is the same.
-zero_status reduce_units(zero_plan *p, int32_t slot, int32_t first, int32_t count, const void *const *src,
-                         float *grad_out, float loss_scale, int64_t bucket_elems, cudaStream_t s) {
+zero_status reduce_jobs(zero_plan *p, const std::vector<ReduceJob> &jobs, float loss_scale,
+                        int64_t bucket_elems, cudaStream_t s) {
     const float inv = float(1.0 / (double(loss_scale) * double(p->n_ranks)));
-    double *partials = p->d_partials + int64_t(slot) * p->tiles_per_part;
     const int64_t piece = bucket_elems == 0 ? 0 : round_up(bucket_elems, zk::kTile);
+    const size_t table = size_t(zk::reduce_src_table(p->n_ranks));
+    std::vector<const void *> srcs;
     std::vector<zk::ReduceSegment> segs;
     int64_t launch_elems = 0;
+    int64_t in_table = -1;  // the job whose slices were appended last
+    int32_t src0 = 0;
     auto flush = [&]() -> zero_status {
         if (segs.empty()) return ZERO_OK;
-        cudaError_t e = zk::launch_reduce(src, p->n_ranks, p->lp, p->reduce_lp_accum, segs.data(),
-                                          int(segs.size()), inv, grad_out, partials, p->d_overflow + slot, s);
+        cudaError_t e = zk::launch_reduce(srcs.data(), int(srcs.size()), p->n_ranks, p->lp, p->reduce_lp_accum,
+                                          segs.data(), int(segs.size()), inv, s);
         segs.clear();
+        srcs.clear();
+        in_table = -1;
         launch_elems = 0;
         if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
         return ZERO_OK;
     };
-    for (int32_t u = first; u < first + count; ++u) {
-        const int64_t shard = p->shard_len(u);
-        const int64_t base = p->unit_part_off[size_t(u)];
-        const int64_t step = piece == 0 ? std::max<int64_t>(shard, 1) : piece;
-        for (int64_t b0 = 0; b0 < shard; b0 += step) {
-            const int64_t len = std::min(step, shard - b0);
-            if (!segs.empty() && ((piece > 0 && launch_elems + len > piece) ||
-                                  int(segs.size()) == zk::kMaxReduceSegments)) {
-                zero_status st = flush();
-                if (st != ZERO_OK) return st;
+    for (size_t ji = 0; ji < jobs.size(); ++ji) {
+        const ReduceJob &jb = jobs[ji];
+        double *partials = p->d_partials + int64_t(jb.slot) * p->tiles_per_part;
+        for (int32_t u = jb.first; u < jb.first + jb.count; ++u) {
+            const int64_t shard = p->shard_len(u);
+            const int64_t base = p->unit_part_off[size_t(u)];
+            const int64_t step = piece == 0 ? std::max<int64_t>(shard, 1) : piece;
+            for (int64_t b0 = 0; b0 < shard; b0 += step) {
+                const int64_t len = std::min(step, shard - b0);
+                const size_t need = in_table == int64_t(ji) ? 0 : size_t(p->n_ranks);
+                if (!segs.empty() && ((piece > 0 && launch_elems + len > piece) ||
+                                      int(segs.size()) == zk::kMaxReduceSegments || srcs.size() + need > table)) {
+                    zero_status st = flush();
+                    if (st != ZERO_OK) return st;
+                }
+                if (in_table != int64_t(ji)) {
+                    src0 = int32_t(srcs.size());
+                    srcs.insert(srcs.end(), jb.src, jb.src + p->n_ranks);
+                    in_table = int64_t(ji);
+                }
+                segs.push_back({base + b0, len, p->unit_tile_base[size_t(u)] + b0 / zk::kTile, jb.grad_out, partials,
+                                p->d_overflow + jb.slot, src0});
+                launch_elems += len;
             }
-            segs.push_back({base + b0, len, p->unit_tile_base[size_t(u)] + b0 / zk::kTile});
-            launch_elems += len;
         }
     }
     return flush();
@@ -546,12 +578,42 @@ zero_status zero_reduce_partition(zero_plan *p, int32_t rank, const void *const 
                                   void *stream) {
     if (!p) return fail(ZERO_EINVAL, "plan is NULL");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    zero_status st = check_reduce_scalars(loss_scale, bucket_elems);
+    if (st != ZERO_OK) return st;
     std::vector<const void *> src;
-    zero_status st = begin_reduce(p, rank, grad_slices, grad_out, loss_scale, bucket_elems, s, &src);
+    st = check_reduce_job(p, rank, grad_slices, grad_out, &src);
+    if (st != ZERO_OK) return st;
+    st = start_step(p, s);
     if (st != ZERO_OK) return st;
     const int32_t slot = p->stage == 0 ? 0 : rank;
     p->active[slot >> 6] |= uint64_t(1) << (slot & 63);
-    st = reduce_units(p, slot, 0, p->n_units(), src.data(), grad_out, loss_scale, bucket_elems, s);
+    st = reduce_jobs(p, {ReduceJob{slot, 0, p->n_units(), src.data(), grad_out}}, loss_scale, bucket_elems, s);
+    if (st != ZERO_OK) return st;
+    return note_work(p, s);
+}
+
+zero_status zero_reduce_partitions(zero_plan *p, int32_t n_parts, const int32_t *ranks,
+                                   const void *const *grad_slices, float *const *grad_out,
+                                   float loss_scale, int64_t bucket_elems, void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (n_parts < 1 || n_parts > p->n_ranks || !ranks || !grad_slices || !grad_out)
+        return fail(ZERO_EINVAL, "n_parts outside [1, N] or a NULL array");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    zero_status st = check_reduce_scalars(loss_scale, bucket_elems);
+    if (st != ZERO_OK) return st;
+    std::vector<std::vector<const void *>> srcs(static_cast<size_t>(n_parts));
+    std::vector<ReduceJob> jobs;
+    std::vector<char> seen(size_t(p->n_ranks), 0);
+    for (int32_t i = 0; i < n_parts; ++i) {
+        st = check_reduce_job(p, ranks[i], grad_slices + int64_t(i) * p->n_ranks, grad_out[i], &srcs[size_t(i)]);
+        if (st != ZERO_OK) return st;
+        if (seen[size_t(ranks[i])]++) return fail(ZERO_EINVAL, "rank %d listed twice", ranks[i]);
+        jobs.push_back({p->stage == 0 ? 0 : ranks[i], 0, p->n_units(), srcs[size_t(i)].data(), grad_out[i]});
+    }
+    st = start_step(p, s);
+    if (st != ZERO_OK) return st;
+    for (const ReduceJob &jb : jobs) p->active[jb.slot >> 6] |= uint64_t(1) << (jb.slot & 63);
+    st = reduce_jobs(p, jobs, loss_scale, bucket_elems, s);
     if (st != ZERO_OK) return st;
     return note_work(p, s);
 }
@@ -564,13 +626,16 @@ zero_status zero_reduce_units(zero_plan *p, int32_t rank, int32_t first_unit, in
     if (first_unit < 0 || n_units < 1 || first_unit + n_units > p->n_units())
         return fail(ZERO_EINVAL, "units [%d, %d) outside [0, %d)", first_unit, first_unit + n_units,
                     p->n_units());
-    std::vector<const void *> src;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    zero_status st = begin_reduce(p, rank, grad_slices, grad_out, loss_scale, 0, s, &src);
+    zero_status st = check_reduce_scalars(loss_scale, 0);
     if (st != ZERO_OK) return st;
-    const int32_t slot = rank;
-    p->active[slot >> 6] |= uint64_t(1) << (slot & 63);
-    st = reduce_units(p, slot, first_unit, n_units, src.data(), grad_out, loss_scale, 0, s);
+    std::vector<const void *> src;
+    st = check_reduce_job(p, rank, grad_slices, grad_out, &src);
+    if (st != ZERO_OK) return st;
+    st = start_step(p, s);
+    if (st != ZERO_OK) return st;
+    p->active[rank >> 6] |= uint64_t(1) << (rank & 63);
+    st = reduce_jobs(p, {ReduceJob{rank, first_unit, n_units, src.data(), grad_out}}, loss_scale, 0, s);
     if (st != ZERO_OK) return st;
     return note_work(p, s);
 }
@@ -622,23 +687,41 @@ zero_status zero_step_set_global_stats(zero_plan *p, const double *stats) {
 
 namespace {
 
-// The decision (first call of a step) and the Adam launch over partition
-// elements [begin, begin + len) of rank `rank`; shared by zero_adam_step
-// (the whole partition) and zero_adam_step_range (one sub-group).
-zero_status adam_impl(zero_plan *p, int32_t rank, int64_t begin, int64_t len, const float *grad,
-                      float *master, float *m, float *v, void *param_out, float lr, float beta1,
+// One partition's part of an Adam call: elements [begin, begin + len) of
+// rank `rank`'s partition, with that call's pointers.
+struct AdamJob {
+    int32_t rank;
+    int64_t begin, len;
+    const float *grad;
+    float *master, *m, *v;
+    void *param_out;
+};
+
+zero_status check_adam_job(const zero_plan *p, const AdamJob &j) {
+    zero_status st = check_rank(p, j.rank);
+    if (st != ZERO_OK) return st;
+    if (p->part > 0 && (!j.grad || !j.master || !j.m || !j.v)) return fail(ZERO_EINVAL, "NULL state pointer");
+    if (!aligned16(j.grad) || !aligned16(j.master) || !aligned16(j.m) || !aligned16(j.v) || !aligned16(j.param_out))
+        return fail(ZERO_EALIGN, "a state or parameter pointer is not 16-byte aligned");
+    return ZERO_OK;
+}
+
+// The decision (first call of a step) and the Adam launches over the jobs,
+// shared by zero_adam_step (one whole partition), zero_adam_step_range (one
+// sub-group) and zero_adam_step_partitions (several partitions, one launch
+// per kMaxAdamSegments of them).
+zero_status adam_impl(zero_plan *p, const std::vector<AdamJob> &jobs, float lr, float beta1,
                       float beta2, float eps, float wd, int32_t adamw, float loss_scale, float clip,
                       double remote_sumsq, int32_t remote_overflow, void *stream) {
-    zero_status st = check_rank(p, rank);
-    if (st != ZERO_OK) return st;
-    if (p->part > 0 && (!grad || !master || !m || !v)) return fail(ZERO_EINVAL, "NULL state pointer");
-    if (!aligned16(grad) || !aligned16(master) || !aligned16(m) || !aligned16(v) || !aligned16(param_out))
-        return fail(ZERO_EALIGN, "a state or parameter pointer is not 16-byte aligned");
+    for (const AdamJob &j : jobs) {
+        zero_status st = check_adam_job(p, j);
+        if (st != ZERO_OK) return st;
+    }
     if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale))
         return fail(ZERO_EINVAL, "loss_scale must be finite and > 0");
     if (!(remote_sumsq >= 0.0)) return fail(ZERO_EINVAL, "remote_sumsq must be >= 0");
     if (p->phase == kIdle) return fail(ZERO_ESTATE, "zero_adam_step before any zero_reduce_partition");
-    st = ensure_device(p);
+    zero_status st = ensure_device(p);
     if (st != ZERO_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->phase == kReducing) {
@@ -681,19 +764,34 @@ zero_status adam_impl(zero_plan *p, int32_t rank, int64_t begin, int64_t len, co
         p->phase = kDecided;
         p->t_hint += 1;
     }
-    if (len == 0) return note_work(p, s);
     const float omb1 = 1.0f - beta1;
     const float omb2 = 1.0f - beta2;
     const float decay = float(1.0 - double(lr) * double(wd));
-    void *param = nullptr;
-    if (param_out) {
-        const int64_t off = ((p->stage == 3) ? 0 : int64_t(rank) * p->part) + begin;
-        param = static_cast<uint16_t *>(param_out) + off;
+    std::vector<zk::AdamSegment> segs;
+    auto flush = [&]() -> zero_status {
+        if (segs.empty()) return ZERO_OK;
+        cudaError_t e = zk::launch_adam(segs.data(), int(segs.size()), p->lp, p->d_rec, &p->d_rec->error,
+                                        p->spin_limit, lr, beta1, beta2, omb1, omb2, eps, wd, decay,
+                                        adamw ? 1 : 0, s);
+        segs.clear();
+        if (e != cudaSuccess) return cuda_fail(e, "adam kernel launch");
+        return ZERO_OK;
+    };
+    for (const AdamJob &j : jobs) {
+        if (j.len == 0) continue;
+        void *param = nullptr;
+        if (j.param_out) {
+            const int64_t off = ((p->stage == 3) ? 0 : int64_t(j.rank) * p->part) + j.begin;
+            param = static_cast<uint16_t *>(j.param_out) + off;
+        }
+        segs.push_back({j.grad + j.begin, j.master + j.begin, j.m + j.begin, j.v + j.begin, param, j.len});
+        if (int(segs.size()) == zk::kMaxAdamSegments) {
+            st = flush();
+            if (st != ZERO_OK) return st;
+        }
     }
-    cudaError_t e = zk::launch_adam(grad + begin, master + begin, m + begin, v + begin, param, p->lp, len,
-                                    p->d_rec, &p->d_rec->error, p->spin_limit, lr, beta1, beta2, omb1, omb2,
-                                    eps, wd, decay, adamw ? 1 : 0, s);
-    if (e != cudaSuccess) return cuda_fail(e, "adam kernel launch");
+    st = flush();
+    if (st != ZERO_OK) return st;
     return note_work(p, s);
 }
 
@@ -706,7 +804,7 @@ zero_status zero_adam_step(zero_plan *p, int32_t rank, const float *grad, float 
                            float wd, int32_t adamw, float loss_scale, float clip,
                            double remote_sumsq, int32_t remote_overflow, void *stream) {
     if (!p) return fail(ZERO_EINVAL, "plan is NULL");
-    return adam_impl(p, rank, 0, p->part, grad, master, m, v, param_out, lr, beta1, beta2, eps, wd,
+    return adam_impl(p, {AdamJob{rank, 0, p->part, grad, master, m, v, param_out}}, lr, beta1, beta2, eps, wd,
                      adamw, loss_scale, clip, remote_sumsq, remote_overflow, stream);
 }
 
@@ -721,8 +819,29 @@ zero_status zero_adam_step_range(zero_plan *p, int32_t rank, int64_t begin, int6
                     (long long)begin, (long long)begin, (long long)len, (long long)p->part);
     if (begin % 8 != 0 || len % 8 != 0)
         return fail(ZERO_EALIGN, "sub-group begin and length must be multiples of 8 elements");
-    return adam_impl(p, rank, begin, len, grad, master, m, v, param_out, lr, beta1, beta2, eps, wd,
+    return adam_impl(p, {AdamJob{rank, begin, len, grad, master, m, v, param_out}}, lr, beta1, beta2, eps, wd,
                      adamw, loss_scale, clip, remote_sumsq, remote_overflow, stream);
+}
+
+zero_status zero_adam_step_partitions(zero_plan *p, int32_t n_parts, const int32_t *ranks,
+                                      const float *const *grad, float *const *master, float *const *m,
+                                      float *const *v, void *const *param_out, float lr, float beta1,
+                                      float beta2, float eps, float wd, int32_t adamw, float loss_scale,
+                                      float clip, double remote_sumsq, int32_t remote_overflow,
+                                      void *stream) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    if (n_parts < 1 || n_parts > p->n_ranks || !ranks || !grad || !master || !m || !v || !param_out)
+        return fail(ZERO_EINVAL, "n_parts outside [1, N] or a NULL array");
+    std::vector<AdamJob> jobs;
+    std::vector<char> seen(size_t(p->n_ranks), 0);
+    for (int32_t i = 0; i < n_parts; ++i) {
+        if (ranks[i] < 0 || ranks[i] >= p->n_ranks)
+            return fail(ZERO_EINVAL, "rank %d outside [0, %d)", ranks[i], p->n_ranks);
+        if (seen[size_t(ranks[i])]++) return fail(ZERO_EINVAL, "rank %d listed twice", ranks[i]);
+        jobs.push_back({ranks[i], 0, p->part, grad[i], master[i], m[i], v[i], param_out[i]});
+    }
+    return adam_impl(p, jobs, lr, beta1, beta2, eps, wd, adamw, loss_scale, clip, remote_sumsq,
+                     remote_overflow, stream);
 }
 
 zero_status zero_step_result(zero_plan *p, double *norm, int32_t *skipped, float *new_loss_scale,

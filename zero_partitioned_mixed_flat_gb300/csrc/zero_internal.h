@@ -40,19 +40,28 @@ int sm_count();
 void set_last_error(const char *msg);
 
 // One run of whole norm tiles for the reduce kernel: elements [off, off + len)
-// of the partition (off and len multiples of 8; the run starts a tile), whose
-// first tile's partial sum goes to partials[pbase].
+// of one partition (off and len multiples of 8; the run starts a tile), whose
+// first tile's partial sum goes to partials[pbase].  The partition's N slices
+// are table entries src0 .. src0 + N - 1 (pointers to the partition start),
+// its output starts at g, its overflow word is *overflow.
 struct ReduceSegment {
     int64_t off, len, pbase;
+    float *g;
+    double *partials;
+    unsigned *overflow;
+    int32_t src0;
 };
 constexpr int kMaxReduceSegments = 64;
+// Slice pointers one reduce launch can carry: enough for
+// kReduceSrcTable / N partitions when N <= 64, one partition beyond.
+constexpr int kReduceSrcTable = 512;
+inline int reduce_src_table(int n) { return n > 64 ? 1024 : kReduceSrcTable; }
 
-// Reduce the segments (at most kMaxReduceSegments) of the N slices -- pointers
-// to the partition start -- into g (partition start), one launch; partials is
-// the partition's partial array; overflow is OR-ed.
-cudaError_t launch_reduce(const void *const *slices, int n, int lp, int acc_lp,
-                          const ReduceSegment *segs, int n_segs, float inv, float *g,
-                          double *partials, unsigned *overflow, cudaStream_t stream);
+// Reduce the segments (at most kMaxReduceSegments) in one launch; slices is the
+// table of slice pointers the segments index (n_src entries, at most
+// reduce_src_table(n)); every slice holds the same lp type.
+cudaError_t launch_reduce(const void *const *slices, int n_src, int n, int lp, int acc_lp,
+                          const ReduceSegment *segs, int n_segs, float inv, cudaStream_t stream);
 
 // Bias corrections computed on the host for the step counters the decision
 // is likely to reach: entry i is for t = bc_t0 - i (1 - beta^t in fp64, then
@@ -88,8 +97,18 @@ struct NormLaunch {
 
 cudaError_t launch_norm(const NormLaunch &a, cudaStream_t stream);
 
-cudaError_t launch_adam(const float *g, float *master, float *m, float *v,
-                        void *param, int lp, int64_t len,
+// One run of the Adam kernel: len elements (a multiple of 8) at these
+// pointers (param may be NULL: no cast).
+struct AdamSegment {
+    const float *g;
+    float *master, *m, *v;
+    void *param;
+    int64_t len;
+};
+constexpr int kMaxAdamSegments = 64;
+
+// Adam + cast over the segments (at most kMaxAdamSegments) in one launch.
+cudaError_t launch_adam(const AdamSegment *segs, int n_segs, int lp,
                         const StepRecord *rec, int *error, int64_t spin_limit,
                         float lr, float beta1, float beta2, float omb1, float omb2,
                         float eps, float wd, float decay, int adamw,

@@ -58,6 +58,16 @@ class ZeroPlan:
         A.zero_reduce_partition(self.handle, rank, grad_slices, grad_out, loss_scale,
                                 bucket_elems, stream)
 
+    def reduce_many(self, ranks, grad_slices, grad_out, loss_scale, bucket_elems=0, stream=None):
+        A.zero_reduce_partitions(self.handle, ranks, grad_slices, grad_out, loss_scale, bucket_elems,
+                                 stream)
+
+    def adam_many(self, ranks, grad, master, m, v, param_out, lr, beta1, beta2, eps, wd, adamw,
+                  loss_scale, clip, remote_sumsq=0.0, remote_overflow=0, stream=None):
+        A.zero_adam_step_partitions(self.handle, ranks, grad, master, m, v, param_out, lr, beta1,
+                                    beta2, eps, wd, adamw, loss_scale, clip, remote_sumsq,
+                                    remote_overflow, stream)
+
     def reduce_units(self, rank, first_unit, n_units, grad_slices, grad_out, loss_scale, stream=None):
         A.zero_reduce_units(self.handle, rank, first_unit, n_units, grad_slices, grad_out, loss_scale,
                             stream)

@@ -83,12 +83,18 @@ class StepSchedule:
     gather: stage-3 forward/backward gathers; quantized: through codes/scales."""
 
     def __init__(self, plan, bufs: StepBuffers, hyper: Hyper, loss_scale: float,
-                 bucket_elems: int = 0, gather: bool = False, quantized: bool = False):
+                 bucket_elems: int = 0, gather: bool = False, quantized: bool = False,
+                 many: Optional[bool] = None):
         self.plan, self.bufs, self.hp = plan, bufs, hyper
         self.loss_scale = loss_scale
         self.bucket_elems = bucket_elems
         self.gather = bool(gather and plan.stage == 3)
         self.quantized = bool(quantized and self.gather)
+        # several partitions per process (stages 0-2): one reduce and one Adam
+        # call for all of them (zero_reduce_partitions, zero_adam_step_partitions)
+        if many is None:
+            many = len(bufs.ranks) > 1
+        self.many = bool(many and plan.stage != 3 and len(bufs.ranks) > 1)
         tile = A.ZERO_NORM_TILE   # buckets are rounded up to whole norm tiles
         if bucket_elems:
             b = -(-bucket_elems // tile) * tile
@@ -155,6 +161,12 @@ class StepSchedule:
                                             r, first, cnt, lists[r], b.g[r], self.loss_scale, sh),
                                         stream))
                     pending = []
+        elif self.many:
+            # every partition in one call (zero_reduce_partitions)
+            rk = list(b.ranks)
+            out.append(Call("reduce", red_b * plan.part_len * len(rk), self.many_reduce_launches(),
+                            lambda: plan.reduce_many(rk, [lists[r] for r in rk], [b.g[r] for r in rk],
+                                                     self.loss_scale, self.bucket_elems, sh), stream))
         else:
             launches = self.reduce_launches if plan.stage != 3 else -(-plan.n_units // 64)
             for r in b.ranks:
@@ -169,6 +181,11 @@ class StepSchedule:
                 # skip, loss scale, t) as its own call: an empty Adam range
                 out.append(Call("decide", 8 * self.tiles_per_partition() * len(b.ranks), 1,
                                 lambda r=r: self._adam(r, sh, decide_only=True), stream))
+            if self.many:
+                if i == 0:
+                    out.append(Call("adam", 30 * plan.part_len * len(b.ranks),
+                                    -(-len(b.ranks) // 64), lambda: self._adam_many(sh), stream))
+                continue
             out.append(Call("adam", 30 * plan.part_len, 1, lambda r=r: self._adam(r, sh), stream))
             if self.quantized:
                 out.append(Call("quantize", int((3 + 4 / 128) * plan.part_len), 1,
@@ -195,6 +212,39 @@ class StepSchedule:
             self.plan.adam_range(r, 0, 0, *args)
         else:
             self.plan.adam(r, *args)
+
+    def _adam_many(self, stream):
+        b, hp = self.bufs, self.hp
+        rk = list(b.ranks)
+        self.plan.adam_many(rk, [b.g[r] for r in rk], [b.master[r] for r in rk], [b.m[r] for r in rk],
+                            [b.v[r] for r in rk], [b.param] * len(rk), hp.lr, hp.beta1, hp.beta2,
+                            hp.eps, hp.wd, int(hp.adamw), self.loss_scale, hp.clip, 0.0, 0, stream)
+
+    def many_reduce_launches(self) -> int:
+        """Kernel launches of zero_reduce_partitions over this step's partitions
+        (the library's grouping: consecutive pieces while a launch holds at most
+        one bucket, at most 64 pieces and the slices of 512/N partitions)."""
+        P, n = self.plan.part_len, self.plan.n_ranks
+        if P == 0:
+            return 0
+        tile = A.ZERO_NORM_TILE
+        piece = -(-self.bucket_elems // tile) * tile if self.bucket_elems else 0
+        per_table = max(1, (512 if n <= 64 else 1024) // n)
+        pieces = [min(piece, P - b0) for b0 in range(0, P, piece)] if piece else [P]
+        launches, elems, segs, parts = 0, 0, 0, 0
+        for _ in self.bufs.ranks:
+            new_part = True
+            for length in pieces:
+                need = 1 if new_part else 0
+                if segs and ((piece and elems + length > piece) or segs == 64 or parts + need > per_table):
+                    launches += 1
+                    elems = segs = parts = 0
+                    need = 1
+                parts += need
+                new_part = False
+                segs += 1
+                elems += length
+        return launches + (1 if segs else 0)
 
     def tiles_per_partition(self) -> int:
         """Norm tiles of one partition (per unit shard in stage 3)."""

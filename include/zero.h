@@ -121,6 +121,13 @@ zero_status zero_plan_query(const zero_plan *plan, int64_t *psi_padded,
 zero_status zero_plan_units(const zero_plan *plan, int32_t *n_units,
                             int64_t *unit_offsets, int64_t *unit_padded);
 
+/* Each unit's shard within a rank's partition (the same for every rank):
+ * shard_len[u] = U_p / N (stage 0: U_p) and shard_offset[u] = the sum of the
+ * shard lengths of units 0 .. u-1.  n_units entries each; either array may be
+ * NULL.  Host only. */
+zero_status zero_plan_unit_shards(const zero_plan *plan, int64_t *shard_len,
+                                  int64_t *shard_offset);
+
 /* Fragments of rank r's partition: maximal runs of partition elements lying
  * in one tensor, in partition order, 4 int64 each: (tensor id, offset in the
  * tensor, offset in the partition, length).  Writes min(count, max_frag)

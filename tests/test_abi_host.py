@@ -84,6 +84,12 @@ def _cmp_layout(orc, sizes, n, align, stage, units):
         nu, uoff, upad = Z.zero_plan_units(plan)
         assert nu == lay["n_units"]
         assert list(uoff) == list(lay["unit_offsets"]) and list(upad) == list(lay["unit_padded"])
+        # each unit's shard: U_p / N (stage 0: U_p) at the running offset in a partition
+        sl, so = Z.zero_plan_unit_shards(plan, nu)
+        exp_len = [int(x) if stage == 0 else int(x) // n for x in lay["unit_padded"]]
+        assert list(sl) == exp_len
+        assert list(so) == [sum(exp_len[:u]) for u in range(nu)]
+        assert sum(exp_len) == part
         for r in range(n):
             got = Z.zero_plan_fragments(plan, r)
             exp = orc.fragments(sizes or [0], n, align, stage, r, units)

@@ -912,8 +912,12 @@ def test_stage3_prefetch_schedule_matches_the_oracle(zlib, quant, prefetch):
     # of the shards as they stood before the step, and the step's state
     # with the oracle's, over 3 steps (the own shard changes every step).
     import dataclasses
-    w = WORKLOADS["profile-zero3"]
-    w = dataclasses.replace(w, bucket_elems=300_000)   # units 2 and 1 share a bucket, unit 0 alone
+    from zero_partitioned_mixed_flat_gb300.workloads import gpt2_block
+    # the 7.5B layout in small: a rest unit and two transformer blocks, N = 64
+    blocks = gpt2_block(512)
+    w = dataclasses.replace(WORKLOADS["profile-zero3"], sizes=[8 << 20] + blocks + blocks,
+                            unit_of_tensor=[0] + [1] * len(blocks) + [2] * len(blocks),
+                            bucket_elems=60_000)   # units 2 and 1 share a bucket, unit 0 alone
     if quant is not None:
         w = dataclasses.replace(w, gather_quantized=True, quant_format=quant)
     h = Harness(w, full=True, threads=16, prefetch=prefetch)

@@ -13,6 +13,7 @@ from ._abi import (  # noqa: F401
     zero_last_error,
     zero_memory_report, zero_partition_stats, zero_plan_check, zero_plan_create,
     zero_plan_destroy, zero_plan_fragments, zero_plan_query, zero_plan_set_loss_scaler,
+    zero_plan_unit_shards,
     zero_plan_set_spin_limit, zero_plan_set_state, zero_plan_set_reduce_precision,
     zero_plan_units, zero_reduce_partition, zero_reduce_units, zero_step_result,
     zero_reduce_partitions, zero_adam_step_partitions,

@@ -30,6 +30,7 @@ SIGNATURES = {
     "zero_plan_query": (_i32, [_vp, _vp, _vp, _vp]),
     "zero_plan_units": (_i32, [_vp, _vp, _vp, _vp]),
     "zero_plan_fragments": (_i32, [_vp, _i32, _i64, _vp, _vp]),
+    "zero_plan_unit_shards": (_i32, [_vp, _vp, _vp]),
     "zero_plan_set_loss_scaler": (_i32, [_vp, _i32]),
     "zero_plan_set_state": (_i32, [_vp, _i64, _i32]),
     "zero_plan_set_spin_limit": (_i32, [_vp, _i64]),
@@ -143,6 +144,14 @@ def zero_plan_units(plan: int):
     pads = np.zeros(n.value, np.int64)
     _check(load().zero_plan_units(plan, C.byref(n), _ptr(offs), _ptr(pads)), "zero_plan_units")
     return n.value, offs, pads
+
+
+def zero_plan_unit_shards(plan: int, n_units: int):
+    """(shard length, shard offset in the partition) of every unit."""
+    ln = np.zeros(max(n_units, 1), np.int64)
+    off = np.zeros(max(n_units, 1), np.int64)
+    _check(load().zero_plan_unit_shards(plan, _ptr(ln), _ptr(off)), "zero_plan_unit_shards")
+    return ln[:n_units], off[:n_units]
 
 
 def zero_plan_fragments(plan: int, rank: int) -> np.ndarray:

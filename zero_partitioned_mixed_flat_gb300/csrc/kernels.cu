@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <climits>
 #include <mutex>
 
 namespace zk {
@@ -573,12 +574,27 @@ struct AdamTmaParams {
     int adamw;
 };
 
-// the segment holding tile t, searched forward from segment c (a CTA's tiles
-// increase, so each thread's cursor only moves forward)
-__device__ __forceinline__ int adam_seg_of(const AdamTmaParams &p, long long t, int c) {
-    while (c + 1 < p.n_seg && t >= p.seg[c + 1].tile0) ++c;
-    return c;
-}
+// A thread's current segment, kept in registers: a CTA's tiles increase, so
+// the cursor only moves forward, and the segment table (kernel parameters,
+// read with a computed index) is touched only when a tile starts a new
+// segment -- never with a single segment, whose fields are read once at
+// constant offsets.
+struct AdamCursor {
+    AdamSegDev sg;
+    long long next_tile0;  // first tile of the next segment
+    int cur;
+
+    __device__ __forceinline__ explicit AdamCursor(const AdamTmaParams &p)
+        : sg(p.seg[0]), next_tile0(p.n_seg > 1 ? p.seg[1].tile0 : LLONG_MAX), cur(0) {}
+
+    __device__ __forceinline__ void seek(const AdamTmaParams &p, long long t) {
+        while (t >= next_tile0) {
+            ++cur;
+            sg = p.seg[cur];
+            next_tile0 = cur + 1 < p.n_seg ? p.seg[cur + 1].tile0 : LLONG_MAX;
+        }
+    }
+};
 
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
@@ -614,7 +630,7 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
         if (lane != 0) return;
         long long k = 0;
         bool ok = true;
-        int c = 0;
+        AdamCursor at(p);
         for (; k < count; ++k) {
             const int s = (int)(k % kAdamInStages);
             if (k >= kAdamInStages &&
@@ -623,8 +639,8 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
                 break;
             }
             const long long t = blockIdx.x + k * gridDim.x;
-            c = adam_seg_of(p, t, c);
-            const AdamSegDev &sg = p.seg[c];
+            at.seek(p, t);
+            const AdamSegDev &sg = at.sg;
             const long long e0 = (t - sg.tile0) * (long long)kAdamTile;
             const long long n = sg.len - e0 < kAdamTile ? sg.len - e0 : kAdamTile;
             const uint32_t bytes = (uint32_t)(n * sizeof(float));
@@ -664,13 +680,13 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
     c.decay = p.decay;
     c.adamw = p.adamw;
     bool ok = true;
-    int cur = 0;
+    AdamCursor at(p);
     for (long long k = 0; k < count; ++k) {
         const int s = (int)(k % kAdamInStages);
         const int so = (int)(k % kAdamOutStages);
         const long long t = blockIdx.x + k * gridDim.x;
-        cur = adam_seg_of(p, t, cur);
-        const AdamSegDev &sg = p.seg[cur];
+        at.seek(p, t);
+        const AdamSegDev &sg = at.sg;
         const long long e0 = (t - sg.tile0) * (long long)kAdamTile;
         const int n = (int)(sg.len - e0 < kAdamTile ? sg.len - e0 : kAdamTile);
         const bool got = mbar_wait_bounded(&full[s], (uint32_t)((k / kAdamInStages) & 1), p.spin_limit);

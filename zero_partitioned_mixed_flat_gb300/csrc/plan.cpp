@@ -377,6 +377,15 @@ zero_status zero_plan_units(const zero_plan *p, int32_t *n_units, int64_t *unit_
     return ZERO_OK;
 }
 
+zero_status zero_plan_unit_shards(const zero_plan *p, int64_t *shard_len, int64_t *shard_offset) {
+    if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+    for (int32_t u = 0; u < p->n_units(); ++u) {
+        if (shard_len) shard_len[u] = p->shard_len(u);
+        if (shard_offset) shard_offset[u] = p->unit_part_off[size_t(u)];
+    }
+    return ZERO_OK;
+}
+
 zero_status zero_plan_fragments(const zero_plan *p, int32_t rank, int64_t max_frag, int64_t *frag,
                                 int64_t *count) {
     if (!p || !count) return fail(ZERO_EINVAL, "plan or count is NULL");

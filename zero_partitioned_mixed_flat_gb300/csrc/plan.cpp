@@ -39,7 +39,6 @@ int64_t round_up(int64_t x, int64_t q) { return q == 0 ? x : ((x + q - 1) / q) *
 
 enum Phase { kIdle = 0, kReducing = 1, kDecided = 2 };
 
-constexpr int64_t kDefaultSpinLimit = int64_t(1) << 22;
 
 }  // namespace
 
@@ -81,7 +80,7 @@ struct zero_plan {
     int32_t growth_interval = 1000;
     int32_t reduce_lp_accum = 0;  // 1: partial sums rounded to the lp type
     int32_t quant_format = ZERO_QUANT_INT8;  // codes of the quantized gather
-    int64_t spin_limit = kDefaultSpinLimit;
+    int64_t spin_limit = zk::kDefaultSpinLimit;
     // the device step counter as far as the host can tell without reading it:
     // the last value read back or set, plus one per decision launched since
     int64_t t_hint = 0;

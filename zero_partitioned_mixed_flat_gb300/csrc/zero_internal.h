@@ -17,6 +17,9 @@ constexpr int64_t kTile = 4096;
 // tree of the norm is a function of the partition only).
 constexpr int64_t kPartialChunk = 4096;
 
+// Default bound on the polls of a device pipeline wait (zero_plan_set_spin_limit).
+constexpr int64_t kDefaultSpinLimit = int64_t(1) << 22;
+
 // Per-plan device record of the step decision and the optimizer step state.
 struct StepRecord {
     double norm;          // global gradient norm of the decided step

@@ -182,30 +182,48 @@ def test_all_ranks_of_a_maximal_plan_in_one_step(zlib):
     plan.close()
 
 
-@pytest.mark.parametrize("n,ranks,lp,bucket", [
-    (8, list(range(8)), 1, 0),
-    (8, [5, 2, 7], 0, 3 * TILE),            # a subset, out of order, ragged bucket pieces
-    (3, [0, 1, 2], 0, 0),                   # the few-slice reduce variant
-    (70, list(range(70)), 1, 0),            # > 64 slices: 14 partitions per launch; Adam in 2 launches
-    (16, list(range(16)), 0, 5 * TILE + 8),
+@pytest.mark.parametrize("n,ranks,lp,bucket,stage", [
+    (8, list(range(8)), 1, 0, 2),
+    (8, [5, 2, 7], 0, 3 * TILE, 1),         # a subset, out of order, ragged bucket pieces
+    (3, [0, 1, 2], 0, 0, 2),                # the few-slice reduce variant
+    (70, list(range(70)), 1, 0, 2),         # > 64 slices: 14 partitions per launch; Adam in 2 launches
+    (16, list(range(16)), 0, 5 * TILE + 8, 2),
+    (4, [3, 0, 1], 1, 0, 3),                # stage 3: units, per-unit tiles, lp shards
+    (1, [0], 0, 0, 0),                      # stage 0: the DDP replica
 ])
-def test_many_partitions_in_one_call_equal_one_by_one(zlib, n, ranks, lp, bucket):
+def test_many_partitions_in_one_call_equal_one_by_one(zlib, n, ranks, lp, bucket, stage):
     # zero_reduce_partitions / zero_adam_step_partitions against the same
     # per-partition calls: outputs, statistics, decision and state bit for bit
     dev = torch.device("cuda")
-    part = 2 * TILE + 8 * (n % 5 + 1)
+    if stage == 3:
+        sizes, units = [70_000, 5, 33_000, 100_000, 7], [0, 0, 1, 2, 2]
+        probe = _plan(-1, n, lp, stage=3, sizes=sizes, units=units)
+    else:
+        sizes, units = None, None
+        probe = _plan(n * (2 * TILE + 8 * (n % 5 + 1)), n, lp, stage=stage)
+    part = probe.part_len
+    probe.close()
     scale = 64.0 if lp == 0 else 1.0
     sl = {r: [synth.grad_slice(part, lp, 1e-2, scale, 21, 1, j, r, dev) for j in range(n)] for r in ranks}
     w0 = {r: synth.master_init(part, 0.02, 21, r, dev) for r in ranks}
     hp = (1e-3, .9, .999, 1e-8, 0.01, 1, scale, 0.05)
     res = []
     for mode in ("one", "many"):
-        plan = _plan(n * part, n, lp, stage=2)
+        if stage == 3:
+            plan = _plan(-1, n, lp, stage=3, sizes=sizes, units=units)
+        else:
+            plan = _plan(n * part, n, lp, stage=stage)
         g = {r: torch.full((part,), float("nan"), device=dev) for r in ranks}
         w = {r: w0[r].clone() for r in ranks}
         m = {r: torch.zeros(part, device=dev) for r in ranks}
         v = {r: torch.zeros(part, device=dev) for r in ranks}
-        param = torch.zeros(n * part, dtype=synth.LP_DTYPES[lp], device=dev)
+        if stage == 3:
+            shard = {r: torch.zeros(part, dtype=synth.LP_DTYPES[lp], device=dev) for r in ranks}
+            outs = [shard[r] for r in ranks]
+            param = torch.cat([shard[r] for r in ranks])   # snapshot below
+        else:
+            param = torch.zeros(plan.psi_padded, dtype=synth.LP_DTYPES[lp], device=dev)
+            outs = [param] * len(ranks)
         for step in range(2):
             if mode == "one":
                 for r in ranks:
@@ -214,11 +232,13 @@ def test_many_partitions_in_one_call_equal_one_by_one(zlib, n, ranks, lp, bucket
                 plan.reduce_many(ranks, [sl[r] for r in ranks], [g[r] for r in ranks], scale, bucket)
             _, _, vec = plan_stats(plan)
             if mode == "one":
-                for r in ranks:
-                    plan.adam(r, g[r], w[r], m[r], v[r], param, *hp)
+                for r, out in zip(ranks, outs):
+                    plan.adam(r, g[r], w[r], m[r], v[r], out, *hp)
             else:
                 plan.adam_many(ranks, [g[r] for r in ranks], [w[r] for r in ranks], [m[r] for r in ranks],
-                               [v[r] for r in ranks], [param] * len(ranks), *hp)
+                               [v[r] for r in ranks], outs, *hp)
+            if stage == 3:
+                param = torch.cat([shard[r] for r in ranks])
             res.append((mode, step, plan.result(), vec, {r: (g[r].clone(), w[r].clone(), m[r].clone(),
                                                              v[r].clone()) for r in ranks}, param.clone()))
         plan.close()

@@ -1,12 +1,13 @@
 """GPU parity on the five workloads at their full sizes, in the launch
-configuration the benchmark times (same plan, same calls, same buckets).
+configuration the benchmark times (the schedule module's call list: same plan,
+same calls, same buckets, the same two-stream gather prefetch).
 
-Small workloads are compared element by element over whole partitions; the
-7.5B and 13B partitions compare the reduced gradient over the whole partition
-(the oracle reduces every element, chunked over host threads, to get the
-global norm) and master/m/v/param at ~1M sampled positions (all tile
-boundaries, both ends, random interior points), whose oracle state evolves on
-its own across the steps.
+Every workload is compared element by element over whole partitions: the
+reduced gradient bit for bit, and master, m, v and the lp parameters against
+the oracle's own state, which evolves on its own across the steps (the oracle
+runs piecewise on the host's threads: 812.5M elements per step at 13B).  The
+7.5B step's 66 unit gathers are checked against the oracle's gather in sampled
+windows of every rank's segment of every unit.
 """
 import numpy as np
 import pytest
@@ -90,9 +91,10 @@ def _check_gathers(plan, w, shards, gen, quantized, fmt=0):
 
 def test_7p5b_zero3_with_gathers(zlib):
     w = WORKLOADS["7.5b-zero3"]
-    h = Harness(w, full=False, threads=16, chunk=1 << 21)
+    h = Harness(w, full=True, threads=16, chunk=1 << 21, gather_windows=True)
     for _ in range(w.steps):
         h.step()
+    assert h.gather_log == [2 * h.plan.n_units] * w.steps
     shards = _synthetic_shards(h.plan, w, h.dev)
     _check_gathers(h.plan, w, shards, np.random.default_rng(7), quantized=False)
     _check_gathers(h.plan, w, shards, np.random.default_rng(8), quantized=True)
@@ -102,6 +104,7 @@ def test_7p5b_zero3_with_gathers(zlib):
 
 def test_13b_zero2(zlib):
     w = WORKLOADS["13b-zero2"]
-    infos = _run(Harness(w, full=False, threads=16, chunk=1 << 22), w.steps)
+    infos = _run(Harness(w, full=True, threads=16, chunk=1 << 22), w.steps)
     assert all(i["gpu"]["skipped"] == 0 for i in infos)
     assert all(i["oracle"]["coef"] < 1.0 for i in infos)   # clipping is active
+    assert all(i["compared"][0] == 812_500_096 for i in infos)

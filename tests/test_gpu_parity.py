@@ -855,6 +855,44 @@ def test_quantize_fp8_rounding_boundaries(zlib, lp):
     plan.close()
 
 
+@pytest.mark.parametrize("lp", [0, 1])
+@pytest.mark.parametrize("fmt", [Z.ZERO_QUANT_INT8, Z.ZERO_QUANT_FP8_E4M3])
+def test_quantize_every_block_maximum(zlib, lp, fmt):
+    # every positive finite lp value as the maximum |x| of a block (the block
+    # scale depends on it alone): scales and codes bit for bit against the
+    # oracle, so the quantizer's scale arithmetic is checked on its whole domain
+    rng = np.random.default_rng(70 + lp)
+    top = 0x7BFF if lp == 0 else 0x7F7F                  # the largest finite value
+    amax = np.arange(1, top + 1, dtype=np.uint16)
+    n_blocks = amax.size + 1                               # plus one all-zero block
+    n_blocks += (-n_blocks) % 2
+    blocks = np.zeros((n_blocks, 128), np.uint16)
+    blocks[:amax.size, 0] = amax
+    amax_f = oracle.lp_to_float(amax, lp)
+    frac = rng.uniform(-1.0, 1.0, (amax.size, 127)).astype(np.float32)
+    x = oracle.float_to_lp((frac * amax_f[:, None]).astype(np.float32), lp)
+    xf = oracle.lp_to_float(x, lp)
+    x[~(np.abs(xf) <= amax_f[:, None])] = 0                # |x| <= amax after rounding
+    blocks[:amax.size, 1:] = x
+    host = blocks.reshape(-1)
+    n = 2
+    plan = _plan(-1, n, lp, stage=3, align=128, sizes=[n * host.size], units=[0])
+    plan.set_gather_quantization(fmt)
+    P = plan.part_len
+    assert P == host.size
+    dev = torch.device("cuda")
+    shard = torch.from_numpy(host.view(np.int16)).to(dev).view(synth.LP_DTYPES[lp])
+    codes = torch.empty(P, dtype=torch.int8, device=dev)
+    scales = torch.empty(P // 128, dtype=torch.float32, device=dev)
+    plan.quantize(shard, codes, scales)
+    torch.cuda.synchronize()
+    o_quant, _, code_t = _quant_fns(fmt)
+    oq, osc = o_quant(host, lp, 128)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), osc.view(np.uint32))
+    assert np.array_equal(codes.cpu().numpy().view(code_t), oq.view(code_t))
+    plan.close()
+
+
 def test_quantized_gather_rejects_small_align(zlib):
     plan = _plan(-1, 2, 0, stage=3, align=8, sizes=[64, 64], units=[0, 1])
     buf = torch.zeros(1024, dtype=torch.float16, device="cuda")

@@ -66,7 +66,8 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return r;
 }
 
-// 8 codes of one thread's elements, packed 4 per word (byte k = element k).
+// K codes of one thread's elements (K a multiple of 4), packed 4 per word
+// (byte k = element k).
 // Fast path, with p = x * rcp the exact product (rcp within one ulp of
 // 1/scale, so p lies within 2^-23 |x/scale| <= 1.6e-5 of the exact quotient):
 // one fused multiply-add rounds p to its nearest-even integer k (through the
@@ -76,28 +77,49 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // to the same k (and |k| <= 127 needs no clamp).  Otherwise (rare: ties, a
 // NaN element), and for a zero, subnormal-small, huge or non-finite scale,
 // every element is divided.
-__device__ __forceinline__ void quant_codes8(const float v[8], float scale, uint32_t packed[2]) {
+template <int K>
+__device__ __forceinline__ void quant_codes(const float v[K], float scale, uint32_t packed[K / 4]) {
     bool divide = !(scale >= 0x1p-100f && scale <= 0x1p+100f);
     if (!divide) {
         const float rcp = rcp_approx(scale);
-        uint32_t t[8];
+        uint32_t t[K];
         bool near = false;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < K; ++k) {
             const float r = __fmaf_rn(v[k], rcp, kRoundMagic);
             const float d = __fmaf_rn(v[k], rcp, -__fsub_rn(r, kRoundMagic));
             near |= !(fabsf(d) < 0.5f - 0x1p-13f);
             t[k] = __float_as_uint(r);
         }
-        packed[0] = __byte_perm(__byte_perm(t[0], t[1], 0x0040u), __byte_perm(t[2], t[3], 0x0040u), 0x5410u);
-        packed[1] = __byte_perm(__byte_perm(t[4], t[5], 0x0040u), __byte_perm(t[6], t[7], 0x0040u), 0x5410u);
+#pragma unroll
+        for (int w = 0; w < K / 4; ++w)
+            packed[w] = __byte_perm(__byte_perm(t[4 * w], t[4 * w + 1], 0x0040u),
+                                    __byte_perm(t[4 * w + 2], t[4 * w + 3], 0x0040u), 0x5410u);
         divide = near;
     }
     if (divide) {
-        packed[0] = packed[1] = 0u;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) packed[k >> 2] |= code_by_division(v[k], scale) << (8 * (k & 3));
+        for (int w = 0; w < K / 4; ++w) packed[w] = 0u;
+#pragma unroll
+        for (int k = 0; k < K; ++k) packed[k >> 2] |= code_by_division(v[k], scale) << (8 * (k & 3));
     }
+}
+
+// scale = amax / 127 correctly rounded, without the division routine for the
+// usual range: Markstein's correction step (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): with y = RN(1/127) and q0 = RN(amax * y), the remainder
+// r = amax - 127 q0 is exact in one fused multiply-add, and q1 = RN(q0 + r y)
+// is the correctly rounded quotient.  The block maximum is always an lp value,
+// and the test suite checks q1 against the IEEE division for every positive
+// finite fp16 and bf16 value in [2^-90, 2^100]; outside that range (and for an
+// infinite maximum) the division routine is used.
+__device__ __forceinline__ float scale_of_amax(float amax) {
+    if (!(amax >= 0x1p-90f && amax <= 0x1p+100f)) return __fdiv_rn(amax, 127.0f);
+    constexpr float y = 1.0f / 127.0f;
+    const float q0 = __fmul_rn(amax, y);
+    const float r = __fmaf_rn(-q0, 127.0f, amax);
+    return __fmaf_rn(r, y, q0);
 }
 
 // ---- fp8 (OCP E4M3) variant: a power-of-two block scale 2^e with
@@ -127,21 +149,24 @@ __device__ __forceinline__ int fp8_scale_exponent(float amax) {
     return e > 120 ? 120 : e;
 }
 
-__device__ __forceinline__ void quant_codes8_fp8(const float v[8], float amax, float &scale,
-                                                 uint32_t packed[2]) {
+template <int K>
+__device__ __forceinline__ void quant_codes_fp8(const float v[K], float amax, float &scale,
+                                                uint32_t packed[K / 4]) {
     if (amax == 0.0f) {  // an all-zero block: scale 0 and codes 0 (also for -0)
         scale = 0.0f;
-        packed[0] = packed[1] = 0u;
+#pragma unroll
+        for (int w = 0; w < K / 4; ++w) packed[w] = 0u;
         return;
     }
     const int e = fp8_scale_exponent(amax);
     scale = __uint_as_float((uint32_t)(e + 127) << 23);
     const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
-    uint32_t h[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) h[k] = to_e4m3x2(__fmul_rn(v[2 * k], inv), __fmul_rn(v[2 * k + 1], inv));
-    packed[0] = h[0] | (h[1] << 16);
-    packed[1] = h[2] | (h[3] << 16);
+    for (int w = 0; w < K / 4; ++w) {
+        const uint32_t lo = to_e4m3x2(__fmul_rn(v[4 * w], inv), __fmul_rn(v[4 * w + 1], inv));
+        const uint32_t hi = to_e4m3x2(__fmul_rn(v[4 * w + 2], inv), __fmul_rn(v[4 * w + 3], inv));
+        packed[w] = lo | (hi << 16);
+    }
 }
 
 template <bool BF16>
@@ -160,53 +185,67 @@ __device__ __forceinline__ void from_lp4(uint2 raw, float v[4]) {
     }
 }
 
-// A half-warp per 128-element block (a warp takes a pair of blocks per 16-byte
-// load; kQuantUnroll pairs per pass): lane l holds elements 8(l mod 16) ..
-// 8(l mod 16) + 7 of block 2*pair + l/16.  scale = amax / 127 (float
-// division), code = nearest-even integer of x / scale (the correctly rounded
-// float quotient, see quant_codes8), clamped to +-127.  FP8: the E4M3 codes
-// and power-of-two scale of quant_codes8_fp8 instead.
+// Eight lanes per 128-element block, 16 contiguous elements per lane (two
+// 16-byte loads), four blocks per warp and kQuantPasses groups of them in
+// flight per pass: lane l holds elements 16(l mod 8) .. 16(l mod 8) + 15 of
+// block 4*group + l/8.  The block maximum takes three xor shuffles; scale =
+// amax / 127 (correctly rounded, scale_of_amax), code = nearest-even integer of
+// x / scale (the correctly rounded float quotient, see quant_codes), clamped to
+// +-127.  FP8: the E4M3 codes and power-of-two scale of quant_codes_fp8
+// instead.  Each lane writes its 16 codes with one 16-byte store.  (Versus a
+// half-warp per block with 8 elements per lane: the per-block work -- the
+// shuffles and the scale -- is shared by twice the elements.)
+constexpr int kQuantPasses = 2;
+
 template <bool BF16, bool FP8>
-__global__ void __launch_bounds__(kQuantThreads)
-quantize_shard_blocks(const uint4 *__restrict__ x, uint2 *__restrict__ q, float *__restrict__ scales,
+__global__ void __launch_bounds__(kQuantThreads, 2)  // room for 16 values per lane without spills
+quantize_shard_blocks(const uint4 *__restrict__ x, uint4 *__restrict__ q, float *__restrict__ scales,
                       long long n_blocks) {
     pdl_enter();
     const int lane = threadIdx.x & 31;
-    const long long n_pairs = (n_blocks + 1) / 2;
+    const int l8 = lane & 7;
+    const long long n_groups = (n_blocks + 3) / 4;
     const long long warps = (long long)gridDim.x * (kQuantThreads / 32);
     const long long w0 = (long long)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
-    for (long long base = w0; base < n_pairs; base += warps * kQuantUnroll) {
-        uint4 raw[kQuantUnroll];
+    for (long long base = w0; base < n_groups; base += warps * kQuantPasses) {
+        uint4 raw[kQuantPasses][2];
 #pragma unroll
-        for (int u = 0; u < kQuantUnroll; ++u) {
-            const long long b = 2 * (base + u * warps) + (lane >> 4);
-            raw[u] = b < n_blocks ? __ldcs(x + b * 16 + (lane & 15)) : make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < kQuantPasses; ++u) {
+            const long long b = 4 * (base + u * warps) + (lane >> 3);
+            if (b < n_blocks) {
+                raw[u][0] = __ldg(x + b * 16 + 2 * l8);
+                raw[u][1] = __ldg(x + b * 16 + 2 * l8 + 1);
+            } else {
+                raw[u][0] = raw[u][1] = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
 #pragma unroll
-        for (int u = 0; u < kQuantUnroll; ++u) {
-            const long long pair = base + u * warps;
-            if (pair >= n_pairs) break;  // uniform across the warp
-            const long long b = 2 * pair + (lane >> 4);
-            float v[8];
-            from_lp4<BF16>(make_uint2(raw[u].x, raw[u].y), v);
-            from_lp4<BF16>(make_uint2(raw[u].z, raw[u].w), v + 4);
+        for (int u = 0; u < kQuantPasses; ++u) {
+            const long long group = base + u * warps;
+            if (group >= n_groups) break;  // uniform across the warp
+            const long long b = 4 * group + (lane >> 3);
+            float v[16];
+            from_lp4<BF16>(make_uint2(raw[u][0].x, raw[u][0].y), v);
+            from_lp4<BF16>(make_uint2(raw[u][0].z, raw[u][0].w), v + 4);
+            from_lp4<BF16>(make_uint2(raw[u][1].x, raw[u][1].y), v + 8);
+            from_lp4<BF16>(make_uint2(raw[u][1].z, raw[u][1].w), v + 12);
             float amax = 0.0f;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
+            for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
 #pragma unroll
-            for (int off = 8; off > 0; off >>= 1)  // within each half-warp
+            for (int off = 4; off > 0; off >>= 1)  // within each group of 8 lanes
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
             float scale;
-            uint32_t packed[2];
+            uint32_t packed[4];
             if constexpr (FP8) {
-                quant_codes8_fp8(v, amax, scale, packed);
+                quant_codes_fp8<16>(v, amax, scale, packed);
             } else {
-                scale = __fdiv_rn(amax, 127.0f);
-                quant_codes8(v, scale, packed);
+                scale = scale_of_amax(amax);
+                quant_codes<16>(v, scale, packed);
             }
             if (b < n_blocks) {
-                __stcs(q + b * 16 + (lane & 15), make_uint2(packed[0], packed[1]));
-                if ((lane & 15) == 0) scales[b] = scale;
+                __stcs(q + b * 8 + l8, make_uint4(packed[0], packed[1], packed[2], packed[3]));
+                if (l8 == 0) scales[b] = scale;
             }
         }
     }
@@ -313,11 +352,11 @@ cudaError_t quantize_impl(const void *shard, int64_t len, int8_t *codes, float *
     if (blocks == 0) return cudaSuccess;
     static const int occ = blocks_per_sm(quantize_shard_blocks<BF16, FP8>);
     long long grid = (long long)sm_count() * occ;
-    const long long per_cta = (kQuantThreads / 32) * kQuantUnroll * 2;
+    const long long per_cta = (kQuantThreads / 32) * kQuantPasses * 4;
     const long long need = (blocks + per_cta - 1) / per_cta;
     if (grid > need) grid = need;
     return launch_pdl(quantize_shard_blocks<BF16, FP8>, dim3((unsigned)grid), dim3(kQuantThreads), 0, stream,
-                      static_cast<const uint4 *>(shard), reinterpret_cast<uint2 *>(codes), scales, blocks);
+                      static_cast<const uint4 *>(shard), reinterpret_cast<uint4 *>(codes), scales, blocks);
 }
 
 }  // namespace

@@ -186,8 +186,7 @@ __device__ __forceinline__ void from_lp4(uint2 raw, float v[4]) {
 }
 
 // Eight lanes per 128-element block, 16 contiguous elements per lane (two
-// 16-byte loads), four blocks per warp and kQuantPasses groups of them in
-// flight per pass: lane l holds elements 16(l mod 8) .. 16(l mod 8) + 15 of
+// 16-byte loads), four blocks per warp, kQuantPasses groups of them per pass: lane l holds elements 16(l mod 8) .. 16(l mod 8) + 15 of
 // block 4*group + l/8.  The block maximum takes three xor shuffles; scale =
 // amax / 127 (correctly rounded, scale_of_amax), code = nearest-even integer of
 // x / scale (the correctly rounded float quotient, see quant_codes), clamped to
@@ -195,10 +194,10 @@ __device__ __forceinline__ void from_lp4(uint2 raw, float v[4]) {
 // instead.  Each lane writes its 16 codes with one 16-byte store.  (Versus a
 // half-warp per block with 8 elements per lane: the per-block work -- the
 // shuffles and the scale -- is shared by twice the elements.)
-constexpr int kQuantPasses = 2;
+constexpr int kQuantPasses = 1;  // 1, 2, 3, 4 swept on GB300: 1 is fastest (int8 0.081 vs 0.083-0.097 ms at 7.5B)
 
 template <bool BF16, bool FP8>
-__global__ void __launch_bounds__(kQuantThreads, 2)  // room for 16 values per lane without spills
+__global__ void __launch_bounds__(kQuantThreads, 3)  // 16 values per lane without spills
 quantize_shard_blocks(const uint4 *__restrict__ x, uint4 *__restrict__ q, float *__restrict__ scales,
                       long long n_blocks) {
     pdl_enter();

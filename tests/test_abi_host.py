@@ -206,6 +206,44 @@ def test_step_calls_validate_before_touching_the_device(lib):
         with pytest.raises(Z.ZeroError):
             Z.zero_plan_fragments(plan, 5)
         assert "rank" in Z.zero_last_error()
+        # several partitions in one call: every argument checked before any CUDA call
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_reduce_partitions(plan, [1, 1], [[buf, buf], [buf, buf]], [buf, buf], 1.0,
+                                     stream=0)
+        assert e.value.code == Z.ZERO_EINVAL and "twice" in Z.zero_last_error()
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_reduce_partitions(plan, [0, 2], [[buf, buf], [buf, buf]], [buf, buf], 1.0,
+                                     stream=0)
+        assert e.value.code == Z.ZERO_EINVAL                     # rank >= N
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_reduce_partitions(plan, [0, 1], [[buf, buf], [buf, buf + 8]], [buf, buf], 1.0,
+                                     stream=0)
+        assert e.value.code == Z.ZERO_EALIGN                     # misaligned slice of rank 1
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_reduce_partitions(plan, [0, 1, 1], [[buf, buf]] * 3, [buf] * 3, 1.0, stream=0)
+        assert e.value.code == Z.ZERO_EINVAL                     # more partitions than N
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_adam_step_partitions(plan, [0, 0], [buf] * 2, [buf] * 2, [buf] * 2, [buf] * 2,
+                                        [buf] * 2, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0, stream=0)
+        assert e.value.code == Z.ZERO_EINVAL and "twice" in Z.zero_last_error()
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_adam_step_partitions(plan, [0, 1], [buf] * 2, [buf, buf + 4], [buf] * 2,
+                                        [buf] * 2, [buf] * 2, 1e-3, .9, .999, 1e-8, 0., 1, 1.0, 1.0,
+                                        stream=0)
+        assert e.value.code == Z.ZERO_EALIGN
+        # the statistics exchange: order and pointer checks
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_partition_stats(plan, buf, stream=0)
+        assert e.value.code == Z.ZERO_ESTATE                     # nothing reduced yet
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_partition_stats(plan, buf + 4, stream=0)
+        assert e.value.code == Z.ZERO_EALIGN
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_partition_stats(plan, None, stream=0)
+        assert e.value.code == Z.ZERO_EINVAL
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_step_set_global_stats(plan, buf)
+        assert e.value.code == Z.ZERO_ESTATE
     finally:
         Z.zero_plan_destroy(plan)
     p3 = Z.zero_plan_create(-1, 2, [64, 64], 8, 3, [0, 1], 0)

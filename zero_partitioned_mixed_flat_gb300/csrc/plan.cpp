@@ -464,10 +464,9 @@ zero_status zero_plan_set_state(zero_plan *p, int64_t step, int32_t good_steps) 
 
 namespace {
 
-// Validation and pointer classification of one partition's reduce inputs
-// (no device work): the N translated slice pointers go to *src.
-zero_status check_reduce_job(zero_plan *p, int32_t rank, const void *const *grad_slices, float *grad_out,
-                             std::vector<const void *> *src) {
+// Argument checks of one partition's reduce inputs (host only, no CUDA call).
+zero_status check_reduce_args(const zero_plan *p, int32_t rank, const void *const *grad_slices,
+                              const float *grad_out) {
     zero_status st = check_rank(p, rank);
     if (st != ZERO_OK) return st;
     if (!grad_slices || (!grad_out && p->part > 0)) return fail(ZERO_EINVAL, "NULL slices or output");
@@ -476,6 +475,15 @@ zero_status check_reduce_job(zero_plan *p, int32_t rank, const void *const *grad
         if (!aligned16(grad_slices[j])) return fail(ZERO_EALIGN, "grad_slices[%d] is not 16-byte aligned", j);
     }
     if (!aligned16(grad_out)) return fail(ZERO_EALIGN, "grad_out is not 16-byte aligned");
+    return ZERO_OK;
+}
+
+// The argument checks, then the classification of the slice pointers (a CUDA
+// query): the N translated slice pointers go to *src.
+zero_status check_reduce_job(zero_plan *p, int32_t rank, const void *const *grad_slices, float *grad_out,
+                             std::vector<const void *> *src) {
+    zero_status st = check_reduce_args(p, rank, grad_slices, grad_out);
+    if (st != ZERO_OK) return st;
     st = ensure_device(p);
     if (st != ZERO_OK) return st;
     src->assign(size_t(p->n_ranks), nullptr);
@@ -609,13 +617,17 @@ zero_status zero_reduce_partitions(zero_plan *p, int32_t n_parts, const int32_t 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     zero_status st = check_reduce_scalars(loss_scale, bucket_elems);
     if (st != ZERO_OK) return st;
+    std::vector<char> seen(size_t(p->n_ranks), 0);
+    for (int32_t i = 0; i < n_parts; ++i) {  // every argument before any CUDA call
+        st = check_reduce_args(p, ranks[i], grad_slices + int64_t(i) * p->n_ranks, grad_out[i]);
+        if (st != ZERO_OK) return st;
+        if (seen[size_t(ranks[i])]++) return fail(ZERO_EINVAL, "rank %d listed twice", ranks[i]);
+    }
     std::vector<std::vector<const void *>> srcs(static_cast<size_t>(n_parts));
     std::vector<ReduceJob> jobs;
-    std::vector<char> seen(size_t(p->n_ranks), 0);
     for (int32_t i = 0; i < n_parts; ++i) {
         st = check_reduce_job(p, ranks[i], grad_slices + int64_t(i) * p->n_ranks, grad_out[i], &srcs[size_t(i)]);
         if (st != ZERO_OK) return st;
-        if (seen[size_t(ranks[i])]++) return fail(ZERO_EINVAL, "rank %d listed twice", ranks[i]);
         jobs.push_back({p->stage == 0 ? 0 : ranks[i], 0, p->n_units(), srcs[size_t(i)].data(), grad_out[i]});
     }
     st = start_step(p, s);

@@ -683,6 +683,32 @@ def test_global_stats_replace_the_local_sum(zlib):
     one.close()
 
 
+def test_stats_vector_in_pinned_host_memory(zlib):
+    # the statistics vector may live in pinned host memory (e.g. a gloo
+    # exchange buffer): exported and read back by the kernels in place
+    dev = torch.device("cuda")
+    n, part = 3, 2 * TILE + 24
+    res = []
+    for where in ("device", "host"):
+        plan = _plan(n * part, n, 0, stage=2)
+        sl = [synth.grad_slice(part, 0, 1e-2, 64.0, 31, 1, j, 1, dev) for j in range(n)]
+        g = torch.empty(part, device=dev)
+        w, m, v = (torch.zeros(part, device=dev) for _ in range(3))
+        plan.reduce(1, sl, g, 64.0)
+        stats = (torch.full((2 * n,), float("nan"), dtype=torch.float64, device=dev) if where == "device"
+                 else torch.full((2 * n,), float("nan"), dtype=torch.float64, pin_memory=True))
+        plan.partition_stats(stats)
+        torch.cuda.synchronize()
+        vec = stats.cpu().numpy().copy()
+        assert vec[0] == 0.0 and vec[2] == 0.0 and vec[1] > 0 and not vec[n:].any()
+        plan.set_global_stats(stats)
+        plan.adam(1, g, w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 64.0, 0.05)
+        res.append((plan.result(), vec, w.clone()))
+        plan.close()
+    assert res[0][0] == res[1][0] and res[0][1].tobytes() == res[1][1].tobytes()
+    assert torch.equal(res[0][2], res[1][2])
+
+
 def test_exported_stats_decide_like_the_local_sum(zlib):
     # every partition of a ragged random plan reduced in one process: deciding
     # from the exported vector gives the local decision's bits (norm included)

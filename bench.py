@@ -60,6 +60,9 @@ def parse_args():
                     help="sum the gradient slices in the lp type (reduce_dtype=float16)")
     ap.add_argument("--quant-format", choices=["int8", "fp8"], default=None,
                     help="code format of the quantized gather (default: the workload's)")
+    ap.add_argument("--dist-backend", choices=["nccl", "gloo"], default="nccl",
+                    help="torch.distributed backend under torchrun (gloo: host-staged exchange, "
+                         "e.g. several processes on one GPU)")
     return ap.parse_args()
 
 
@@ -260,16 +263,23 @@ class Run:
         return int(sum(c.nbytes for c in self.calls(torch.cuda.current_stream())))
 
 
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend="nccl"):
+    """(world size, rank, device index, torch.distributed or None).  One process
+    per GPU; with fewer visible GPUs than local ranks (a gloo run of several
+    processes on one GPU) the ranks share devices round-robin."""
     import torch
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-        return ws, rank, local, dist
+        dev = local % max(1, torch.cuda.device_count())
+        torch.cuda.set_device(dev)
+        if backend == "nccl":
+            dist.init_process_group("nccl", device_id=torch.device("cuda", dev))
+        else:
+            dist.init_process_group(backend)
+        return ws, rank, dev, dist
     torch.cuda.set_device(0)
     return 1, 0, 0, None
 
@@ -416,7 +426,7 @@ def main():
     import zero_partitioned_mixed_flat_gb300 as Z
     from zero_partitioned_mixed_flat_gb300.workloads import WORKLOADS
     Z.load()
-    ws, rank, local, dist = dist_setup(args.gpus)
+    ws, rank, local, dist = dist_setup(args.gpus, args.dist_backend)
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
     if args.n_ranks:

@@ -41,3 +41,29 @@ def test_bench_json_line(zlib, extra):
     assert set(d["kernels"]) == {"reduce", "decide", "adam"}
     if extra:
         assert d["graph"]["graph_ms_per_step"] == d["ms_per_step"]
+
+
+def test_bench_one_job_over_two_ranks(zlib):
+    # the multi-GPU path of the benchmark (one job, the per-partition statistics
+    # all-reduced before every decision), run as two gloo ranks sharing this
+    # GPU: the same code as under nccl on two GPUs except the exchange backend
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--gpus", "2",
+           "--workload", "gpt2-xl-zero2", "--steps", "3", "--warmup", "3", "--no-cpu-baseline",
+           "--e2e-steps", "2", "--no-clocks", "--dist-backend", "gloo"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1                       # rank 0 alone prints
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["value"] > 0 and d["scaling"] == "weak"
+    assert "job over 2 GPUs" in d["config"]["parallelism"]
+    assert d["config"]["partitions_per_gpu"] == 1
+    # per step: the reduce, the statistics export, the decision, Adam
+    assert d["gpu_launches"] == 3 * 4
+    assert "exchange" in d["kernels"] and d["e2e"]["value"] > 0
+    assert d["decision"]["skipped"] == 0 and d["decision"]["step"] == 3 + 3   # warm-up + timed

@@ -691,10 +691,19 @@ def measure_e2e(run, steps, stream, side, ws, dist, dev):
     torch.cuda.synchronize()
     need = sum(int(t.numel()) * t.element_size() for t in run.slices.values())
     avail = host_mem_available()
-    if avail is not None and need * 2 > avail:
-        log("e2e skipped: %.1f GB of host buffers needed, %.1f GB available" % (need / 1e9, avail / 1e9))
-        return {"value": None, "unit": UNIT, "skipped": "host memory: %.1f GB needed, %.1f GB "
-                "available" % (need / 1e9, avail / 1e9)}
+    if avail is not None:
+        # the processes of this node share its memory
+        avail //= max(1, int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
+    ok = avail is None or need * 2 <= avail
+    if dist:  # every rank takes the same branch (the timed part has collectives)
+        flag = torch.tensor([1.0 if ok else 0.0], device=dev, dtype=torch.float64)
+        dist.all_reduce(flag, op=dist.ReduceOp.MIN)
+        ok = bool(flag.item() > 0)
+    if not ok:
+        log("e2e skipped: %.1f GB of host buffers needed per process, %s GB available"
+            % (need / 1e9, "%.1f" % (avail / 1e9) if avail is not None else "?"))
+        return {"value": None, "unit": UNIT, "skipped": "host memory: %.1f GB needed per process"
+                % (need / 1e9)}
     host = {}
     try:
         for r in run.ranks:

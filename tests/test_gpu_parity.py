@@ -274,6 +274,40 @@ def test_many_partitions_validation(zlib):
     plan.close()
 
 
+def test_all_ranks_of_a_maximal_plan_in_few_calls(zlib):
+    # the 1024 partitions of a maximal plan through zero_reduce_partitions (one
+    # partition per launch: 1024 slice pointers fill the table) and
+    # zero_adam_step_partitions (16 launches of 64): the bits of the
+    # per-partition calls
+    n, part, lr, b1, b2, eps, wd = Z.ZERO_MAX_RANKS, 16, 1e-3, 0.9, 0.999, 1e-8, 0.01
+    dev = torch.device("cuda")
+    big = synth.grad_slice(n * n * part, 0, 1e-2, 1.0, 5, 1, 0, 0, dev).view(n, n, part)
+    base, row = big.data_ptr(), part * 2
+    w0 = synth.master_init(n * part, 0.02, 5, 0, dev).view(n, part)
+    out = []
+    for many in (False, True):
+        plan = _plan(n * part, n, 0)
+        g = torch.empty((n, part), dtype=torch.float32, device=dev)
+        w, m, v = w0.clone(), torch.zeros_like(w0), torch.zeros_like(w0)
+        param = torch.zeros(n * part, dtype=torch.float16, device=dev)
+        sl = [[base + (r * n + j) * row for j in range(n)] for r in range(n)]
+        hp = (lr, b1, b2, eps, wd, 1, 1.0, 0.05)
+        if many:
+            plan.reduce_many(list(range(n)), sl, [g[r] for r in range(n)], 1.0)
+            plan.adam_many(list(range(n)), [g[r] for r in range(n)], [w[r] for r in range(n)],
+                           [m[r] for r in range(n)], [v[r] for r in range(n)], [param] * n, *hp)
+        else:
+            for r in range(n):
+                plan.reduce(r, sl[r], g[r], 1.0)
+            for r in range(n):
+                plan.adam(r, g[r], w[r], m[r], v[r], param, *hp)
+        out.append((plan.result(), g.clone(), w.clone(), m.clone(), v.clone(), param.clone()))
+        plan.close()
+    assert out[0][0] == out[1][0]
+    for a, b in zip(out[0][1:], out[1][1:]):
+        assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("sub_group", [8, 40_000, 1 << 20])
 def test_adam_in_sub_groups(zlib, sub_group):
     # the optimizer step taken a sub-group at a time (sub_group_size) against

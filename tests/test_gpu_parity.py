@@ -717,6 +717,34 @@ def test_global_stats_replace_the_local_sum(zlib):
     one.close()
 
 
+def test_exported_flags_name_the_overflowing_partition(zlib):
+    # three partitions reduced in one process, an inf in partition 1's slices:
+    # the export flags exactly that partition, its sum is not finite, the other
+    # sums are the oracle's; deciding from the vector skips the step
+    dev = torch.device("cuda")
+    n, part = 3, TILE + 8
+    plan = _plan(n * part, n, 0, stage=2)
+    sl = {r: [synth.grad_slice(part, 0, 1e-2, 64.0, 41, 1, j, r, dev) for j in range(n)] for r in range(n)}
+    sl[1][2][TILE - 3] = float("inf")
+    g = {r: torch.empty(part, device=dev) for r in range(n)}
+    for r in range(n):
+        plan.reduce(r, sl[r], g[r], 64.0)
+    _, _, vec = plan_stats(plan)
+    assert list(vec[n:]) == [0.0, 1.0, 0.0]
+    assert not np.isfinite(vec[1])
+    for r in (0, 2):
+        _, oss, oof = oracle.reduce([synth.to_numpy_codes(t) for t in sl[r]], 0, 64.0)
+        assert oof == 0 and abs(vec[r] - oss) <= 1e-9 * oss
+    stats = torch.from_numpy(vec.copy()).to(dev)
+    plan.set_global_stats(stats)
+    w = torch.zeros(part, device=dev)
+    m, v = torch.zeros_like(w), torch.zeros_like(w)
+    plan.adam(0, g[0], w, m, v, None, 1e-3, .9, .999, 1e-8, 0., 1, 64.0, 1.0)
+    r = plan.result()
+    assert r["skipped"] == 1 and r["step"] == 0 and not w.any().item()
+    plan.close()
+
+
 def test_stats_vector_in_pinned_host_memory(zlib):
     # the statistics vector may live in pinned host memory (e.g. a gloo
     # exchange buffer): exported and read back by the kernels in place

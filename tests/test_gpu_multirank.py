@@ -1,4 +1,4 @@
-"""libzero's multi-rank path across processes, on one GPU.
+"""libzero's multi-rank path across processes, on one GPU (stages 2 and 3).
 
 Two or three processes share the GPU and exchange bytes with gloo (through
 host memory).  No kernel of one process waits for another process: the only
@@ -12,7 +12,10 @@ exchanges are host-side collectives between a step's launches.  Two flows:
  - full data path: W = N = 2 or 3 ranks, each holding its own flat gradient.
    An all-to-all hands every rank the N slices of its partition (the
    reduce-scatter's input), the statistics go as above, and after the update
-   the lp partitions are all-gathered into every rank's full layout.
+   the lp partitions are all-gathered into every rank's full layout;
+ - stage 3, W = N = 2 or 3: the same reduce-scatter and statistics, the update
+   into each rank's own shard, then every unit all-gathered across the ranks
+   into a layer buffer, checked against the oracle's gather of the shards.
 
 Every rank's decision must be identical, and its master, m, v and parameters
 bit-identical to one process stepping all N partitions through the parity
@@ -28,6 +31,7 @@ import pytest
 import torch
 import torch.multiprocessing as mp
 
+from zero_partitioned_mixed_flat_gb300 import synth
 from zero_partitioned_mixed_flat_gb300.workloads import Workload
 
 from .zstep import Harness
@@ -38,7 +42,12 @@ SEED = 0
 STEPS = 3
 
 
-def _workload(n):
+def _workload(n, stage=2):
+    if stage == 3:
+        return Workload(name="multirank3", sizes=[70_000, 5, 33_000, 100_000, 7], n_ranks=n,
+                        stage=3, unit_of_tensor=[0, 0, 1, 2, 2], lp=0, ranks=list(range(n)),
+                        steps=STEPS, loss_scale=1024.0, growth_interval=1000,
+                        grads_times_scale=True, inject_inf_step=2, align=8, lr=1e-3, clip=0.05)
     return Workload(name="multirank", sizes=[100_000, 7, 33_333], n_ranks=n, stage=2, lp=0,
                     ranks=list(range(n)), steps=STEPS, loss_scale=1024.0, growth_interval=1000,
                     grads_times_scale=True, inject_inf_step=2, align=8, lr=1e-3, clip=0.05)
@@ -49,6 +58,7 @@ def _child(rank, world, port, wfields, mode, q):
     import zero_partitioned_mixed_flat_gb300 as Z
     from zero_partitioned_mixed_flat_gb300 import synth
     from zero_partitioned_mixed_flat_gb300.parallel_host import (allgather_partitions,
+                                                                allgather_unit,
                                                                 exchange_gradients,
                                                                 global_decision_inputs,
                                                                 partitions_for)
@@ -60,7 +70,7 @@ def _child(rank, world, port, wfields, mode, q):
         Z.load()
         w = Workload(**wfields)
         N = w.n_ranks
-        plan = Z.ZeroPlan(-1, N, w.sizes, w.align, w.stage, None, w.lp,
+        plan = Z.ZeroPlan(-1, N, w.sizes, w.align, w.stage, w.unit_of_tensor, w.lp,
                           growth_interval=w.growth_interval)
         P = plan.part_len
         mine = partitions_for(world, rank, N) if mode == "owned" else [rank]
@@ -70,6 +80,9 @@ def _child(rank, world, port, wfields, mode, q):
         v = {p: torch.zeros(P, device=dev) for p in mine}
         g = {p: torch.empty(P, device=dev) for p in mine}
         param = torch.zeros(plan.psi_padded, dtype=synth.LP_DTYPES[w.lp], device=dev)
+        shard = torch.zeros(P, dtype=synth.LP_DTYPES[w.lp], device=dev)      # stage 3
+        layer = torch.empty(max(plan.shard_len(u) for u in range(plan.n_units)) * N,
+                            dtype=synth.LP_DTYPES[w.lp], device=dev)
         stats = torch.empty(2 * N, dtype=torch.float64, device=dev)
         S = w.loss_scale
         out = []
@@ -98,16 +111,25 @@ def _child(rank, world, port, wfields, mode, q):
                 plan.reduce(rank, [slices[j] for j in range(N)], g[rank], S)
             global_decision_inputs(plan, stats)
             for p in mine:
-                plan.adam(p, g[p], master[p], m[p], v[p], param, w.lr, w.beta1, w.beta2, w.eps,
-                          w.wd, int(w.adamw), S, w.clip)
+                plan.adam(p, g[p], master[p], m[p], v[p], shard if w.stage == 3 else param, w.lr,
+                          w.beta1, w.beta2, w.eps, w.wd, int(w.adamw), S, w.clip)
             res = plan.result()
-            if mode == "data":
+            layers = None
+            if w.stage == 3:
+                # every unit's shards all-gathered into a layer buffer
+                layers = []
+                for u in range(plan.n_units):
+                    layers.append(allgather_unit(plan, u, shard, layer).view(torch.int16).cpu().numpy())
+            elif mode == "data":
                 allgather_partitions(param, rank, P)
             torch.cuda.synchronize()
+            own = shard if w.stage == 3 else None
             state = {p: (master[p].cpu().numpy(), m[p].cpu().numpy(), v[p].cpu().numpy(),
-                         param[p * P:(p + 1) * P].view(torch.int16).cpu().numpy()) for p in mine}
-            full_param = param.view(torch.int16).cpu().numpy() if mode == "data" else None
-            out.append((res, state, full_param))
+                         (own if own is not None else param[p * P:(p + 1) * P]).view(torch.int16)
+                         .cpu().numpy()) for p in mine}
+            full_param = param.view(torch.int16).cpu().numpy() if (mode == "data" and w.stage != 3) \
+                else None
+            out.append((res, state, full_param, layers))
             S = res["loss_scale"]
         plan.close()
         q.put((rank, out))
@@ -148,36 +170,55 @@ def _same_decision(a, b):
 
 
 def _reference(w):
-    """One process, every partition: per step (decision, state per partition, param)."""
+    """One process, every partition: per step (decision, state per partition,
+    param, and in stage 3 the oracle's gather of every unit from the shards)."""
+    import oracle
     h = Harness(w)
     ref = []
     for _ in range(STEPS):
         info = h.step()                      # checked against the oracle
         P = h.P
         torch.cuda.synchronize()
+        if w.stage == 3:
+            lp_of = {r: h.st[r].shard for r in h.ranks}
+        else:
+            lp_of = {r: h.param[r * P:(r + 1) * P] for r in h.ranks}
         state = {r: (h.st[r].master.cpu().numpy(), h.st[r].m.cpu().numpy(),
-                     h.st[r].v.cpu().numpy(),
-                     h.param[r * P:(r + 1) * P].view(torch.int16).cpu().numpy()) for r in h.ranks}
-        ref.append((info["gpu"], state, h.param.view(torch.int16).cpu().numpy()))
+                     h.st[r].v.cpu().numpy(), lp_of[r].view(torch.int16).cpu().numpy())
+                 for r in h.ranks}
+        layers = None
+        if w.stage == 3:
+            layers = []
+            for u in range(h.plan.n_units):
+                sl, off = h.plan.shard_len(u), h.plan.unit_shard_offset(u)
+                layers.append(oracle.gather([synth.to_numpy_codes(h.st[r].shard[off:off + sl])
+                                             for r in h.ranks]).view(np.int16))
+        full = h.param.view(torch.int16).cpu().numpy() if h.param is not None else None
+        ref.append((info["gpu"], state, full, layers))
     h.close()
     return ref
 
 
-@pytest.mark.parametrize("world,mode", [(2, "owned"), (3, "owned"), (2, "data"), (3, "data")])
-def test_ranks_across_processes_equal_one_process(zlib, world, mode):
-    w = _workload(4 if mode == "owned" else world)
+@pytest.mark.parametrize("world,mode,stage", [(2, "owned", 2), (3, "owned", 2), (2, "data", 2),
+                                              (3, "data", 2), (2, "data", 3), (3, "data", 3)])
+def test_ranks_across_processes_equal_one_process(zlib, world, mode, stage):
+    w = _workload(4 if mode == "owned" else world, stage)
     ref = _reference(w)
     res = _run(world, w, mode)
     seen_skip = False
     for step in range(STEPS):
-        r_dec, r_state, r_param = ref[step]
+        r_dec, r_state, r_param, r_layers = ref[step]
         seen_skip |= bool(r_dec["skipped"])
         for rank in range(world):
-            dec, state, full = res[rank][step]
+            dec, state, full, layers = res[rank][step]
             assert _same_decision(dec, r_dec), (step, rank, dec, r_dec)
             for p, arrays in state.items():
                 for name, a, b in zip(("master", "m", "v", "param"), arrays, r_state[p]):
                     assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), (step, rank, p, name)
             if full is not None:
                 assert np.array_equal(full, r_param), (step, rank)
+            if stage == 3:      # every unit gathered across the ranks = the oracle's gather
+                assert len(layers) == len(r_layers)
+                for u, (a, b) in enumerate(zip(layers, r_layers)):
+                    assert np.array_equal(a, b), (step, rank, u)
     assert seen_skip    # the overflow on partition 0 skipped the step on every rank

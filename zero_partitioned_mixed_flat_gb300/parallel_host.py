@@ -80,6 +80,29 @@ def allgather_partitions(param_full, rank: int, part_len: int, group=None):
     return param_full
 
 
+def allgather_unit(plan, unit: int, shard, layer, group=None):
+    """Stage 3 ("10.6 ZeRO 与 FSDP" §10.6.4 step 1): all-gather unit `unit`'s
+    shards of every rank (this rank's is its P-element shard buffer `shard`)
+    into `layer`, whose first N * U_p/N elements receive the unit in full
+    layout (rank j's shard at [j * U_p/N, (j+1) * U_p/N))."""
+    import torch.distributed as dist
+    n = dist.get_world_size(group)
+    if n != plan.n_ranks:
+        raise ValueError("one process per rank: world size must equal N")
+    sl, off = plan.shard_len(unit), plan.unit_shard_offset(unit)
+    mine = shard[off:off + sl]
+    out = layer[:n * sl]
+    work, staged = _staged(out, group)
+    if staged or dist.get_backend(group) == "gloo":
+        src = mine.cpu() if mine.is_cuda else mine.clone()
+    else:
+        src = mine
+    dist.all_gather_into_tensor(work, src, group=group)
+    if staged:
+        out.copy_(work)
+    return out
+
+
 def global_decision_inputs(plan, stats, group=None):
     """The multi-rank exchange of one step, between the reduces and the first
     Adam call: export this rank's per-partition statistics into `stats`

@@ -208,8 +208,8 @@ zero_status zero_reduce_partition(zero_plan *plan, int32_t rank,
  * every partition (bucket_elems as for zero_reduce_partition) share launches:
  * a launch takes consecutive pieces while they hold at most bucket_elems
  * elements in total (all of them when bucket_elems is 0), at most 64 pieces
- * and the slices of at most 512/N partitions (N <= 64; one partition per
- * launch when N > 512).  Every argument is validated before any launch. */
+ * and the slice pointers of floor(512/N) partitions when N <= 64, of
+ * floor(1024/N) when N > 64.  Every argument is validated before any launch. */
 zero_status zero_reduce_partitions(zero_plan *plan, int32_t n_parts, const int32_t *ranks,
                                    const void *const *grad_slices, float *const *grad_out,
                                    float loss_scale, int64_t bucket_elems, void *stream);

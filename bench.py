@@ -502,16 +502,20 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3 if not args.no_clocks else 0.0)
+    # the timed steps: no event between a step's calls (an event record between
+    # two kernels costs their programmatic-launch overlap); with the L2 flush,
+    # one event pair per step keeps the flush out of the step's time
     start.record(stream)
     for k in range(K):
         if flush is not None:
             with torch.cuda.stream(stream):
                 flush.fill_(float(k))
-        step_ev[k][0].record(stream)
-        step(evs[k])
+            step_ev[k][0].record(stream)
+        step()
         if side is not None:
             stream.wait_stream(side)
-        step_ev[k][1].record(stream)
+        if flush is not None:
+            step_ev[k][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -526,6 +530,17 @@ def main():
     res = run.plan.result()
     if res["skipped"]:
         log("warning: a timed step was skipped (overflow)")
+    # per-kind times: K more steps, now with an event pair around every call
+    kstart = torch.cuda.Event(enable_timing=True)
+    kstart.record(stream)
+    for k in range(K):
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush.fill_(float(k))
+        step(evs[k])
+        if side is not None:
+            stream.wait_stream(side)
+    torch.cuda.synchronize()
     # per kind: time per step (sum of its calls), bytes per step, launches per step
     # time per kind and step = the union of its calls' intervals (calls of one
     # kind may overlap when gathers are prefetched on the second stream)
@@ -533,7 +548,7 @@ def main():
     for e in evs:
         spans = {k: [] for k in kinds}
         for i, c in enumerate(timed_calls):
-            spans[c.kind].append((start.elapsed_time(e[i][0]), start.elapsed_time(e[i][1])))
+            spans[c.kind].append((kstart.elapsed_time(e[i][0]), kstart.elapsed_time(e[i][1])))
         for k, iv in spans.items():
             iv.sort()
             cur0, cur1 = iv[0]

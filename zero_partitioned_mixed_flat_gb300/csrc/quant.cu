@@ -186,15 +186,16 @@ __device__ __forceinline__ void from_lp4(uint2 raw, float v[4]) {
 }
 
 // Eight lanes per 128-element block, 16 contiguous elements per lane (two
-// 16-byte loads), four blocks per warp, kQuantPasses groups of them per pass: lane l holds elements 16(l mod 8) .. 16(l mod 8) + 15 of
-// block 4*group + l/8.  The block maximum takes three xor shuffles; scale =
+// 16-byte loads), four blocks per warp, one group of four blocks per warp and
+// iteration (1 to 4 groups per iteration were swept on GB300: 1 is fastest):
+// lane l holds elements 16(l mod 8) .. 16(l mod 8) + 15 of block
+// 4*group + l/8.  The block maximum takes three xor shuffles; scale =
 // amax / 127 (correctly rounded, scale_of_amax), code = nearest-even integer of
 // x / scale (the correctly rounded float quotient, see quant_codes), clamped to
 // +-127.  FP8: the E4M3 codes and power-of-two scale of quant_codes_fp8
 // instead.  Each lane writes its 16 codes with one 16-byte store.  (Versus a
 // half-warp per block with 8 elements per lane: the per-block work -- the
 // shuffles and the scale -- is shared by twice the elements.)
-constexpr int kQuantPasses = 1;  // 1, 2, 3, 4 swept on GB300: 1 is fastest (int8 0.081 vs 0.083-0.097 ms at 7.5B)
 
 template <bool BF16, bool FP8>
 __global__ void __launch_bounds__(kQuantThreads, 3)  // 16 values per lane without spills
@@ -206,46 +207,54 @@ quantize_shard_blocks(const uint4 *__restrict__ x, uint4 *__restrict__ q, float 
     const long long n_groups = (n_blocks + 3) / 4;
     const long long warps = (long long)gridDim.x * (kQuantThreads / 32);
     const long long w0 = (long long)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5);
-    for (long long base = w0; base < n_groups; base += warps * kQuantPasses) {
-        uint4 raw[kQuantPasses][2];
-#pragma unroll
-        for (int u = 0; u < kQuantPasses; ++u) {
-            const long long b = 4 * (base + u * warps) + (lane >> 3);
-            if (b < n_blocks) {
-                raw[u][0] = __ldg(x + b * 16 + 2 * l8);
-                raw[u][1] = __ldg(x + b * 16 + 2 * l8 + 1);
-            } else {
-                raw[u][0] = raw[u][1] = make_uint4(0u, 0u, 0u, 0u);
-            }
+    // int8: a software pipeline, the next group's two loads in flight while
+    // this group is quantized (the exactness test makes the compute long: 0.081
+    // -> 0.071 ms at 7.5B); fp8, whose compute is short, loads then computes
+    // (the pipeline measured 3 % slower there)
+    auto load = [&](long long group, uint4 r[2]) {
+        const long long b = 4 * group + (lane >> 3);
+        if (group < n_groups && b < n_blocks) {
+            r[0] = __ldg(x + b * 16 + 2 * l8);
+            r[1] = __ldg(x + b * 16 + 2 * l8 + 1);
+        } else {
+            r[0] = r[1] = make_uint4(0u, 0u, 0u, 0u);
         }
+    };
+    uint4 cur[2], nxt[2];
+    if constexpr (!FP8) load(w0, cur);
+    for (long long group = w0; group < n_groups; group += warps) {  // uniform across the warp
+        if constexpr (FP8) {
+            load(group, cur);
+        } else {
+            load(group + warps, nxt);
+        }
+        const long long b = 4 * group + (lane >> 3);
+        float v[16];
+        from_lp4<BF16>(make_uint2(cur[0].x, cur[0].y), v);
+        from_lp4<BF16>(make_uint2(cur[0].z, cur[0].w), v + 4);
+        from_lp4<BF16>(make_uint2(cur[1].x, cur[1].y), v + 8);
+        from_lp4<BF16>(make_uint2(cur[1].z, cur[1].w), v + 12);
+        float amax = 0.0f;
 #pragma unroll
-        for (int u = 0; u < kQuantPasses; ++u) {
-            const long long group = base + u * warps;
-            if (group >= n_groups) break;  // uniform across the warp
-            const long long b = 4 * group + (lane >> 3);
-            float v[16];
-            from_lp4<BF16>(make_uint2(raw[u][0].x, raw[u][0].y), v);
-            from_lp4<BF16>(make_uint2(raw[u][0].z, raw[u][0].w), v + 4);
-            from_lp4<BF16>(make_uint2(raw[u][1].x, raw[u][1].y), v + 8);
-            from_lp4<BF16>(make_uint2(raw[u][1].z, raw[u][1].w), v + 12);
-            float amax = 0.0f;
+        for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
 #pragma unroll
-            for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
-#pragma unroll
-            for (int off = 4; off > 0; off >>= 1)  // within each group of 8 lanes
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-            float scale;
-            uint32_t packed[4];
-            if constexpr (FP8) {
-                quant_codes_fp8<16>(v, amax, scale, packed);
-            } else {
-                scale = scale_of_amax(amax);
-                quant_codes<16>(v, scale, packed);
-            }
-            if (b < n_blocks) {
-                __stcs(q + b * 8 + l8, make_uint4(packed[0], packed[1], packed[2], packed[3]));
-                if (l8 == 0) scales[b] = scale;
-            }
+        for (int off = 4; off > 0; off >>= 1)  // within each group of 8 lanes
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        float scale;
+        uint32_t packed[4];
+        if constexpr (FP8) {
+            quant_codes_fp8<16>(v, amax, scale, packed);
+        } else {
+            scale = scale_of_amax(amax);
+            quant_codes<16>(v, scale, packed);
+        }
+        if (b < n_blocks) {
+            __stcs(q + b * 8 + l8, make_uint4(packed[0], packed[1], packed[2], packed[3]));
+            if (l8 == 0) scales[b] = scale;
+        }
+        if constexpr (!FP8) {
+            cur[0] = nxt[0];
+            cur[1] = nxt[1];
         }
     }
 }
@@ -351,7 +360,7 @@ cudaError_t quantize_impl(const void *shard, int64_t len, int8_t *codes, float *
     if (blocks == 0) return cudaSuccess;
     static const int occ = blocks_per_sm(quantize_shard_blocks<BF16, FP8>);
     long long grid = (long long)sm_count() * occ;
-    const long long per_cta = (kQuantThreads / 32) * kQuantPasses * 4;
+    const long long per_cta = (kQuantThreads / 32) * 4;  // blocks per CTA per iteration
     const long long need = (blocks + per_cta - 1) / per_cta;
     if (grid > need) grid = need;
     return launch_pdl(quantize_shard_blocks<BF16, FP8>, dim3((unsigned)grid), dim3(kQuantThreads), 0, stream,

@@ -223,7 +223,8 @@ class StepSchedule:
     def many_reduce_launches(self) -> int:
         """Kernel launches of zero_reduce_partitions over this step's partitions
         (the library's grouping: consecutive pieces while a launch holds at most
-        one bucket, at most 64 pieces and the slices of 512/N partitions)."""
+        one bucket, at most 64 pieces and the slices of floor(512/N) partitions,
+        floor(1024/N) when N > 64)."""
         P, n = self.plan.part_len, self.plan.n_ranks
         if P == 0:
             return 0

@@ -222,3 +222,39 @@ def test_ranks_across_processes_equal_one_process(zlib, world, mode, stage):
                 for u, (a, b) in enumerate(zip(layers, r_layers)):
                     assert np.array_equal(a, b), (step, rank, u)
     assert seen_skip    # the overflow on partition 0 skipped the step on every rank
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_random_jobs_across_processes(zlib, seed):
+    # random layouts, world sizes and stages through the full data path
+    rng = np.random.default_rng(300 + seed)
+    world = int(rng.choice([2, 3]))
+    stage = int(rng.choice([2, 3]))
+    k = int(rng.integers(2, 6))
+    sizes = [int(x) for x in rng.integers(1, 60_000, k)]
+    units = None
+    if stage == 3:
+        units, u = [0], 0
+        for _ in range(k - 1):
+            u += int(rng.integers(0, 2))
+            units.append(u)
+    w = dataclasses.replace(_workload(world, stage), sizes=sizes, unit_of_tensor=units,
+                            lp=int(rng.integers(0, 2)), clip=float(rng.choice([0.0, 0.05])),
+                            adamw=bool(rng.integers(0, 2)))
+    if w.lp == 1:
+        w = dataclasses.replace(w, loss_scale=1.0, grads_times_scale=False, inject_inf_step=0)
+    ref = _reference(w)
+    res = _run(world, w, "data")
+    for step in range(STEPS):
+        r_dec, r_state, r_param, r_layers = ref[step]
+        for rank in range(world):
+            dec, state, full, layers = res[rank][step]
+            assert _same_decision(dec, r_dec), (seed, step, rank)
+            for p, arrays in state.items():
+                for name, a, b in zip(("master", "m", "v", "param"), arrays, r_state[p]):
+                    assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), (seed, step, rank, name)
+            if stage == 3:
+                for a, b in zip(layers, r_layers):
+                    assert np.array_equal(a, b), (seed, step, rank)
+            else:
+                assert np.array_equal(full, r_param), (seed, step, rank)

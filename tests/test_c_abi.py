@@ -1,6 +1,7 @@
 """The ABI from plain C (CPU only): a C11 program compiled against
-include/zero.h and linked to libzero.so creates a plan, reads its layout and
-the memory report, and destroys it; the values must be the oracle's."""
+include/zero.h and linked to libzero.so creates plans, reads their layout
+(stage-3 unit shards included) and the memory report, checks the exchange
+calls' state errors, and destroys the plans; the values must be the oracle's."""
 import os
 import subprocess
 import tempfile
@@ -34,6 +35,17 @@ int main(void) {
     for (int k = 0; k < 4; ++k) printf("%.17g %lld %lld\n", formula[k], (long long)actual[k], (long long)comm[k]);
     if (zero_plan_create(-1, 0, sizes, 3, 128, 2, NULL, ZERO_BF16, &plan) != ZERO_EINVAL) return 4;
     printf("%s\n", zero_last_error()[0] ? "error-message" : "no-message");
+    /* a stage-3 plan: each unit's shard, and the exchange calls out of order */
+    const int32_t units[3] = {0, 0, 1};
+    if (zero_plan_create(-1, 4, sizes, 3, 8, 3, units, ZERO_FP16, &plan) != ZERO_OK) return 5;
+    int64_t shard_len[2], shard_off[2];
+    if (zero_plan_unit_shards(plan, shard_len, shard_off) != ZERO_OK) return 6;
+    printf("%lld %lld %lld %lld\n", (long long)shard_len[0], (long long)shard_len[1],
+           (long long)shard_off[0], (long long)shard_off[1]);
+    double stats[8];
+    if (zero_partition_stats(plan, stats, NULL) != ZERO_ESTATE) return 7;
+    if (zero_step_set_global_stats(plan, stats) != ZERO_ESTATE) return 8;
+    zero_plan_destroy(plan);
     return 0;
 }
 """
@@ -64,3 +76,6 @@ def test_c_program_uses_the_abi():
         f, a, c = lines[1 + k].split()
         assert float(f) == formula[k] and int(a) == actual[k] and int(c) == comm[k]
     assert lines[5] == "error-message"
+    lay3 = oracle.layout([1000, 24, 70000], 4, 8, 3, [0, 0, 1])
+    shard = [int(x) // 4 for x in lay3["unit_padded"]]
+    assert [int(x) for x in lines[6].split()] == shard + [0, shard[0]]

@@ -636,6 +636,82 @@ def test_synchronising_calls_wait_only_for_the_plan(zlib):
     plan.close()
 
 
+def test_plans_on_host_threads_are_independent(zlib):
+    # different plans are independent: three plans stepped at once from three
+    # host threads, each on its own stream (ctypes releases the GIL inside
+    # every call), end bit-identical to one plan stepped alone, decision by
+    # decision; one of the threads overflows on its second step and must be
+    # the only one that skips
+    import threading
+    dev = torch.device("cuda")
+    n, part, steps, rank = 4, 3 * TILE + 40, 3, 1
+    hp = (1e-3, .9, .999, 1e-8, 0.01, 1, 1024.0, 0.05)
+
+    def inputs(inject):
+        sl = [[synth.grad_slice(part, 0, 1e-3, 1024.0, 5, s + 1, j, rank, dev) for j in range(n)]
+              for s in range(steps)]
+        if inject:
+            sl[1][2][77] = float("inf")
+        return sl
+
+    def state():
+        return dict(g=torch.empty(part, device=dev), w=synth.master_init(part, 0.02, 5, rank, dev),
+                    m=torch.zeros(part, device=dev), v=torch.zeros(part, device=dev),
+                    p=torch.zeros(n * part, dtype=torch.float16, device=dev))
+
+    def run(plan, sl, st, stream, out, errors):
+        try:
+            scale = hp[6]
+            dec = []
+            for s in range(steps):
+                plan.reduce(rank, sl[s], st["g"], scale, stream=stream)
+                plan.adam(rank, st["g"], st["w"], st["m"], st["v"], st["p"], *hp[:6], scale, hp[7],
+                          stream=stream)
+                r = plan.result()
+                dec.append(r)
+                scale = r["loss_scale"]
+            out.extend(dec)
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    cases = [False, True, False]          # the second thread's plan overflows
+    plans = [_plan(n * part, n, 0, stage=2) for _ in cases]
+    sls = [inputs(inj) for inj in cases]
+    sts = [state() for _ in cases]
+    streams = [torch.cuda.Stream() for _ in cases]
+    outs = [[] for _ in cases]
+    errors = []
+    torch.cuda.synchronize()
+    threads = [threading.Thread(target=run, args=(plans[i], sls[i], sts[i], streams[i], outs[i], errors))
+               for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for inj in (False, True):             # the same step alone, one plan, one thread
+        ref_plan, ref_st, ref_out, ref_err = _plan(n * part, n, 0, stage=2), state(), [], []
+        run(ref_plan, inputs(inj), ref_st, torch.cuda.current_stream(), ref_out, ref_err)
+        assert not ref_err, ref_err
+        torch.cuda.synchronize()
+        for i, c in enumerate(cases):
+            if c != inj:
+                continue
+            assert [d["skipped"] for d in outs[i]] == ([0, 1, 0] if inj else [0, 0, 0])
+            for a, b in zip(outs[i], ref_out):
+                assert np.float64(a["norm"]).tobytes() == np.float64(b["norm"]).tobytes()
+                assert {k: a[k] for k in a if k != "norm"} == {k: b[k] for k in b if k != "norm"}
+            for k in ("w", "m", "v", "p"):
+                assert torch.equal(sts[i][k].view(torch.int32 if k != "p" else torch.int16),
+                                   ref_st[k].view(torch.int32 if k != "p" else torch.int16)), (i, k)
+        ref_plan.close()
+    # the steps did update the state
+    assert not torch.equal(sts[0]["w"], synth.master_init(part, 0.02, 5, rank, dev))
+    for p in plans:
+        p.close()
+
+
 @pytest.mark.parametrize("n,lp,bucket", [(2, 0, 0), (3, 1, 4096), (8, 0, 1000), (64, 1, 200_000),
                                          (5, 0, 8)])
 def test_allgather_params_buckets(zlib, n, lp, bucket):

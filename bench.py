@@ -63,6 +63,9 @@ def parse_args():
     ap.add_argument("--dist-backend", choices=["nccl", "gloo"], default="nccl",
                     help="torch.distributed backend under torchrun (gloo: host-staged exchange, "
                          "e.g. several processes on one GPU)")
+    ap.add_argument("--one-job", action="store_true",
+                    help="take the multi-rank path (statistics exported, all-reduced and decided "
+                         "from the sum) even in a world of one process")
     return ap.parse_args()
 
 
@@ -263,16 +266,26 @@ class Run:
         return int(sum(c.nbytes for c in self.calls(torch.cuda.current_stream())))
 
 
-def dist_setup(n_gpus, backend="nccl"):
+def dist_setup(n_gpus, backend="nccl", force=False):
     """(world size, rank, device index, torch.distributed or None).  One process
     per GPU; with fewer visible GPUs than local ranks (a gloo run of several
-    processes on one GPU) the ranks share devices round-robin."""
+    processes on one GPU) the ranks share devices round-robin.  force: a
+    process group even for a world of one (outside torchrun: 127.0.0.1 on a
+    free port)."""
     import torch
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if ws > 1:
+    if ws > 1 or force:
+        import socket
         import torch.distributed as dist
+        if "MASTER_PORT" not in os.environ:
+            with socket.socket() as s:
+                s.bind(("127.0.0.1", 0))
+                os.environ["MASTER_PORT"] = str(s.getsockname()[1])
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("RANK", str(rank))
+        os.environ.setdefault("WORLD_SIZE", str(ws))
         dev = local % max(1, torch.cuda.device_count())
         torch.cuda.set_device(dev)
         if backend == "nccl":
@@ -426,7 +439,7 @@ def main():
     import zero_partitioned_mixed_flat_gb300 as Z
     from zero_partitioned_mixed_flat_gb300.workloads import WORKLOADS
     Z.load()
-    ws, rank, local, dist = dist_setup(args.gpus, args.dist_backend)
+    ws, rank, local, dist = dist_setup(args.gpus, args.dist_backend, force=args.one_job)
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
     if args.n_ranks:
@@ -448,7 +461,7 @@ def main():
     # (configs that update every partition on one GPU) each GPU runs its own
     # replica of the job.
     per = len(w.ranks)
-    one_job = ws > 1 and ws * per <= w.n_ranks
+    one_job = (ws > 1 or args.one_job) and ws * per <= w.n_ranks
     if one_job:
         part_ranks = [rank * per + i for i in range(per)]
     else:
@@ -660,10 +673,11 @@ def main():
                                  "inputs larger than L2 (%.1f GB touched per step vs 129 MB L2)"
                                  % (run.bytes_per_step() / 1e9),
                            "parallelism": ("dp%d job over %d GPUs: GPU k owns partitions %s of "
-                                           "it, step statistics all-reduced (nccl) before the "
+                                           "it, step statistics all-reduced (%s) before the "
                                            "decision; the other ranks' slices simulated on each "
                                            "GPU" % (w.n_ranks, ws, "k" if per == 1 else
-                                                    "k*%d..k*%d+%d" % (per, per, per - 1)))
+                                                    "k*%d..k*%d+%d" % (per, per, per - 1),
+                                                    dist.get_backend()))
                                           if run.bufs.group is not None else
                                           ("dp%d simulated on each GPU (ranks as device buffers)"
                                            % w.n_ranks) + (", one replica per GPU" if ws > 1 else "")},

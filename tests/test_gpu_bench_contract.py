@@ -67,3 +67,27 @@ def test_bench_one_job_over_two_ranks(zlib):
     assert d["gpu_launches"] == 3 * 4
     assert "exchange" in d["kernels"] and d["e2e"]["value"] > 0
     assert d["decision"]["skipped"] == 0 and d["decision"]["step"] == 3 + 3   # warm-up + timed
+
+
+def test_bench_one_job_nccl_world_of_one(zlib):
+    # the multi-GPU step's nccl exchange (statistics exported, all-reduced by
+    # nccl, decided from the sum) in a world of one process: the decision must
+    # be the one the local path takes, bit for bit, at one launch more per step
+    def bench(*extra):
+        cmd = [sys.executable, "bench.py", "--workload", "gpt2-xl-zero2", "--steps", "3", "--warmup",
+               "3", "--no-cpu-baseline", "--no-e2e", "--no-clocks"] + list(extra)
+        env = {k: v for k, v in os.environ.items()
+               if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+        r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900, env=env)
+        assert r.returncode == 0, r.stderr[-3000:]
+        lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+        assert len(lines) == 1
+        return json.loads(lines[0])
+
+    local, job = bench(), bench("--one-job", "--dist-backend", "nccl")
+    assert "job over 1 GPUs" in job["config"]["parallelism"] and "(nccl)" in job["config"]["parallelism"]
+    assert job["n_gpus"] == 1 and job["value"] > 0
+    assert "exchange" in job["kernels"] and "exchange" not in local["kernels"]
+    assert local["gpu_launches"] == 3 * 3 and job["gpu_launches"] == 3 * 4
+    assert job["decision"] == local["decision"]
+    assert job["decision"]["step"] == 3 + 3

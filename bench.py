@@ -73,6 +73,18 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+def emit(line):
+    """Print the JSON line as the last line of stdout: first write out what C
+    libraries left in the C stdio buffer (nccl prints its version banner there
+    at the first collective), then the line."""
+    import ctypes
+    try:
+        ctypes.CDLL(None).fflush(None)
+    except (OSError, AttributeError):
+        pass
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- byte model
 
 def bytes_per_element(n_ranks: int):
@@ -427,7 +439,7 @@ def run_reference(args):
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+    emit(line)
     return 0
 
 
@@ -687,7 +699,7 @@ def main():
                 "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
                 "gpu_launches": run.launches_per_step() * K,
                 "decision": res, "graph": graph_info}
-        print(json.dumps(line), flush=True)
+        emit(line)
     if dist:
         dist.barrier()
         dist.destroy_process_group()

@@ -82,6 +82,7 @@ def test_bench_one_job_nccl_world_of_one(zlib):
         assert r.returncode == 0, r.stderr[-3000:]
         lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
         assert len(lines) == 1
+        assert r.stdout.strip().splitlines()[-1] == lines[0]   # nccl's banner comes before it
         return json.loads(lines[0])
 
     local, job = bench(), bench("--one-job", "--dist-backend", "nccl")

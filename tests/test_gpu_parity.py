@@ -139,12 +139,18 @@ def test_ddp_replica_equals_sharded_step(zlib):
     dict(bucket_elems=40_000),                             # several buckets
     dict(reduce_lp_accum=True),                            # fp16 reduce dtype
     dict(reduce_lp_accum=True, lp=1, loss_scale=1.0, grads_times_scale=False),
+    dict(growth_interval=2, steps=5),                      # the scale doubles every 2 good steps
+    dict(growth_interval=3, inject_inf_step=2, steps=6),   # a skip restarts the good-step count
+    dict(growth_interval=0, inject_inf_step=2, steps=3),   # static scale: a skip keeps it
 ])
 def test_tiny_variants(zlib, kw):
     h = Harness(_tiny(**kw))
-    for _ in range(2):
-        h.step()
+    scales = [h.step()["gpu"]["loss_scale"] for _ in range(kw.get("steps", 2))]
     h.close()
+    if "growth_interval" in kw:   # the scale after each step (from 1024)
+        expect = {2: [1024, 2048, 2048, 4096, 4096], 3: [1024, 512, 512, 512, 1024, 1024],
+                  0: [1024, 1024, 1024]}[kw["growth_interval"]]
+        assert scales == expect, scales
 
 
 def test_all_ranks_of_a_maximal_plan_in_one_step(zlib):

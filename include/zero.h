@@ -110,8 +110,9 @@ zero_status zero_plan_create(int64_t psi, int32_t n_ranks,
                              const int32_t *unit_of_tensor, zero_lp lp,
                              zero_plan **out);
 
-/* Padded length Ψ_p, partition length P, and (nullable, n_tensors entries)
- * the flat offset of each tensor.  Host only. */
+/* Padded length Ψ_p, partition length P, and (nullable) the flat offset of
+ * each tensor: n_tensors entries, or one entry (0) for a plan created from psi
+ * alone, whose buffer is one tensor.  Host only. */
 zero_status zero_plan_query(const zero_plan *plan, int64_t *psi_padded,
                             int64_t *part_len, int64_t *tensor_offsets);
 

@@ -473,8 +473,9 @@ zero_status zero_memory_report(int64_t psi, int32_t n_ranks, int32_t align,
                                double formula_bytes[4], int64_t actual_bytes[4],
                                int64_t comm_elems[4]);
 
-/* Frees the plan and its device scratch (synchronises the device first if
- * scratch was allocated).  NULL is allowed. */
+/* Frees the plan and its device scratch, after waiting for the plan's own
+ * device work (the whole device once one of its calls was captured into a
+ * graph).  NULL is allowed. */
 void zero_plan_destroy(zero_plan *plan);
 
 /* Message for the last failing call on this thread ("" if none). */
